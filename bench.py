@@ -1,0 +1,502 @@
+#!/usr/bin/env python3
+"""Benchmark of the hybrid-tree verify step on one or more GPUs.
+
+One step = graft_build_tree (prune, retrieve, merge) + graft_tree_attention
+for every layer + graft_accept_compact + graft_update_M, on synthetic inputs
+resident in HBM, replayed from one CUDA graph.  Default workload: the
+LLaMA-3-8B-shaped verify step (batch 1, 32 layers, 32/8 heads, prefix 4096,
+Kmax 64, vocab 128256, M 128256x16).
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs an
+independent replica of the step on its own GPU (no collective on the data
+path); ``value`` is the steps all ranks completed divided by the slowest
+rank's time.
+
+``--impl reference`` times the CPU oracle (a plain NumPy restatement of the
+method) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify steps/s; tree-attention HBM GB/s vs GB300 peak; retrieval fill µs"
+UNIT = "steps/s"
+FALLBACK_HBM_GBS = 6800.0
+ATTN_SOURCES = ["attention_mma.cu", "attention.cuh", "attention_api.cu"]
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["graft", "reference"], default="graft")
+    p.add_argument("--workload", default="llama3_8b")
+    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-budget-s", type=float, default=20.0)
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "--query-gpu=" + self.QUERY, "--format=csv,noheader,nounits",
+                                          "-i", self.gpu, "-lms", "100"], stdout=subprocess.PIPE,
+                                         stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=5)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def attn_source_hash() -> str:
+    h = hashlib.sha256()
+    for fn in ATTN_SOURCES:
+        with open(os.path.join(ROOT, "tree_verification_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per attention call from the committed ncu summary, if it matches this kernel source."""
+    path = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        ent = j.get(workload)
+        if ent and ent.get("source_hash") == attn_source_hash():
+            return float(ent["dram_bytes_per_call"])
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads", 0) for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------------------------
+# CPU oracle timing (the reference arm and the cpu_baseline leg)
+# ----------------------------------------------------------------------------------------------
+
+class OracleSample:
+    """The oracle's step on host copies of a workload's inputs, timed piecewise.
+
+    A sample runs the whole tree build, acceptance and M update for the
+    sampled requests, the attention of one layer on ``attn_kv_heads`` KV
+    heads, and the compaction of one layer; the step time is extrapolated to
+    every request, KV head and layer.
+    """
+
+    def __init__(self, wl, inputs, max_requests=4):
+        import numpy as np
+        from oracle import config as oconfig
+        self.np = np
+        self.wl = wl
+        self.cfg = oconfig.make_config(Kmax=wl.Kmax, D=wl.D, k=wl.k, V=wl.V, W=wl.W, checkpoints=wl.checkpoints,
+                                       tau=wl.tau)
+        self.reqs = list(range(min(wl.B, max_requests)))
+        dl, tl, roots, L, succ, cnt, layer0 = inputs
+        self.dl = dl[self.reqs].float().cpu().numpy()
+        self.tl = tl[self.reqs].cpu().numpy()
+        self.roots = roots[self.reqs].cpu().numpy()
+        self.L = L[self.reqs].cpu().numpy()
+        self.succ = succ.cpu().numpy()
+        self.cnt = cnt.cpu().numpy()
+        Q, Kc, Vc, Kt, Vt = layer0
+        r = self.reqs
+        self.Q = Q[r].float().cpu().numpy()
+        self.Kc = Kc[r].float().cpu().numpy()
+        self.Vc = Vc[r].float().cpu().numpy()
+        self.Kt = Kt[r].float().cpu().numpy()
+        self.Vt = Vt[r].float().cpu().numpy()
+
+    def step(self, attn_kv_heads: int):
+        """Run one sampled step; returns (extrapolated seconds, seconds actually spent)."""
+        np = self.np
+        from oracle import accept as oacc
+        from oracle import attention as oatt
+        from oracle import tree as otree
+        from oracle import update_m as oupd
+        wl, cfg = self.wl, self.cfg
+        t0 = time.perf_counter()
+        tree = otree.build_tree_batch(self.dl, self.roots, self.succ, self.L, cfg)
+        t1 = time.perf_counter()
+        group = wl.Hq // wl.Hkv
+        heads = list(range(attn_kv_heads * group))
+        for b in range(len(self.reqs)):
+            lb = int(self.L[b])
+            oatt.tree_attention_one(self.Q[b], self.Kc[b, :lb], self.Vc[b, :lb], self.Kt[b], self.Vt[b], lb,
+                                    tree["mask"][b], 1 / math.sqrt(wl.head_dim), heads=heads)
+        t2 = time.perf_counter()
+        a = oacc.accept_batch(self.tl, tree)
+        Kc, Vc = self.Kc.copy(), self.Vc.copy()
+        oacc.compact(Kc, Vc, self.Kt, self.Vt, self.L.astype(np.int64), a["path"], a["acc_len"])
+        t3 = time.perf_counter()
+        oupd.update_M(self.succ, self.cnt, tree["tok"].reshape(-1), a["argmax"].reshape(-1))
+        t4 = time.perf_counter()
+        scale_req = wl.B / len(self.reqs)
+        attn = (t2 - t1) * (wl.Hkv / attn_kv_heads) * wl.n_layers
+        est = (t1 - t0) * scale_req + attn * scale_req + (t3 - t2) * scale_req + (t4 - t3) * scale_req
+        return est, t4 - t0
+
+    def describe(self, attn_kv_heads, n_steps):
+        return (f"oracle (NumPy, float64 attention) on {len(self.reqs)} of {self.wl.B} requests: full tree build, "
+                f"acceptance, compaction of one layer and M update; attention of layer 0 on {attn_kv_heads} of "
+                f"{self.wl.Hkv} KV heads; extrapolated to all requests, heads and {self.wl.n_layers} layers; "
+                f"{n_steps} sampled steps")
+
+
+def oracle_timing(wl, inputs, budget_s: float, n_steps: int):
+    samp = OracleSample(wl, inputs)
+    est, spent = samp.step(1)  # one untimed pass sizes the sample
+    kvh = wl.Hkv
+    per = spent * max(1, wl.Hkv)  # rough cost of a step with every KV head
+    if per * n_steps > budget_s:
+        kvh = 1
+    ests = []
+    t_start = time.perf_counter()
+    for _ in range(n_steps):
+        e, _ = samp.step(kvh)
+        ests.append(e)
+        if time.perf_counter() - t_start > budget_s:
+            break
+    value = len(ests) / sum(ests)
+    return value, samp.describe(kvh, len(ests))
+
+
+# ----------------------------------------------------------------------------------------------
+# GPU arm
+# ----------------------------------------------------------------------------------------------
+
+def make_inputs(wl, dev, gb, synth):
+    import torch
+    cfg = gb.graft_config_init(wl.Kmax, wl.D, wl.k, wl.V, wl.W, list(wl.checkpoints), wl.tau)
+    Lcap = wl.lcap(1)
+    dl = synth.draft_logits(wl, dev)
+    roots = synth.root_tokens(wl).to(dev)
+    L0 = synth.prefix_lengths(wl).to(dev)
+    if wl.M_init == "zipf":
+        s, c = synth.zipf_M(wl.V, wl.W, wl.seed + 5)
+    else:
+        s, c = synth.empty_M(wl.V, wl.W)
+    M_succ, M_cnt = torch.from_numpy(s).to(dev), torch.from_numpy(c).to(dev)
+    if wl.M_init == "warm":
+        src, dst = synth.stream_pairs(synth.token_stream(wl.Lmax, wl.V, wl.seed + 41))
+        sd, dd = torch.from_numpy(src).to(dev), torch.from_numpy(dst).to(dev)
+        for _ in range(5):
+            gb.graft_update_M(M_succ, M_cnt, sd, dd)
+    layers = [synth.layer_tensors(wl, l, dev, Lcap=Lcap) for l in range(wl.n_layers)]
+    tl = synth.target_logits(wl, dev)
+    tree = gb.graft_build_tree(cfg, dl, roots, M_succ, L0)
+    torch.cuda.synchronize()
+    synth.plant_paths(tl, tree["tok"].cpu().numpy(), tree["parent"].cpu().numpy(), tree["depth"].cpu().numpy(),
+                      synth.planted_lengths(wl))
+    return cfg, Lcap, dl, roots, L0, M_succ, M_cnt, layers, tl
+
+
+def attention_bytes_per_call(wl, L0) -> float:
+    """Compulsory bytes of one layer call: prefix K and V, tree K and V, Q in, O out (bf16)."""
+    d = wl.head_dim
+    prefix = 2 * int(L0.sum()) * wl.Hkv * d * 2
+    tree_kv = 2 * wl.B * wl.Kmax * wl.Hkv * d * 2
+    q_o = 2 * wl.B * wl.Kmax * wl.Hq * d * 2
+    return float(prefix + tree_kv + q_o)
+
+
+def run_graft(args):
+    import torch
+    import torch.distributed as dist
+    from tree_verification_gb300 import _build, synth
+    from tree_verification_gb300 import binding as gb
+    from tree_verification_gb300.step import VerifyStep
+
+    world, rank, local = dist_env()
+    if world > 1:
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    _build.build()
+    wl = synth.WORKLOADS[args.workload]
+    cfg, Lcap, dl, roots, L0, M_succ, M_cnt, layers, tl = make_inputs(wl, dev, gb, synth)
+    Q = [x[0] for x in layers]
+    step = VerifyStep(cfg, wl.B, wl.Hq, wl.Hkv, wl.n_layers, Lcap, dev, [x[1] for x in layers],
+                      [x[2] for x in layers], [x[3] for x in layers], [x[4] for x in layers])
+    L = L0.clone()
+
+    def body():
+        L.copy_(L0)
+        step.run(dl, roots, M_succ, M_cnt, L, Q, tl)
+
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        body()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    n0 = gb.graft_launch_count()
+    with torch.cuda.graph(graph):
+        body()
+    launches_per_step = gb.graft_launch_count() - n0
+
+    # attention alone (every layer call of a step), for the roofline
+    attn_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(attn_graph):
+        for l in range(wl.n_layers):
+            gb.graft_tree_attention(Q[l], step.Kc[l], step.Vc[l], step.Kt[l], step.Vt[l], L0, step.tree["mask"],
+                                    step.scale, O=step.O, status=step.status, ws=step.ws_attn)
+    # retrieval fill alone and the whole tree build
+    n_rep = 100
+    ret_out = torch.empty(wl.B, max(1, cfg.n_tmpl), dtype=torch.int32, device=dev)
+    ret_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ret_graph):
+        for _ in range(n_rep):
+            gb.graft_retrieve(cfg, roots, M_succ, ret_tok=ret_out)
+    tree_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(tree_graph):
+        for _ in range(n_rep):
+            gb.graft_build_tree(cfg, dl, roots, M_succ, L0, out=step.tree, ws=step.ws_tree)
+
+    def timed(g, reps):
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        s.record()
+        for _ in range(reps):
+            g.replay()
+        e.record()
+        e.synchronize()
+        return s.elapsed_time(e) / 1000.0
+
+    for _ in range(max(3, args.warmup)):
+        graph.replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    ids = [x for x in vis.split(",") if x.strip()]
+    sampler = ClockSampler(ids[local] if local < len(ids) else str(local))
+    sampler.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t_main = timed(graph, args.steps)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    t_max = t_main
+    if world > 1:
+        t = torch.tensor([t_main], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_max = float(t.item())
+    status = int(step.status.item())
+
+    # secondary timings (after the main timed region)
+    reps_attn = max(20, min(args.steps, 300))
+    t_attn = timed(attn_graph, reps_attn) / (reps_attn * wl.n_layers)
+    t_ret = timed(ret_graph, 20) / (20 * n_rep)
+    t_tree = timed(tree_graph, 20) / (20 * n_rep)
+
+    # end-to-end through the public step API: pinned host inputs copied in, results read back every step
+    host = {"dl": dl, "tl": tl, "roots": roots, "L0": L0}
+    for l in range(wl.n_layers):
+        host[f"Q{l}"], host[f"Kt{l}"], host[f"Vt{l}"] = Q[l], step.Kt[l], step.Vt[l]
+    pinned = {k: v.cpu().pin_memory() for k, v in host.items()}
+    out_host = torch.empty(wl.B, wl.Kmax, dtype=torch.int32).pin_memory()
+    len_host = torch.empty(wl.B, dtype=torch.int32).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out_host.numel() * 4 + len_host.numel() * 4
+
+    def e2e_step():
+        for k, v in host.items():
+            v.copy_(pinned[k], non_blocking=True)
+        graph.replay()
+        out_host.copy_(step.acc["out_tok"], non_blocking=True)
+        len_host.copy_(step.acc["acc_len"], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    n_e2e = max(10, min(args.e2e_steps, args.steps))
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    t_e2e = time.perf_counter() - t0
+    if world > 1:
+        t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        t_e2e = float(t.item())
+
+    bytes_call = attention_bytes_per_call(wl, L0.cpu())
+    peak, peak_kind = measured_peaks()
+    achieved = bytes_call / t_attn / 1e9
+    traffic = recorded_traffic(args.workload)
+    result = {
+        "metric": METRIC, "value": world * args.steps / t_max, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1000.0 * t_max / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.B, "layers": wl.n_layers, "heads_q_kv": [wl.Hq, wl.Hkv],
+                   "head_dim": wl.head_dim, "prefix": list(wl.L), "Kmax": wl.Kmax, "draft_depth_topk": [wl.D, wl.k],
+                   "vocab": wl.V, "M_width": wl.W, "tau": wl.tau, "checkpoints": list(wl.checkpoints),
+                   "l2": f"inputs larger than L2: {bytes_call * wl.n_layers / 1e6:.0f} MB of attention operands "
+                         f"per step in distinct per-layer buffers",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "accumulate": "fp32"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "kernel": "graft_tree_attention (one layer call)",
+                     "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_call": bytes_call,
+                     "call_us": t_attn * 1e6},
+        "e2e": {"value": world * n_e2e / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "secondary": {"tree_attention_gbs": achieved, "tree_attention_frac_of_peak": achieved / peak,
+                      "retrieval_fill_us": t_ret * 1e6, "build_tree_us": t_tree * 1e6,
+                      "launches_per_step": launches_per_step, "device_status": status},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        inputs = (dl, tl, roots, L0, M_succ, M_cnt, layers[0])
+        v, desc = oracle_timing(wl, inputs, args.cpu_budget_s, n_steps=50)
+        result["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+                                  "sample": desc}
+    if rank == 0:
+        print(json.dumps(result), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_reference(args):
+    import torch
+    from tree_verification_gb300 import _build, synth
+    from tree_verification_gb300 import binding as gb
+
+    world, rank, local = dist_env()
+    if rank != 0:
+        return  # the reference arm runs once, on rank 0
+    wl = synth.WORKLOADS[args.workload]
+    # inputs are drawn exactly as the GPU arm draws them (on the GPU when one is present)
+    if torch.cuda.is_available():
+        dev = torch.device(f"cuda:{local}")
+        torch.cuda.set_device(dev)
+        _build.build()
+        cfg, Lcap, dl, roots, L0, M_succ, M_cnt, layers, tl = make_inputs(wl.scaled(n_layers=1), dev, gb, synth)
+        inputs = (dl, tl, roots, L0, M_succ, M_cnt, layers[0])
+    else:
+        dev = torch.device("cpu")
+        small = wl
+        Lcap = wl.lcap(1)
+        s, c = synth.empty_M(wl.V, wl.W) if wl.M_init != "zipf" else synth.zipf_M(wl.V, wl.W, wl.seed + 5)
+        inputs = (synth.draft_logits(small, dev), synth.target_logits(small, dev), synth.root_tokens(small),
+                  synth.prefix_lengths(small), torch.from_numpy(s), torch.from_numpy(c),
+                  synth.layer_tensors(small, 0, dev, Lcap=Lcap))
+    samp = OracleSample(wl, inputs)
+    for _ in range(max(0, min(args.warmup, 3))):
+        samp.step(1)
+    budget = 150.0
+    _, spent = samp.step(1)
+    n_run = max(1, min(args.steps, int(budget / max(spent, 1e-3))))
+    ests = [samp.step(1)[0] for _ in range(n_run)]
+    value = len(ests) / sum(ests)
+    desc = samp.describe(1, n_run) + f" (of {args.steps} requested steps, bounded to about {budget:.0f} s)"
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / value, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": wl.name, "batch": wl.B, "layers": wl.n_layers, "prefix": list(wl.L),
+                      "Kmax": wl.Kmax, "vocab": wl.V},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_graft(args)
+
+
+if __name__ == "__main__":
+    main()

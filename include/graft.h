@@ -1,0 +1,250 @@
+/*
+ * graft.h — C ABI of the GB300 hybrid-tree verify-step library (libgraft.so).
+ *
+ * The library computes one verify step of hybrid-tree speculative decoding
+ * as described by "Draft Less, Retrieve More: Hybrid Tree Construction for
+ * Speculative Decoding" (the aitrends.kr article on it, cited below as the
+ * Graft article, and the chatpaper.ai abstract, cited as the Graft
+ * abstract):
+ *
+ *   graft_build_tree      prune the draft, fill the retrieval template from M
+ *                         and merge both into one Kmax-node tree
+ *   graft_retrieve        the retrieval fill alone
+ *   graft_tree_attention  tree-masked GQA attention for one layer
+ *   graft_accept_compact  greedy longest accepted path, KV compaction
+ *   graft_update_M        online update of the adjacency table M
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor argument is a caller-owned DEVICE pointer unless marked
+ *   "host".  The library never allocates, frees or retains memory: scratch
+ *   space comes from a caller buffer `ws` of at least the size the matching
+ *   *_workspace_size function reports (pointer aligned to 256 bytes).
+ * - Every call is asynchronous on the caller's CUDA stream (`stream`, a
+ *   cudaStream_t; NULL is the legacy default stream).  A return value of
+ *   GRAFT_OK means the work was enqueued.
+ * - Arguments are validated on the host before any launch; an invalid call
+ *   returns a negative code and enqueues nothing.  Errors that depend on
+ *   device data (token ids out of range, a cache that would overflow) are
+ *   OR-ed as GRAFT_STATUS_* bits into the caller's device word `status`
+ *   (may be NULL to ignore them), readable after the stream synchronises.
+ * - bf16 tensors are IEEE bfloat16 stored as 16-bit words; all layouts are
+ *   dense row-major in the order written, with no padding.
+ * - Token ids are int32 in [0, V).  Node indices are int32 in [0, Kmax).
+ */
+#ifndef GRAFT_H_
+#define GRAFT_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t, spelled without including CUDA headers. */
+typedef struct CUstream_st* graft_stream_t;
+
+/* Return codes. */
+#define GRAFT_OK 0
+#define GRAFT_ERR_INVALID_ARG (-1)      /* null pointer, negative size, inconsistent config */
+#define GRAFT_ERR_UNSUPPORTED_SHAPE (-2) /* a size outside what the kernels handle (limits below) */
+#define GRAFT_ERR_WORKSPACE (-3)        /* ws missing, too small or misaligned */
+#define GRAFT_ERR_CUDA (-4)             /* a CUDA launch or device query failed */
+
+/* Device status bits, OR-ed into *status by the kernels. */
+#define GRAFT_STATUS_TOKEN_RANGE 1    /* a token id outside [0, V) was read; the node became a pad / the pair was skipped */
+#define GRAFT_STATUS_CACHE_OVERFLOW 2 /* L[b] + accepted length > Lcap; that request was not compacted */
+#define GRAFT_STATUS_LENGTH 4         /* L[b] < 0 or L[b] > Lcap; that request was skipped */
+#define GRAFT_STATUS_TREE 8           /* a kept draft node's parent was not kept (cannot happen for finite logits) */
+
+/* Limits. */
+#define GRAFT_MAX_KMAX 64        /* tree nodes per request (one uint64 ancestor mask) */
+#define GRAFT_MAX_CHECKPOINTS 4  /* pruning checkpoints */
+#define GRAFT_MAX_TOPK 16        /* draft branching k */
+#define GRAFT_MAX_DEPTH 16       /* drafter calls D */
+#define GRAFT_MAX_W 32           /* successors per row of M */
+#define GRAFT_HEAD_DIM 128       /* the only head size the attention kernel supports */
+
+/*
+ * GraftConfig — the method's parameters (host struct, passed by pointer).
+ *
+ * Graft article, method paragraph (first point) and architecture paragraph:
+ * pruning tests a per-depth confidence c_d against a threshold tau_d at
+ * checkpoints d0, d1, d5, and each stage s splits the budget as
+ * Kmax = K_draft_s + K_ret_s, a smaller s giving retrieval more; the
+ * retrieval templates G_ret_s are per-stage prefixes of one envelope.
+ *
+ *   Kmax            tree nodes per request, root included (1..64)
+ *   D, k            drafter calls and top-k branching of the draft tree
+ *   V               vocabulary size; W successors per row of M
+ *   n_checkpoints   number of pruning checkpoints (0..4)
+ *   checkpoint[s]   drafter call (0-based) after which c is tested; strictly increasing, < D
+ *   tau[s]          threshold: drafting stops at the first s with c_{checkpoint[s]} < tau[s]
+ *   K_draft[s]      draft nodes kept (root included) when stopped at s;
+ *                   K_draft[n_checkpoints] is the unpruned stage and must equal Kmax
+ *   n_tmpl          envelope size = max_s (Kmax - K_draft[s])
+ *   tmpl_parent[j]  parent of envelope node j: -1 = the root, else an index < j
+ *   tmpl_rank[j]    rank (0..W-1) of node j among its parent token's successors in M
+ */
+typedef struct GraftConfig {
+    int32_t Kmax, D, k, V, W;
+    int32_t n_checkpoints;
+    int32_t checkpoint[GRAFT_MAX_CHECKPOINTS];
+    float tau[GRAFT_MAX_CHECKPOINTS];
+    int32_t K_draft[GRAFT_MAX_CHECKPOINTS + 1];
+    int32_t n_tmpl;
+    int32_t tmpl_parent[GRAFT_MAX_KMAX];
+    int32_t tmpl_rank[GRAFT_MAX_KMAX];
+} GraftConfig;
+
+/*
+ * graft_config_init — fill *cfg (host) with the default budget split and
+ * retrieval envelope for the given sizes.  Checkpoints >= D are dropped.
+ *   K_draft[s] = 1 + min(k + d_s k^2, floor((Kmax - 1)(d_s + 1) / D)), K_draft[last] = Kmax;
+ *   envelope = rank paths (r_1..r_m), m <= D, r_i < W, ordered by
+ *   (prod(r_i + 1), m, lexicographic), first n_tmpl of them.
+ * Host only; no CUDA call.  Returns GRAFT_ERR_INVALID_ARG /
+ * GRAFT_ERR_UNSUPPORTED_SHAPE for sizes outside the limits or a draft too
+ * small to fill Kmax.
+ */
+int graft_config_init(GraftConfig* cfg, int Kmax, int D, int k, int V, int W,
+                      int n_checkpoints, const int32_t* checkpoints /* host */,
+                      const float* tau /* host */);
+
+/* graft_config_validate — check a (possibly hand-edited) config. Host only. */
+int graft_config_validate(const GraftConfig* cfg);
+
+/*
+ * graft_build_tree — stages 1 to 3 of the step for B requests
+ * (Graft article, step summary and method paragraph, first three points;
+ * Graft abstract: "prune-then-graft").
+ *
+ *   draft_logits [B][D][k][V] f32  drafter logits; row (b, d, f) belongs to
+ *                                  the f-th frontier node of drafter call d
+ *                                  (call 0 reads only slot f = 0, the root).
+ *                                  Rows past the pruning point are not read.
+ *   root_tok [B] i32               last emitted token of each request
+ *   M_succ [V][W] i32              successor table (-1 = empty slot)
+ *   L [B] i32                      tokens already in each request's KV cache
+ * Outputs, [B][Kmax] unless noted:
+ *   tree_tok, tree_parent (root -1), tree_depth, tree_pos (= L[b] + depth) i32,
+ *   tree_mask u64 (bit j of node i set iff j is i or an ancestor of i),
+ *   stage [B] i32 (pruning stage; n_checkpoints = not pruned).
+ * Tree order: root; kept draft nodes by (depth asc, score desc); then the
+ * stage's first K_ret envelope nodes (empty M slots give pad token 0).
+ * Workspace: graft_build_tree_workspace_size.
+ */
+int graft_build_tree_workspace_size(const GraftConfig* cfg, int B, size_t* bytes);
+int graft_build_tree(const GraftConfig* cfg, int B, const float* draft_logits,
+                     const int32_t* root_tok, const int32_t* M_succ, const int32_t* L,
+                     int32_t* tree_tok, int32_t* tree_parent, int32_t* tree_depth,
+                     int32_t* tree_pos, uint64_t* tree_mask, int32_t* stage,
+                     int32_t* status, void* ws, size_t ws_bytes, graft_stream_t stream);
+
+/*
+ * graft_retrieve — the retrieval fill alone (Graft article, step summary:
+ * retrieval starts from the root token through the GPU-resident adjacency
+ * matrix; method paragraph, second point).
+ *   ret_tok [B][n_tmpl] i32: envelope node j's token = M_succ[parent token][tmpl_rank[j]],
+ *   -1 where the slot is empty or the parent is already -1.
+ * No workspace.
+ */
+int graft_retrieve(const GraftConfig* cfg, int B, const int32_t* root_tok, const int32_t* M_succ,
+                   int32_t* ret_tok, int32_t* status, graft_stream_t stream);
+
+/*
+ * graft_tree_attention — tree-masked GQA attention of one layer (Graft
+ * article, architecture paragraph: the hybrid tree is verified on the
+ * standard tree-attention path in one target forward).
+ *
+ *   Q  [B][Kmax][Hq][128] bf16     queries of the tree nodes (rotary already applied)
+ *   Kc, Vc [B][Lcap][Hkv][128] bf16 this layer's KV cache; rows 0..L[b]-1 are read
+ *   Kt, Vt [B][Kmax][Hkv][128] bf16 the tree nodes' own KV
+ *   L [B] i32, tree_mask [B][Kmax] u64 as produced by graft_build_tree
+ *   O  [B][Kmax][Hq][128] bf16     output (round to nearest even)
+ * O[b,i,h] = softmax over {prefix keys 0..L[b]-1} U {tree keys j in mask[b][i]}
+ * of scale * q.k, applied to V; q head h uses KV head h / (Hq / Hkv).
+ * Float32 scores and accumulation.  Requires head_dim == 128, Hq % Hkv == 0,
+ * Kmax * Hq / Hkv <= 1024.  Workspace: graft_tree_attention_workspace_size
+ * (depends on the current device's SM count).
+ */
+int graft_tree_attention_workspace_size(int B, int Hq, int Hkv, int head_dim, int Kmax,
+                                        int64_t Lcap, size_t* bytes);
+int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Kmax, const void* Q,
+                         const void* Kc, const void* Vc, int64_t Lcap, const void* Kt,
+                         const void* Vt, const int32_t* L, const uint64_t* tree_mask,
+                         float scale, void* O, int32_t* status, void* ws, size_t ws_bytes,
+                         graft_stream_t stream);
+
+/*
+ * graft_accept_compact — greedy lossless acceptance and KV compaction
+ * (Graft article, architecture paragraph: retrieved nodes are ordinary
+ * proposals and the final distribution stays lossless).
+ *
+ *   target_logits [B][Kmax][V] f32 the target's logits at every tree node
+ *   tree_tok, tree_parent, tree_depth [B][Kmax] i32 from graft_build_tree
+ *   Kc_layers, Vc_layers  device arrays of n_layers device pointers, each a
+ *                         [B][Lcap][Hkv][head_dim] bf16 cache (written)
+ *   Kt_layers, Vt_layers  device arrays of n_layers device pointers, each a
+ *                         [B][Kmax][Hkv][head_dim] bf16 tree KV (read)
+ *   L [B] i32             in: cache lengths; out: L[b] + acc_len[b]
+ * Outputs: argmax [B][Kmax] (target argmax per node, ties to the lower id),
+ *   acc_len [B] (accepted path length, root included), path [B][Kmax]
+ *   (accepted node indices from the root, -1 past acc_len), out_tok [B][Kmax]
+ *   (emitted tokens: the path after the root then the bonus, -1 past
+ *   acc_len), bonus [B] (target argmax at the deepest accepted node).
+ * Node i is accepted iff every node on its root path carries the target's
+ * argmax at its parent; the deepest accepted node wins, lower index on ties.
+ * Cache row L[b] + t receives tree row path[b][t] for t < acc_len[b] in every
+ * layer.  A request whose cache would overflow sets
+ * GRAFT_STATUS_CACHE_OVERFLOW and is left uncompacted with L unchanged.
+ * Workspace: graft_accept_compact_workspace_size.
+ */
+int graft_accept_compact_workspace_size(int B, int Kmax, int V, size_t* bytes);
+int graft_accept_compact(int B, int Kmax, int V, int n_layers, const float* target_logits,
+                         const int32_t* tree_tok, const int32_t* tree_parent,
+                         const int32_t* tree_depth, void* const* Kc_layers,
+                         void* const* Vc_layers, const void* const* Kt_layers,
+                         const void* const* Vt_layers, int Hkv, int head_dim, int64_t Lcap,
+                         int32_t* L, int32_t* argmax, int32_t* acc_len, int32_t* path,
+                         int32_t* out_tok, int32_t* bonus, int32_t* status, void* ws,
+                         size_t ws_bytes, graft_stream_t stream);
+
+/*
+ * graft_update_M — online update of the adjacency table from verified
+ * pairs (Graft article, method paragraph, fourth point: M is updated
+ * continuously from the verified tree's logits).
+ *
+ *   M_succ, M_cnt [V][W] i32 (in place); row t ranks up to W successors of
+ *   token t by (count desc, token asc), empty slots (-1, 0) last.
+ *   src, dst [n] i32: the multiset of pairs (src -> dst) to add.
+ * Each pair already in its row adds 1 to that count (an atomic increment);
+ * new successors enter with their multiplicity; each touched row keeps its
+ * top W by (count desc, token asc).  The result depends only on the
+ * multiset, not on pair order, and is bit-exact.  Pairs with an id outside
+ * [0, V) are skipped and flagged.  Workspace: graft_update_M_workspace_size.
+ */
+int graft_update_M_workspace_size(int64_t n, size_t* bytes);
+int graft_update_M(int32_t* M_succ, int32_t* M_cnt, int V, int W, const int32_t* src,
+                   const int32_t* dst, int64_t n, int32_t* status, void* ws, size_t ws_bytes,
+                   graft_stream_t stream);
+
+/* Human-readable text for a return code (static string). */
+const char* graft_status_string(int code);
+
+/* Library version as an integer (major * 10000 + minor * 100 + patch). */
+int graft_version(void);
+
+/*
+ * graft_launch_count — number of kernel launches this process has enqueued
+ * through the library so far (host-side counter, all devices, all threads).
+ * Launches recorded into a CUDA graph count once, at capture time.
+ */
+uint64_t graft_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GRAFT_H_ */

@@ -1,0 +1,413 @@
+"""GPU parity: every stage of the CUDA path against the CPU oracle.
+
+Integer and index outputs (tree, stage, argmax, accepted path and tokens,
+compacted KV bytes, M) must match bit-exactly; attention must satisfy the
+tolerance in tests/helpers.py.  Inputs come from the seeded generators in
+tree_verification_gb300.synth and are copied to the host for the oracle.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import accept as oacc
+from oracle import attention as oatt
+from oracle import tree as otree
+from oracle import update_m as oupd
+from tests.helpers import MARGIN, assert_attention_close, gb, lib_cfg, mask_to_u64, oracle_cfg, to_np
+from tree_verification_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.fail("GPU tests need a CUDA device")
+    gb()
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device=DEV)
+
+
+def _M(wl, device=DEV):
+    if wl.M_init == "zipf":
+        s, c = synth.zipf_M(wl.V, wl.W, wl.seed + 5)
+    else:
+        s, c = synth.empty_M(wl.V, wl.W)
+    return torch.from_numpy(s).to(device), torch.from_numpy(c).to(device)
+
+
+def _oracle_tree(wl, cfg_o, dl_gpu, roots, succ_np, L):
+    """Oracle tree per request, reading drafter rows from the device lazily."""
+    out, margins = [], []
+    for b in range(wl.B):
+        rows = {}
+
+        def row_fn(d, f, _path, b=b):
+            key = (d, f)
+            if key not in rows:
+                rows[key] = dl_gpu[b, d, f].cpu().numpy()
+            return rows[key]
+
+        res = otree.draft_tree(row_fn, int(roots[b]), cfg_o)
+        nodes = otree.retained_draft(res, cfg_o)
+        ret = otree.retrieve(int(roots[b]), succ_np, cfg_o["tmpl_parent"], cfg_o["tmpl_rank"])
+        t = otree.merge(int(roots[b]), nodes, ret, cfg_o["tmpl_parent"], res.stage, int(L[b]), cfg_o)
+        out.append(t)
+        margins.append(otree.draft_margins(row_fn, int(roots[b]), cfg_o))
+    return out, margins
+
+
+def _compare_tree(gpu, trees):
+    tok, par, dep, pos = (to_np(gpu[k]) for k in ("tok", "parent", "depth", "pos"))
+    mask, stage = mask_to_u64(gpu["mask"]), to_np(gpu["stage"])
+    for b, t in enumerate(trees):
+        assert stage[b] == t.stage, f"request {b}: stage {stage[b]} vs {t.stage}"
+        assert tok[b].tolist() == t.tok, f"request {b}: tokens differ"
+        assert par[b].tolist() == t.parent and dep[b].tolist() == t.depth and pos[b].tolist() == t.pos
+        assert [int(x) for x in mask[b]] == t.mask
+
+
+def _build(wl, cfg, dl, roots, succ, L):
+    status = _status()
+    out = gb().graft_build_tree(cfg, dl, roots.to(DEV), succ, L.to(DEV), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b", "qwen3_8b_batch", "llama31_8b_long", "qwen3_235b"])
+def test_build_tree_parity(name):
+    wl = synth.WORKLOADS[name]
+    cfg, cfg_o = lib_cfg(wl), oracle_cfg(wl)
+    dl = synth.draft_logits(wl, DEV)
+    roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
+    if wl.M_init == "warm":
+        succ_np = _warm_M_oracle(wl)[0]
+        succ = torch.from_numpy(succ_np).to(DEV)
+    else:
+        succ, _ = _M(wl)
+        succ_np = succ.cpu().numpy()
+    gpu = _build(wl, cfg, dl, roots, succ, L)
+    trees, margins = _oracle_tree(wl, cfg_o, dl, roots, succ_np, L)
+    assert min(margins) > MARGIN
+    _compare_tree(gpu, trees)
+
+
+def _peaked_wl(V, B, seed):
+    return synth.WORKLOADS["llama3_8b"].scaled(V=V, B=B, seed=seed)
+
+
+@pytest.mark.parametrize("V,seed", [(4096, 1), (128256, 2)])
+def test_build_tree_all_stages(V, seed):
+    """Confident drafts reach every pruning stage, including the dense tree."""
+    wl = _peaked_wl(V, 12, seed)
+    boosts = [0.0, 10.0, 13.0, 14.0, 15.0, 16.0, 17.0, 18.0, 20.0, 22.0, 25.0, 30.0]
+    if V == 4096:
+        boosts = [b - math.log(128256 / 4096) for b in boosts]
+    cfg, cfg_o = lib_cfg(wl), oracle_cfg(wl)
+    dl = synth.peaked_draft_logits(wl, DEV, boosts, seed)
+    roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
+    s_np, _ = synth.zipf_M(wl.V, wl.W, seed)
+    succ = torch.from_numpy(s_np).to(DEV)
+    gpu = _build(wl, cfg, dl, roots, succ, L)
+    trees, margins = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
+    ok = [b for b in range(wl.B) if margins[b] > MARGIN]
+    assert len(ok) >= wl.B - 2, f"too many near-tie requests: {margins}"
+    stages = to_np(gpu["stage"])
+    _compare_tree({k: v[ok] for k, v in gpu.items()}, [trees[b] for b in ok])
+    assert {0, 1, 2, 3} <= {int(stages[b]) for b in ok}
+
+
+@pytest.mark.parametrize("tau", [0.0, 1.5])
+def test_build_tree_tau_extremes(tau):
+    wl = synth.WORKLOADS["tiny"].scaled(B=3, V=2048)
+    cfg, cfg_o = lib_cfg(wl, tau=tau), oracle_cfg(wl, tau=tau)
+    dl = synth.draft_logits(wl, DEV)
+    roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
+    s_np, _ = synth.zipf_M(wl.V, wl.W, 3)
+    succ = torch.from_numpy(s_np).to(DEV)
+    gpu = _build(wl, cfg, dl, roots, succ, L)
+    trees, margins = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
+    if tau == 0.0:
+        assert min(margins) > MARGIN
+    _compare_tree(gpu, trees)
+    assert set(to_np(gpu["stage"]).tolist()) == ({3} if tau == 0.0 else {0})
+
+
+def test_build_tree_single_node_and_empty_M():
+    wl = synth.WORKLOADS["tiny"].scaled(B=2, Kmax=1, V=1000)
+    cfg, cfg_o = lib_cfg(wl), oracle_cfg(wl)
+    dl = synth.draft_logits(wl, DEV)
+    roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
+    s_np, _ = synth.empty_M(wl.V, wl.W)
+    gpu = _build(wl, cfg, dl, roots, torch.from_numpy(s_np).to(DEV), L)
+    trees, _ = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
+    _compare_tree(gpu, trees)
+    wl2 = synth.WORKLOADS["tiny"].scaled(B=2, V=1000)
+    cfg2, cfg2_o = lib_cfg(wl2), oracle_cfg(wl2)
+    dl2 = synth.draft_logits(wl2, DEV)
+    gpu2 = _build(wl2, cfg2, dl2, roots, torch.from_numpy(s_np).to(DEV), L)
+    trees2, _ = _oracle_tree(wl2, cfg2_o, dl2, roots, s_np, L)
+    _compare_tree(gpu2, trees2)
+    assert all(t.tok[t.n_draft:] == [0] * (wl2.Kmax - t.n_draft) for t in trees2)
+
+
+def test_build_tree_zero_batch():
+    wl = synth.WORKLOADS["tiny"].scaled(B=0, V=1000)
+    cfg = lib_cfg(wl)
+    e = torch.empty(0, dtype=torch.int32, device=DEV)
+    out = gb().graft_build_tree(cfg, torch.empty(0, wl.D, wl.k, wl.V, device=DEV), e, _M(wl)[0], e)
+    assert out["tok"].shape == (0, wl.Kmax)
+
+
+@pytest.mark.parametrize("W,seed", [(1, 0), (8, 1), (16, 2), (32, 3)])
+def test_retrieve_parity(W, seed):
+    wl = synth.WORKLOADS["llama3_8b"].scaled(B=20, V=5000, W=W, D=8 if W > 1 else 8, Kmax=64 if W > 1 else 9)
+    cfg, cfg_o = lib_cfg(wl), oracle_cfg(wl)
+    rng = np.random.default_rng(seed)
+    succ = np.full((wl.V, W), -1, np.int32)
+    for t in range(wl.V):  # rows filled to a random depth: exercises pads and pad children
+        n = int(rng.integers(0, W + 1))
+        succ[t, :n] = rng.choice(wl.V, n, replace=False)
+    roots = torch.from_numpy(rng.integers(0, wl.V, wl.B).astype(np.int32))
+    roots[0] = 7
+    succ[7, :] = -1  # a root with an empty row: every envelope node is a pad
+    ret = gb().graft_retrieve(cfg, roots.to(DEV), torch.from_numpy(succ).to(DEV))
+    torch.cuda.synchronize()
+    got = to_np(ret)
+    for b in range(wl.B):
+        want = otree.retrieve(int(roots[b]), succ, cfg_o["tmpl_parent"], cfg_o["tmpl_rank"])
+        assert got[b].tolist() == want
+    assert (got[0] == -1).all()
+
+
+def _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed, layer=0):
+    wl = synth.WORKLOADS["llama3_8b"].scaled(B=B, Hq=Hq, Hkv=Hkv, Kmax=Kmax, seed=seed, L=(0, 0))
+    Q, Kc, Vc, Kt, Vt = synth.layer_tensors(wl, layer, DEV, Lcap=Lcap)
+    rng = np.random.default_rng(seed)
+    masks = np.zeros((B, Kmax), np.uint64)
+    for b in range(B):  # a random tree: parent uniformly among earlier nodes
+        m = [1]
+        for i in range(1, Kmax):
+            m.append(m[int(rng.integers(0, i))] | (1 << i))
+        masks[b] = np.array(m, dtype=np.uint64)
+    L = torch.tensor(Ls, dtype=torch.int32)
+    return Q, Kc, Vc, Kt, Vt, L, masks
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,Kmax,Ls,Lcap", [
+    (1, 8, 2, 32, [512], 576),                 # one 128-row block, one chunk
+    (3, 8, 2, 32, [0, 1, 1500], 1600),         # empty prefix, a single key, a ragged tail
+    (2, 32, 8, 64, [4096, 777], 4160),         # two row blocks, several chunks
+    (2, 64, 4, 64, [2000, 63], 2048),          # group 16: eight row blocks
+    (4, 16, 16, 5, [300, 64, 65, 129], 320),   # no grouping, Kmax not a multiple of 8
+    (1, 8, 1, 1, [999], 1024),                 # single-node tree: decode attention
+])
+def test_attention_parity(B, Hq, Hkv, Kmax, Ls, Lcap):
+    Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed=B * 31 + Kmax)
+    status = _status()
+    O = gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), torch.from_numpy(masks.view(np.int64)).to(DEV),
+                                  1 / math.sqrt(128), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oatt.tree_attention(to_np(Q), to_np(Kc), to_np(Vc), to_np(Kt), to_np(Vt), L.numpy(), masks,
+                              1 / math.sqrt(128))
+    assert_attention_close(to_np(O), ref)
+
+
+def test_attention_length_past_capacity_is_flagged():
+    Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(1, 8, 2, 32, [700], 640, seed=3)
+    status = _status()
+    gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), torch.from_numpy(masks.view(np.int64)).to(DEV), 0.1,
+                              status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & gb().STATUS_LENGTH
+
+
+@pytest.mark.parametrize("name,layers,reqs", [("tiny", [0], None), ("llama3_8b", [0, 31], None),
+                                              ("qwen3_8b_batch", [0], [0, 17, 63]),
+                                              ("llama31_8b_long", [0], None), ("qwen3_235b", [0], [0, 15])])
+def test_attention_full_size_sampled(name, layers, reqs):
+    """Full-size layer calls; the oracle recomputes sampled requests."""
+    wl = synth.WORKLOADS[name]
+    Lcap = wl.lcap()
+    L = synth.prefix_lengths(wl)
+    rng = np.random.default_rng(wl.seed)
+    masks = np.zeros((wl.B, wl.Kmax), np.uint64)
+    for b in range(wl.B):
+        m = [1]
+        for i in range(1, wl.Kmax):
+            m.append(m[int(rng.integers(0, i))] | (1 << i))
+        masks[b] = np.array(m, dtype=np.uint64)
+    mask_d = torch.from_numpy(masks.view(np.int64)).to(DEV)
+    for layer in layers:
+        Q, Kc, Vc, Kt, Vt = synth.layer_tensors(wl, layer, DEV, Lcap=Lcap)
+        O = gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), mask_d, 1 / math.sqrt(128))
+        torch.cuda.synchronize()
+        for b in (range(wl.B) if reqs is None else reqs):
+            lb = int(L[b])
+            ref = oatt.tree_attention_one(to_np(Q[b]), to_np(Kc[b, :lb]), to_np(Vc[b, :lb]), to_np(Kt[b]),
+                                          to_np(Vt[b]), lb, masks[b], 1 / math.sqrt(128))
+            assert_attention_close(to_np(O[b]), ref)
+        del Q, Kc, Vc, Kt, Vt, O
+        torch.cuda.empty_cache()
+
+
+def _tree_from_oracle(wl, dl, roots, succ_np, L):
+    cfg_o = oracle_cfg(wl)
+    trees, _ = _oracle_tree(wl, cfg_o, dl, roots, succ_np, L)
+    tok = np.array([t.tok for t in trees], np.int32)
+    par = np.array([t.parent for t in trees], np.int32)
+    dep = np.array([t.depth for t in trees], np.int32)
+    return tok, par, dep
+
+
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b", "qwen3_8b_batch", "qwen3_235b"])
+def test_accept_compact_parity(name):
+    wl = synth.WORKLOADS[name]
+    n_layers = 2
+    Lcap = wl.lcap()
+    dl = synth.draft_logits(wl, DEV)
+    roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
+    succ, _ = _M(wl)
+    tok, par, dep = _tree_from_oracle(wl, dl, roots, succ.cpu().numpy(), L)
+    tl = synth.target_logits(wl, DEV)
+    synth.plant_paths(tl, tok, par, dep, synth.planted_lengths(wl))
+    layers = [synth.layer_tensors(wl.scaled(L=(8, 8)), l, DEV, Lcap=Lcap) for l in range(n_layers)]
+    Kc = [x[1] for x in layers]
+    Vc = [x[2] for x in layers]
+    Kt = [x[3] for x in layers]
+    Vt = [x[4] for x in layers]
+    Kc0 = [to_np(x).copy() for x in Kc]
+    Vc0 = [to_np(x).copy() for x in Vc]
+    ptr = lambda ts: gb().layer_pointers(ts, DEV)
+    Ld = L.to(DEV)
+    status = _status()
+    out = gb().graft_accept_compact(tl, torch.from_numpy(tok).to(DEV), torch.from_numpy(par).to(DEV),
+                                    torch.from_numpy(dep).to(DEV), ptr(Kc), ptr(Vc), ptr(Kt), ptr(Vt), n_layers,
+                                    wl.Hkv, Lcap, Ld, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oacc.accept_batch(to_np(tl), dict(tok=tok, parent=par, depth=dep))
+    for k in ("argmax", "acc_len", "path", "out_tok", "bonus"):
+        assert np.array_equal(to_np(out[k]), ref[k]), k
+    want_L = L.numpy() + ref["acc_len"]
+    assert np.array_equal(to_np(Ld), want_L)
+    for l in range(n_layers):
+        Kc_ref, Vc_ref = Kc0[l], Vc0[l]
+        oacc.compact(Kc_ref, Vc_ref, to_np(Kt[l]), to_np(Vt[l]), L.numpy().astype(np.int64), ref["path"],
+                     ref["acc_len"])
+        assert np.array_equal(to_np(Kc[l]), Kc_ref) and np.array_equal(to_np(Vc[l]), Vc_ref)
+    if name == "qwen3_8b_batch":
+        assert len(set(ref["acc_len"].tolist())) > 2  # the planted lengths really vary
+
+
+def test_accept_overflow_flagged_and_skipped():
+    wl = synth.WORKLOADS["tiny"].scaled(V=500)
+    Lcap = 516
+    dl = synth.draft_logits(wl, DEV)
+    roots = synth.root_tokens(wl)
+    L = torch.tensor([514], dtype=torch.int32)
+    s_np, _ = synth.zipf_M(wl.V, wl.W, 1)
+    tok, par, dep = _tree_from_oracle(wl, dl, roots, s_np, L)
+    tl = synth.target_logits(wl, DEV)
+    synth.plant_paths(tl, tok, par, dep, [5])
+    Q, Kc, Vc, Kt, Vt = synth.layer_tensors(wl, 0, DEV, Lcap=Lcap)
+    before = to_np(Kc).copy()
+    ptr = lambda ts: gb().layer_pointers(ts, DEV)
+    Ld = L.to(DEV)
+    status = _status()
+    out = gb().graft_accept_compact(tl, torch.from_numpy(tok).to(DEV), torch.from_numpy(par).to(DEV),
+                                    torch.from_numpy(dep).to(DEV), ptr([Kc]), ptr([Vc]), ptr([Kt]), ptr([Vt]), 1,
+                                    wl.Hkv, Lcap, Ld, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & gb().STATUS_CACHE_OVERFLOW
+    assert int(out["acc_len"][0]) == 5 and int(Ld[0]) == 514
+    assert np.array_equal(to_np(Kc), before)
+
+
+def _update_case(V, W, n, seed, fill):
+    rng = np.random.default_rng(seed)
+    succ = np.full((V, W), -1, np.int32)
+    cnt = np.zeros((V, W), np.int32)
+    for t in range(V):
+        k = int(rng.integers(0, fill + 1))
+        toks = rng.choice(V, k, replace=False)
+        cs = rng.integers(1, 6, k)
+        order = sorted(range(k), key=lambda j: (-cs[j], toks[j]))
+        succ[t, :k] = toks[order]
+        cnt[t, :k] = cs[order]
+    src = rng.integers(0, V, n).astype(np.int32)
+    dst = rng.integers(0, max(2, V // 4), n).astype(np.int32)  # few successors per row: ties, duplicates
+    return succ, cnt, src, dst
+
+
+@pytest.mark.parametrize("V,W,n,fill,seed", [(50, 4, 400, 4, 0), (300, 16, 4096, 16, 1), (1000, 32, 1024, 10, 2),
+                                             (20, 1, 200, 1, 3), (151936, 16, 4096, 0, 4)])
+def test_update_M_parity(V, W, n, fill, seed):
+    succ, cnt, src, dst = _update_case(V, W, n, seed, fill)
+    want_s, want_c = oupd.update_M(succ, cnt, src, dst)
+    for perm_seed in (None, 7):  # the device result must not depend on pair order
+        s_d, c_d = torch.from_numpy(succ).to(DEV), torch.from_numpy(cnt).to(DEV)
+        order = np.arange(n) if perm_seed is None else np.random.default_rng(perm_seed).permutation(n)
+        status = _status()
+        gb().graft_update_M(s_d, c_d, torch.from_numpy(src[order]).to(DEV), torch.from_numpy(dst[order]).to(DEV),
+                            status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert np.array_equal(to_np(s_d), want_s) and np.array_equal(to_np(c_d), want_c)
+
+
+def test_update_M_out_of_range_pairs_are_skipped():
+    succ, cnt, src, dst = _update_case(40, 4, 100, 5, 2)
+    src[3] = 40
+    dst[9] = -2
+    keep = np.ones(100, bool)
+    keep[[3, 9]] = False
+    want_s, want_c = oupd.update_M(succ, cnt, src[keep], dst[keep])
+    s_d, c_d = torch.from_numpy(succ).to(DEV), torch.from_numpy(cnt).to(DEV)
+    status = _status()
+    gb().graft_update_M(s_d, c_d, torch.from_numpy(src).to(DEV), torch.from_numpy(dst).to(DEV), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & gb().STATUS_TOKEN_RANGE
+    assert np.array_equal(to_np(s_d), want_s) and np.array_equal(to_np(c_d), want_c)
+
+
+def _warm_pairs(wl):
+    """Every adjacent pair of the seeded long-context token stream."""
+    stream = synth.token_stream(wl.Lmax, wl.V, wl.seed + 41)
+    return synth.stream_pairs(stream)
+
+
+_WARM = {}
+
+
+def _warm_M_oracle(wl):
+    """The oracle's table after five warm-up rounds (input for the tree parity)."""
+    if wl.name not in _WARM:
+        src, dst = _warm_pairs(wl)
+        s, c = synth.empty_M(wl.V, wl.W)
+        for _ in range(5):
+            s, c = oupd.update_M(s, c, src, dst)
+        _WARM[wl.name] = (s, c)
+    return _WARM[wl.name]
+
+
+def test_update_M_long_context_warmup():
+    """Five rounds of 65535 pairs each on the device equal the oracle's table."""
+    wl = synth.WORKLOADS["llama31_8b_long"]
+    src, dst = _warm_pairs(wl)
+    s_np, c_np = synth.empty_M(wl.V, wl.W)
+    s_d, c_d = torch.from_numpy(s_np).to(DEV), torch.from_numpy(c_np).to(DEV)
+    sd, dd = torch.from_numpy(src).to(DEV), torch.from_numpy(dst).to(DEV)
+    for _ in range(5):
+        gb().graft_update_M(s_d, c_d, sd, dd)
+    torch.cuda.synchronize()
+    s, c = _warm_M_oracle(wl)
+    assert np.array_equal(to_np(s_d), s) and np.array_equal(to_np(c_d), c)
+    assert int(c.sum()) == 5 * (wl.Lmax - 1)

@@ -1,0 +1,31 @@
+// Arguments shared by the tree-attention kernels and their host dispatch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace graft {
+
+struct AttnArgs {
+    int B, Hq, Hkv, G, Kmax, R;  // R = Kmax * G query rows per (request, KV head)
+    int nRB;                      // 128-row blocks per (request, KV head)
+    int C;                        // prefix keys per chunk (multiple of 64)
+    int nchunk;                   // chunks per (request, KV head) allowed by Lcap
+    int Lcap;
+    float scale;
+    const void* Q;
+    const void* Kc;
+    const void* Vc;
+    const void* Kt;
+    const void* Vt;
+    const int32_t* L;
+    const uint64_t* mask;
+    void* O;
+    float* part_o;    // [B][Hkv][nRB][nchunk][128][128] normalised partial outputs
+    float* part_lse;  // [B][Hkv][nRB][nchunk][128] log2-sum-exp of each partial
+    int32_t* status;
+};
+
+int attn_mma_launch(const AttnArgs& a, cudaStream_t st);
+
+}  // namespace graft

@@ -1,0 +1,115 @@
+// graft_tree_attention: argument checks, key-chunk policy and dispatch.
+//
+// The chunk size is chosen from the cache capacity so that the number of
+// CTAs is about the device's SM count (small batches, long prefixes) while
+// each chunk stays long enough that partial outputs are a small fraction of
+// the KV bytes read.  The same policy sizes the workspace.
+#include "attention.cuh"
+#include "common.cuh"
+
+namespace graft {
+namespace {
+
+struct AttnPlan {
+    int G, R, nRB, C, nchunk;
+};
+
+AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
+    AttnPlan p;
+    p.G = Hq / Hkv;
+    p.R = Kmax * p.G;
+    p.nRB = (p.R + 127) / 128;
+    const long long units = (long long)B * Hkv * p.nRB;
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 148;
+    const long long target = sms;
+    long long C = (Lcap * units + target - 1) / target;
+    C = (C + 63) / 64 * 64;
+    if (C < 256) C = 256;
+    if (C > (1LL << 30)) C = 1LL << 30;
+    p.C = (int)C;
+    p.nchunk = Lcap > 0 ? (int)((Lcap + C - 1) / C) : 1;
+    if (p.nchunk < 1) p.nchunk = 1;
+    return p;
+}
+
+size_t attn_ws(const AttnPlan& p, int B, int Hkv, AttnArgs* a, void* ws) {
+    WsCarver c(ws);
+    const size_t parts = p.nchunk > 1 ? (size_t)B * Hkv * p.nRB * p.nchunk * 128 : 0;
+    float* po = c.take<float>(parts * GRAFT_HEAD_DIM);
+    float* pl = c.take<float>(parts);
+    if (a) {
+        a->part_o = po;
+        a->part_lse = pl;
+    }
+    return c.bytes();
+}
+
+int check_shape(int B, int Hq, int Hkv, int head_dim, int Kmax, int64_t Lcap) {
+    if (B < 0 || Hq < 1 || Hkv < 1 || Kmax < 1 || Lcap < 0) return GRAFT_ERR_INVALID_ARG;
+    if (head_dim != GRAFT_HEAD_DIM) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    if (Hq % Hkv != 0) return GRAFT_ERR_INVALID_ARG;
+    if (Kmax > GRAFT_MAX_KMAX) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)Kmax * (Hq / Hkv) > 1024) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    if (Lcap > (1LL << 30)) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    if (B > 65535) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    return GRAFT_OK;
+}
+
+}  // namespace
+}  // namespace graft
+
+using namespace graft;
+
+extern "C" int graft_tree_attention_workspace_size(int B, int Hq, int Hkv, int head_dim, int Kmax, int64_t Lcap,
+                                                   size_t* bytes) {
+    if (bytes == nullptr) return GRAFT_ERR_INVALID_ARG;
+    const int rc = check_shape(B, Hq, Hkv, head_dim, Kmax, Lcap);
+    if (rc != GRAFT_OK) return rc;
+    const AttnPlan p = plan_attention(B, Hq, Hkv, Kmax, Lcap);
+    *bytes = attn_ws(p, B, Hkv, nullptr, nullptr);
+    return GRAFT_OK;
+}
+
+extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Kmax, const void* Q, const void* Kc,
+                                    const void* Vc, int64_t Lcap, const void* Kt, const void* Vt, const int32_t* L,
+                                    const uint64_t* tree_mask, float scale, void* O, int32_t* status, void* ws,
+                                    size_t ws_bytes, graft_stream_t stream) {
+    const int rc = check_shape(B, Hq, Hkv, head_dim, Kmax, Lcap);
+    if (rc != GRAFT_OK) return rc;
+    if (B == 0) return GRAFT_OK;
+    if (Q == nullptr || Kt == nullptr || Vt == nullptr || L == nullptr || tree_mask == nullptr || O == nullptr)
+        return GRAFT_ERR_INVALID_ARG;
+    if (Lcap > 0 && (Kc == nullptr || Vc == nullptr)) return GRAFT_ERR_INVALID_ARG;
+    const uintptr_t al = reinterpret_cast<uintptr_t>(Q) | reinterpret_cast<uintptr_t>(Kc) |
+                         reinterpret_cast<uintptr_t>(Vc) | reinterpret_cast<uintptr_t>(Kt) |
+                         reinterpret_cast<uintptr_t>(Vt) | reinterpret_cast<uintptr_t>(O);
+    if (al & 15) return GRAFT_ERR_INVALID_ARG;  // 16-byte vector loads and stores
+    const AttnPlan p = plan_attention(B, Hq, Hkv, Kmax, Lcap);
+    const size_t need = attn_ws(p, B, Hkv, nullptr, nullptr);
+    if (!ws_ok(ws, ws_bytes, need)) return GRAFT_ERR_WORKSPACE;
+    AttnArgs a{};
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.G = p.G;
+    a.Kmax = Kmax;
+    a.R = p.R;
+    a.nRB = p.nRB;
+    a.C = p.C;
+    a.nchunk = p.nchunk;
+    a.Lcap = (int)Lcap;
+    a.scale = scale;
+    a.Q = Q;
+    a.Kc = Kc;
+    a.Vc = Vc;
+    a.Kt = Kt;
+    a.Vt = Vt;
+    a.L = L;
+    a.mask = tree_mask;
+    a.O = O;
+    a.status = status;
+    attn_ws(p, B, Hkv, &a, ws);
+    if ((long long)p.nRB * Hkv > 65535 * 1024LL) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    return attn_mma_launch(a, (cudaStream_t)stream);
+}

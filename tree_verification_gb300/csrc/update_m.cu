@@ -1,0 +1,215 @@
+// Online update of the adjacency table M from verified pairs.
+//
+// Graft article, method paragraph (fourth point) and architecture paragraph:
+// M is refreshed continuously from the verified tree's logits.  Layout and
+// rule (the pages leave both open): succ/cnt [V][W] int32, each row ranked by
+// (count desc, token asc) with empty slots (-1, 0) last; a batch of
+// (src -> dst) pairs adds 1 per pair to successors already present (atomic
+// increments) and lets new successors compete for the row with their
+// multiplicity as count; each touched row keeps its top W.
+//
+// Kernels (work proportional to the number of pairs, never to V):
+//   clear_kernel   resets two open-addressing hash tables in the workspace
+//   pairs_kernel   one thread per pair: registers the row, increments a
+//                  present successor, or counts the new (src, dst) key and
+//                  links it into its row's list
+//   rerank_kernel  one warp per touched row: bitonic-sorts the W slots by
+//                  the packed key, then inserts every new successor with a
+//                  warp ballot; the result depends only on the multiset
+#include "common.cuh"
+
+namespace graft {
+namespace {
+
+constexpr unsigned long long kEmptyPair = ~0ull;
+
+struct UpdWs {
+    unsigned long long* pair_key;  // [cap] (src << 32) | dst, kEmptyPair = free
+    int32_t* pair_mult;            // [cap]
+    int32_t* pair_next;            // [cap] next new pair of the same row, -1 = end
+    int32_t* row_key;              // [cap] src token, -1 = free
+    int32_t* row_head;             // [cap] first new pair of the row, -1 = none
+    int32_t* touched;              // [n] row-table slots in arrival order
+    int32_t* n_touched;            // [1]
+    int cap;                       // power of two >= 2n
+};
+
+__device__ __forceinline__ uint32_t hash32(uint32_t x) {
+    x ^= x >> 16;
+    x *= 0x7feb352dU;
+    x ^= x >> 15;
+    x *= 0x846ca68bU;
+    x ^= x >> 16;
+    return x;
+}
+__device__ __forceinline__ uint32_t hash64(unsigned long long x) {
+    x ^= x >> 33;
+    x *= 0xff51afd7ed558ccdULL;
+    x ^= x >> 33;
+    x *= 0xc4ceb9fe1a85ec53ULL;
+    x ^= x >> 33;
+    return (uint32_t)x;
+}
+
+__global__ void clear_kernel(UpdWs w) {
+    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < w.cap; i += gridDim.x * blockDim.x) {
+        w.pair_key[i] = kEmptyPair;
+        w.pair_mult[i] = 0;
+        w.pair_next[i] = -1;
+        w.row_key[i] = -1;
+        w.row_head[i] = -1;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) *w.n_touched = 0;
+}
+
+__global__ void pairs_kernel(int32_t* __restrict__ succ, int32_t* __restrict__ cnt, int V, int W,
+                             const int32_t* __restrict__ src, const int32_t* __restrict__ dst, int64_t n, UpdWs w,
+                             int32_t* status) {
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int s = src[i], t = dst[i];
+    if (s < 0 || s >= V || t < 0 || t >= V) {
+        flag_status(status, GRAFT_STATUS_TOKEN_RANGE);
+        return;
+    }
+    const uint32_t mask = (uint32_t)w.cap - 1;
+    // register the row (probes end: the table has at least 2n free slots)
+    uint32_t h = hash32((uint32_t)s) & mask;
+    for (int probe = 0; probe < w.cap; ++probe) {
+        const int old = atomicCAS(&w.row_key[h], -1, s);
+        if (old == -1) {
+            w.touched[atomicAdd(w.n_touched, 1)] = (int)h;
+            break;
+        }
+        if (old == s) break;
+        h = (h + 1) & mask;
+    }
+    const int row_slot = (int)h;
+    // successor already present: one atomic increment
+    const int32_t* rs = succ + (size_t)s * W;
+    for (int j = 0; j < W; ++j) {
+        if (rs[j] == t) {
+            atomicAdd(cnt + (size_t)s * W + j, 1);
+            return;
+        }
+    }
+    // new successor: count the (s, t) key; its first arrival links it into the row's list
+    const unsigned long long key = ((unsigned long long)(uint32_t)s << 32) | (uint32_t)t;
+    uint32_t q = hash64(key) & mask;
+    for (int probe = 0; probe < w.cap; ++probe) {
+        const unsigned long long old = atomicCAS(&w.pair_key[q], kEmptyPair, key);
+        if (old == kEmptyPair) {
+            w.pair_next[q] = atomicExch(&w.row_head[row_slot], (int)q);
+            atomicAdd(&w.pair_mult[q], 1);
+            return;
+        }
+        if (old == key) {
+            atomicAdd(&w.pair_mult[q], 1);
+            return;
+        }
+        q = (q + 1) & mask;
+    }
+}
+
+// Packs a slot so that a smaller key ranks first: count desc, then token asc.
+// Empty slots (cnt 0, token -1) sort after every real entry; lanes past W
+// carry count -1 and sort after the empties.
+__device__ __forceinline__ unsigned long long pack_slot(int c, int tok) {
+    return ((unsigned long long)(uint32_t)(0x7fffffff - c) << 32) | (uint32_t)tok;
+}
+
+__global__ void rerank_kernel(int32_t* __restrict__ succ, int32_t* __restrict__ cnt, int W, UpdWs w) {
+    const int warps = blockDim.x >> 5;
+    const int wid = blockIdx.x * warps + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (wid >= *w.n_touched) return;
+    const int slot = w.touched[wid];
+    const int s = w.row_key[slot];
+    int32_t* rs = succ + (size_t)s * W;
+    int32_t* rc = cnt + (size_t)s * W;
+    unsigned long long key = lane < W ? pack_slot(rc[lane], rs[lane]) : pack_slot(-1, -1);
+    // bitonic sort, ascending key
+#pragma unroll
+    for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+            const unsigned long long other = __shfl_xor_sync(0xffffffffu, key, j);
+            const bool up = (lane & k) == 0;
+            const bool lower = (lane & j) == 0;
+            const unsigned long long lo = key < other ? key : other;
+            const unsigned long long hi = key < other ? other : key;
+            key = (lower == up) ? lo : hi;
+        }
+    }
+    // insert each new successor of the row; order of insertion does not matter
+    for (int p = w.row_head[slot]; p >= 0; p = w.pair_next[p]) {
+        const int t = (int)(uint32_t)(w.pair_key[p] & 0xffffffffull);
+        const unsigned long long ck = pack_slot(w.pair_mult[p], t);
+        const unsigned ahead = __ballot_sync(0xffffffffu, key < ck);
+        const int pos = __popc(ahead);  // entries that stay in front (a prefix, the list is sorted)
+        if (pos < W) {
+            const unsigned long long prev = __shfl_up_sync(0xffffffffu, key, 1);
+            if (lane > pos) key = prev;
+            else if (lane == pos) key = ck;
+        }
+    }
+    if (lane < W) {
+        const int c = 0x7fffffff - (int)(key >> 32);
+        const int tok = (int)(uint32_t)(key & 0xffffffffull);
+        rs[lane] = tok;
+        rc[lane] = c;
+    }
+}
+
+int table_cap(int64_t n) {
+    int64_t cap = 64;
+    while (cap < 2 * n) cap <<= 1;
+    return (int)cap;
+}
+
+UpdWs carve_update(WsCarver& c, int64_t n) {
+    UpdWs w;
+    w.cap = table_cap(n);
+    w.pair_key = c.take<unsigned long long>(w.cap);
+    w.pair_mult = c.take<int32_t>(w.cap);
+    w.pair_next = c.take<int32_t>(w.cap);
+    w.row_key = c.take<int32_t>(w.cap);
+    w.row_head = c.take<int32_t>(w.cap);
+    w.touched = c.take<int32_t>(n > 0 ? n : 1);
+    w.n_touched = c.take<int32_t>(1);
+    return w;
+}
+
+}  // namespace
+}  // namespace graft
+
+using namespace graft;
+
+extern "C" int graft_update_M_workspace_size(int64_t n, size_t* bytes) {
+    if (bytes == nullptr || n < 0) return GRAFT_ERR_INVALID_ARG;
+    if (n > (1LL << 28)) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    WsCarver c(nullptr);
+    carve_update(c, n);
+    *bytes = c.bytes();
+    return GRAFT_OK;
+}
+
+extern "C" int graft_update_M(int32_t* M_succ, int32_t* M_cnt, int V, int W, const int32_t* src, const int32_t* dst,
+                              int64_t n, int32_t* status, void* ws, size_t ws_bytes, graft_stream_t stream) {
+    if (V < 1 || W < 1 || n < 0) return GRAFT_ERR_INVALID_ARG;
+    if (W > GRAFT_MAX_W || n > (1LL << 28)) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    if (n == 0) return GRAFT_OK;
+    if (M_succ == nullptr || M_cnt == nullptr || src == nullptr || dst == nullptr) return GRAFT_ERR_INVALID_ARG;
+    WsCarver sizer(nullptr);
+    carve_update(sizer, n);
+    if (!ws_ok(ws, ws_bytes, sizer.bytes())) return GRAFT_ERR_WORKSPACE;
+    WsCarver c(ws);
+    UpdWs w = carve_update(c, n);
+    cudaStream_t st = (cudaStream_t)stream;
+    const int cb = (int)((w.cap + 255) / 256);
+    clear_kernel<<<cb < 1024 ? cb : 1024, 256, 0, st>>>(w);
+    pairs_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(M_succ, M_cnt, V, W, src, dst, n, w, status);
+    rerank_kernel<<<(unsigned)((n + 7) / 8), 256, 0, st>>>(M_succ, M_cnt, W, w);
+    count_launches(3);
+    return launch_status();
+}

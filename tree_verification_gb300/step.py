@@ -1,0 +1,80 @@
+"""One hybrid-tree verify step through the C ABI, with preallocated buffers.
+
+``VerifyStep`` owns the outputs and workspaces of the four library calls
+and runs them in the Graft article's order on one CUDA stream:
+
+    graft_build_tree  ->  graft_tree_attention x n_layers  ->
+    graft_accept_compact  ->  graft_update_M (pairs = every tree node's
+    (token, target argmax))
+
+Because every buffer is fixed, a whole step can be captured once in a CUDA
+graph and replayed, which removes the per-layer host launch cost.  The
+caller owns the model-side tensors: drafter and target logits, per-layer
+Q / tree KV / KV caches, the cache lengths and the table M.
+"""
+from __future__ import annotations
+
+import math
+from typing import List, Optional, Sequence
+
+import torch
+
+from . import binding as gb
+
+
+class VerifyStep:
+    def __init__(self, cfg: gb.GraftConfig, B: int, Hq: int, Hkv: int, n_layers: int, Lcap: int, device,
+                 Kc: Sequence[torch.Tensor], Vc: Sequence[torch.Tensor], Kt: Sequence[torch.Tensor],
+                 Vt: Sequence[torch.Tensor]):
+        self.cfg, self.B, self.Hq, self.Hkv, self.n_layers, self.Lcap = cfg, B, Hq, Hkv, n_layers, Lcap
+        self.device = torch.device(device)
+        K, dev = cfg.Kmax, self.device
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.tree = dict(tok=torch.empty(B, K, **i32), parent=torch.empty(B, K, **i32),
+                         depth=torch.empty(B, K, **i32), pos=torch.empty(B, K, **i32),
+                         mask=torch.empty(B, K, dtype=torch.int64, device=dev), stage=torch.empty(B, **i32))
+        self.acc = dict(argmax=torch.empty(B, K, **i32), acc_len=torch.empty(B, **i32),
+                        path=torch.empty(B, K, **i32), out_tok=torch.empty(B, K, **i32),
+                        bonus=torch.empty(B, **i32))
+        self.status = torch.zeros(1, **i32)
+        u8 = dict(dtype=torch.uint8, device=dev)
+        self.ws_tree = torch.empty(max(1, gb.graft_build_tree_workspace_size(cfg, B)), **u8)
+        self.ws_attn = torch.empty(max(1, gb.graft_tree_attention_workspace_size(B, Hq, Hkv, K, Lcap)), **u8)
+        self.ws_acc = torch.empty(max(1, gb.graft_accept_compact_workspace_size(B, K, cfg.V)), **u8)
+        self.ws_upd = torch.empty(max(1, gb.graft_update_M_workspace_size(B * K)), **u8)
+        self.O = torch.empty(B, K, Hq, gb.HEAD_DIM, dtype=torch.bfloat16, device=dev)
+        self.Kc, self.Vc, self.Kt, self.Vt = list(Kc), list(Vc), list(Kt), list(Vt)
+        self.Kc_ptrs = gb.layer_pointers(self.Kc, dev)
+        self.Vc_ptrs = gb.layer_pointers(self.Vc, dev)
+        self.Kt_ptrs = gb.layer_pointers(self.Kt, dev)
+        self.Vt_ptrs = gb.layer_pointers(self.Vt, dev)
+        self.scale = 1.0 / math.sqrt(gb.HEAD_DIM)
+        self.graph: Optional[torch.cuda.CUDAGraph] = None
+
+    def run(self, draft_logits, root_tok, M_succ, M_cnt, L, Q: Sequence[torch.Tensor], target_logits,
+            attn_layers: Optional[Sequence[int]] = None) -> None:
+        """Enqueue one step on the current stream (asynchronous)."""
+        gb.graft_build_tree(self.cfg, draft_logits, root_tok, M_succ, L, out=self.tree, status=self.status,
+                            ws=self.ws_tree)
+        for l in (range(self.n_layers) if attn_layers is None else attn_layers):
+            gb.graft_tree_attention(Q[l], self.Kc[l], self.Vc[l], self.Kt[l], self.Vt[l], L, self.tree["mask"],
+                                    self.scale, O=self.O, status=self.status, ws=self.ws_attn)
+        gb.graft_accept_compact(target_logits, self.tree["tok"], self.tree["parent"], self.tree["depth"],
+                                self.Kc_ptrs, self.Vc_ptrs, self.Kt_ptrs, self.Vt_ptrs, self.n_layers, self.Hkv,
+                                self.Lcap, L, out=self.acc, status=self.status, ws=self.ws_acc)
+        gb.graft_update_M(M_succ, M_cnt, self.tree["tok"].view(-1), self.acc["argmax"].view(-1),
+                          status=self.status, ws=self.ws_upd)
+
+    def capture(self, *args, **kw) -> torch.cuda.CUDAGraph:
+        """Capture run(*args) into a CUDA graph (the arguments' storage is baked in)."""
+        g = torch.cuda.CUDAGraph()
+        s = torch.cuda.Stream(device=self.device)
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.run(*args, **kw)  # warm the launch path once outside capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize(self.device)
+        with torch.cuda.graph(g):
+            self.run(*args, **kw)
+        self.graph = g
+        return g
