@@ -230,6 +230,30 @@ int graft_update_M(int32_t* M_succ, int32_t* M_cnt, int V, int W, const int32_t*
                    const int32_t* dst, int64_t n, int32_t* status, void* ws, size_t ws_bytes,
                    graft_stream_t stream);
 
+/*
+ * graft_update_M_noalloc — graft_update_M without a workspace argument.
+ *
+ * The Graft pages have no counterpart to this entry point; it exists for
+ * callers that cannot provide device scratch memory: a plug-in that only sees
+ * the tensors its host framework passes in and has no allocator of its own,
+ * or a serving loop that must not call cudaMalloc because it synchronises the
+ * whole device.  Arguments and results are those of graft_update_M.
+ *
+ * Scratch lives in one static device array of the library (1 MiB, kept on
+ * every GPU that loads the library until the process exits), enough for
+ * n <= GRAFT_NOALLOC_MAX_PAIRS pairs; larger n returns
+ * GRAFT_ERR_UNSUPPORTED_SHAPE and enqueues nothing.  The call allocates and
+ * frees nothing.  Its first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  All calls on a device share the array
+ * (each call clears the parts it reads), so calls that may run at the same
+ * time on the GPU — different streams with no ordering between them — race
+ * and corrupt each other's result: order them on one stream or with events.
+ */
+#define GRAFT_NOALLOC_MAX_PAIRS 16384
+int graft_update_M_noalloc(int32_t* M_succ, int32_t* M_cnt, int V, int W, const int32_t* src,
+                           const int32_t* dst, int64_t n, int32_t* status, graft_stream_t stream);
+
 /* Human-readable text for a return code (static string). */
 const char* graft_status_string(int code);
 

@@ -75,6 +75,7 @@ _SIGNATURES = {
                              _P, _P, _SZ, _P],
     "graft_update_M_workspace_size": [_I64, ctypes.POINTER(_SZ)],
     "graft_update_M": [_P, _P, _I, _I, _P, _P, _I64, _P, _P, _SZ, _P],
+    "graft_update_M_noalloc": [_P, _P, _I, _I, _P, _P, _I64, _P, _P],
     "graft_status_string": [_I],
     "graft_version": [],
     "graft_launch_count": [],
@@ -280,6 +281,28 @@ def graft_update_M(M_succ, M_cnt, src, dst, status=None, ws=None, stream=None):
     ws, nws = _ws(graft_update_M_workspace_size(n), M_succ.device, ws)
     _check(lib().graft_update_M(_ptr(M_succ), _ptr(M_cnt), V, W, _ptr(src), _ptr(dst), n, _ptr(status), _ptr(ws),
                                 nws, _stream(stream)), "graft_update_M")
+
+
+NOALLOC_MAX_PAIRS = 16384
+
+
+def graft_update_M_noalloc(M_succ, M_cnt, src, dst, status=None, stream=None):
+    """graft_update_M with the library's own fixed scratch (no workspace, nothing allocated).
+
+    For callers that cannot provide device scratch memory; at most
+    NOALLOC_MAX_PAIRS pairs per call, and calls that may overlap on the GPU
+    must be ordered (they share one scratch array).
+    """
+    V, W = M_succ.shape
+    _need(M_succ, "M_succ", torch.int32)
+    _need(M_cnt, "M_cnt", torch.int32, (V, W))
+    _need(src, "src", torch.int32)
+    _need(dst, "dst", torch.int32)
+    n = src.numel()
+    if dst.numel() != n:
+        raise ValueError("src and dst must have the same length")
+    _check(lib().graft_update_M_noalloc(_ptr(M_succ), _ptr(M_cnt), V, W, _ptr(src), _ptr(dst), n, _ptr(status),
+                                        _stream(stream)), "graft_update_M_noalloc")
 
 
 def graft_status_string(code: int) -> str:

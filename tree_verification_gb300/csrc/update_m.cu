@@ -16,6 +16,8 @@
 //   rerank_kernel  one warp per touched row: bitonic-sorts the W slots by
 //                  the packed key, then inserts every new successor with a
 //                  warp ballot; the result depends only on the multiset
+#include <mutex>
+
 #include "common.cuh"
 
 namespace graft {
@@ -206,6 +208,71 @@ extern "C" int graft_update_M(int32_t* M_succ, int32_t* M_cnt, int V, int W, con
     WsCarver c(ws);
     UpdWs w = carve_update(c, n);
     cudaStream_t st = (cudaStream_t)stream;
+    const int cb = (int)((w.cap + 255) / 256);
+    clear_kernel<<<cb < 1024 ? cb : 1024, 256, 0, st>>>(w);
+    pairs_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(M_succ, M_cnt, V, W, src, dst, n, w, status);
+    rerank_kernel<<<(unsigned)((n + 7) / 8), 256, 0, st>>>(M_succ, M_cnt, W, w);
+    count_launches(3);
+    return launch_status();
+}
+
+// ----------------------------------------------------------------------------
+// graft_update_M_noalloc: the same update, with its scratch in a fixed device
+// array instead of a caller workspace.
+//
+// Some callers cannot hand the library a workspace: a plug-in that only sees
+// the tensors its host framework gives it and has no device allocator of its
+// own, or a latency-critical serving loop that must not call cudaMalloc
+// (which synchronises the whole device).  For them the hash tables live in
+// g_update_scratch below, sized for GRAFT_NOALLOC_MAX_PAIRS pairs; every GPU
+// that loads the library keeps this 1 MiB until the process exits.
+// ----------------------------------------------------------------------------
+namespace graft {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 1u << 20;
+static __device__ __align__(256) unsigned char g_update_scratch[kNoAllocScratchBytes];
+
+std::mutex g_scratch_mutex;
+void* g_scratch_addr[64] = {nullptr};
+
+// Device address of g_update_scratch on the current device, looked up once
+// per device.  In host code the array's name is only a host-side handle, so
+// kernels must be given the address cudaGetSymbolAddress returns.
+int noalloc_scratch(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return GRAFT_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    std::lock_guard<std::mutex> lock(g_scratch_mutex);
+    if (g_scratch_addr[dev] == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_update_scratch) != cudaSuccess || p == nullptr) return GRAFT_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return GRAFT_OK;
+}
+
+}  // namespace
+}  // namespace graft
+
+extern "C" int graft_update_M_noalloc(int32_t* M_succ, int32_t* M_cnt, int V, int W, const int32_t* src,
+                                      const int32_t* dst, int64_t n, int32_t* status, graft_stream_t stream) {
+    if (V < 1 || W < 1 || n < 0) return GRAFT_ERR_INVALID_ARG;
+    if (W > GRAFT_MAX_W || n > GRAFT_NOALLOC_MAX_PAIRS) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    if (n == 0) return GRAFT_OK;
+    if (M_succ == nullptr || M_cnt == nullptr || src == nullptr || dst == nullptr) return GRAFT_ERR_INVALID_ARG;
+    WsCarver sizer(nullptr);
+    carve_update(sizer, n);
+    if (sizer.bytes() > kNoAllocScratchBytes) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    void* scratch = nullptr;
+    const int rc = noalloc_scratch(&scratch);
+    if (rc != GRAFT_OK) return rc;
+    WsCarver c(scratch);
+    UpdWs w = carve_update(c, n);
+    cudaStream_t st = (cudaStream_t)stream;
+    // clear_kernel resets every table the other two kernels read, so whatever
+    // the previous call left in the shared array does not leak into this one
     const int cb = (int)((w.cap + 255) / 256);
     clear_kernel<<<cb < 1024 ? cb : 1024, 256, 0, st>>>(w);
     pairs_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(M_succ, M_cnt, V, W, src, dst, n, w, status);
