@@ -57,6 +57,7 @@ typedef struct CUstream_st* graft_stream_t;
 #define GRAFT_STATUS_CACHE_OVERFLOW 2 /* L[b] + accepted length > Lcap; that request was not compacted */
 #define GRAFT_STATUS_LENGTH 4         /* L[b] < 0 or L[b] > Lcap; that request was skipped */
 #define GRAFT_STATUS_TREE 8           /* a kept draft node's parent was not kept (cannot happen for finite logits) */
+#define GRAFT_STATUS_TIMEOUT 16       /* a bounded wait inside a kernel expired; that CTA's output is incomplete */
 
 /* Limits. */
 #define GRAFT_MAX_KMAX 64        /* tree nodes per request (one uint64 ancestor mask) */

@@ -26,6 +26,12 @@ struct AttnArgs {
     int32_t* status;
 };
 
+// Warp-level mma.sync path: any group size; 128-row CTAs.
 int attn_mma_launch(const AttnArgs& a, cudaStream_t st);
+// tcgen05 path: group sizes dividing 128; 256-row CTAs.
+bool attn_tc_supported(int G);
+int attn_tc_launch(const AttnArgs& a, cudaStream_t st);
+// Merges split-key partials (no-op when every request fits one chunk).
+int attn_combine_launch(const AttnArgs& a, cudaStream_t st);
 
 }  // namespace graft

@@ -4,6 +4,8 @@
 // CTAs is about the device's SM count (small batches, long prefixes) while
 // each chunk stays long enough that partial outputs are a small fraction of
 // the KV bytes read.  The same policy sizes the workspace.
+#include <cstdlib>
+
 #include "attention.cuh"
 #include "common.cuh"
 
@@ -12,20 +14,31 @@ namespace {
 
 struct AttnPlan {
     int G, R, nRB, C, nchunk;
+    bool tc;
 };
 
+// Key-chunk policy: enough chunks that the CTAs cover the SMs about once,
+// but at least kMinChunk keys per chunk so partial outputs stay a small
+// share of the KV bytes.  GRAFT_ATTN_MIN_CHUNK (multiple of 64) overrides the
+// minimum for tuning; the workspace size and the launch read the same value.
 AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
     AttnPlan p;
     p.G = Hq / Hkv;
     p.R = Kmax * p.G;
     p.nRB = (p.R + 127) / 128;
-    const long long units = (long long)B * Hkv * p.nRB;
+    p.tc = attn_tc_supported(p.G);
+    const long long rows_per_cta = p.tc ? 256 : 128;
+    const long long units = (long long)B * Hkv * ((p.R + rows_per_cta - 1) / rows_per_cta);
     int sms = device_sm_count();
     if (sms <= 0) sms = 148;
-    const long long target = sms;
-    long long C = (Lcap * units + target - 1) / target;
+    long long min_chunk = 256;
+    if (const char* env = getenv("GRAFT_ATTN_MIN_CHUNK")) {
+        const long long v = atoll(env);
+        if (v >= 64) min_chunk = (v + 63) / 64 * 64;
+    }
+    long long C = (Lcap * units + sms - 1) / sms;
     C = (C + 63) / 64 * 64;
-    if (C < 256) C = 256;
+    if (C < min_chunk) C = min_chunk;
     if (C > (1LL << 30)) C = 1LL << 30;
     p.C = (int)C;
     p.nchunk = Lcap > 0 ? (int)((Lcap + C - 1) / C) : 1;
@@ -110,6 +123,7 @@ extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Km
     a.O = O;
     a.status = status;
     attn_ws(p, B, Hkv, &a, ws);
-    if ((long long)p.nRB * Hkv > 65535 * 1024LL) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    if ((long long)p.nRB * Hkv > 65535LL || p.nchunk > 65535) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    if (p.tc) return attn_tc_launch(a, (cudaStream_t)stream);
     return attn_mma_launch(a, (cudaStream_t)stream);
 }

@@ -223,17 +223,19 @@ attn_partial_kernel(AttnArgs a) {
         for (int nt = 0; nt < 8; ++nt) {
             float p[4];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                p[e] = fast_exp2(s[nt][e] - base[e >> 1]);
-                rs[e >> 1] += p[e];
-            }
+            for (int e = 0; e < 4; ++e) p[e] = fast_exp2(s[nt][e] - base[e >> 1]);
+            // the row sum uses the bf16-rounded weights that the PV product consumes
+            const __nv_bfloat162 w01 = __floats2bfloat162_rn(p[0], p[1]);
+            const __nv_bfloat162 w23 = __floats2bfloat162_rn(p[2], p[3]);
+            rs[0] += __low2float(w01) + __high2float(w01);
+            rs[1] += __low2float(w23) + __high2float(w23);
             const int ks = nt >> 1;
             if ((nt & 1) == 0) {
-                pa[ks][0] = pack_bf16(p[0], p[1]);
-                pa[ks][1] = pack_bf16(p[2], p[3]);
+                pa[ks][0] = *reinterpret_cast<const uint32_t*>(&w01);
+                pa[ks][1] = *reinterpret_cast<const uint32_t*>(&w23);
             } else {
-                pa[ks][2] = pack_bf16(p[0], p[1]);
-                pa[ks][3] = pack_bf16(p[2], p[3]);
+                pa[ks][2] = *reinterpret_cast<const uint32_t*>(&w01);
+                pa[ks][3] = *reinterpret_cast<const uint32_t*>(&w23);
             }
         }
 #pragma unroll
@@ -296,44 +298,65 @@ attn_partial_kernel(AttnArgs a) {
     }
 }
 
-__global__ void __launch_bounds__(NT)
+}  // namespace attn_mma
+
+// Merges the per-chunk partial outputs of every (request, KV head, row) whose
+// request spans more than one key chunk: O = sum_c 2^(lse_c - lse) O_c with
+// lse = log2 sum_c 2^lse_c.  One warp per output row, four dims per lane.
+__global__ void __launch_bounds__(256)
 attn_combine_kernel(AttnArgs a) {
-    const int nRB = a.nRB;
-    const int rb = blockIdx.x % nRB;
-    const int kvh = blockIdx.x / nRB;
-    const int b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const long long row = (long long)blockIdx.x * 8 + warp;
+    const long long total = (long long)a.B * a.Hkv * a.nRB * 128;
+    if (row >= total) return;
+    const int r = (int)(row % 128);
+    const int tile = (int)((row / 128) % a.nRB);
+    const int kvh = (int)((row / (128LL * a.nRB)) % a.Hkv);
+    const int b = (int)(row / (128LL * a.nRB * a.Hkv));
+    const int gr = tile * 128 + r;
+    if (gr >= a.R) return;
     const int Lb = a.L[b];
     if (Lb < 0 || Lb > a.Lcap) return;
     const int nck = Lb > 0 ? (Lb + a.C - 1) / a.C : 1;
     if (nck == 1) return;
-    const size_t base = (((size_t)b * a.Hkv + kvh) * nRB + rb) * a.nchunk;
-    for (int item = threadIdx.x; item < BM * (HD / 4); item += NT) {
-        const int r = item / (HD / 4);
-        const int q4 = item % (HD / 4);
-        const int gr = rb * BM + r;
-        if (gr >= a.R) break;
-        float mx = -INFINITY;
-        for (int c = 0; c < nck; ++c) mx = fmaxf(mx, a.part_lse[(base + c) * BM + r]);
-        float wsum = 0.f;
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int c = 0; c < nck; ++c) {
-            const size_t pi = (base + c) * BM + r;
-            const float w = exp2f(a.part_lse[pi] - mx);
-            const float4 v = *reinterpret_cast<const float4*>(a.part_o + pi * HD + q4 * 4);
-            acc.x += w * v.x;
-            acc.y += w * v.y;
-            acc.z += w * v.z;
-            acc.w += w * v.w;
-            wsum += w;
-        }
-        const float inv = 1.f / wsum;
-        const int node = gr / a.G, h = kvh * a.G + gr % a.G;
-        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.O) + (((size_t)b * a.Kmax + node) * a.Hq + h) * HD + q4 * 4;
-        reinterpret_cast<__nv_bfloat162*>(dst)[0] = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-        reinterpret_cast<__nv_bfloat162*>(dst)[1] = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    const size_t base = (((size_t)b * a.Hkv + kvh) * a.nRB + tile) * a.nchunk;
+    float mx = -INFINITY;
+    for (int c = lane; c < nck; c += 32) mx = fmaxf(mx, a.part_lse[(base + c) * 128 + r]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float wsum = 0.f;
+    for (int c = 0; c < nck; ++c) {
+        const size_t pi = (base + c) * 128 + r;
+        const float w = exp2f(a.part_lse[pi] - mx);
+        const float4 v = *reinterpret_cast<const float4*>(a.part_o + pi * GRAFT_HEAD_DIM + lane * 4);
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+        wsum += w;
     }
+    const float inv = 1.f / wsum;
+    const int node = gr / a.G, h = kvh * a.G + gr % a.G;
+    __nv_bfloat16* dst =
+        reinterpret_cast<__nv_bfloat16*>(a.O) + (((size_t)b * a.Kmax + node) * a.Hq + h) * GRAFT_HEAD_DIM + lane * 4;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+    __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+    uint2 v;
+    v.x = *reinterpret_cast<uint32_t*>(&lo);
+    v.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(dst) = v;
 }
 
+int attn_combine_launch(const AttnArgs& a, cudaStream_t st) {
+    if (a.nchunk <= 1) return GRAFT_OK;
+    const long long rows = (long long)a.B * a.Hkv * a.nRB * 128;
+    attn_combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(a);
+    count_launches(1);
+    return launch_status();
+}
+
+namespace attn_mma {
 }  // namespace attn_mma
 
 int attn_mma_launch(const AttnArgs& a, cudaStream_t st) {
@@ -348,12 +371,10 @@ int attn_mma_launch(const AttnArgs& a, cudaStream_t st) {
     }
     dim3 grid(a.nRB * a.Hkv, a.nchunk, a.B);
     attn_mma::attn_partial_kernel<<<grid, attn_mma::NT, attn_mma::SMEM, st>>>(a);
-    count_launches(a.nchunk > 1 ? 2 : 1);
-    if (a.nchunk > 1) {
-        dim3 g2(a.nRB * a.Hkv, a.B);
-        attn_mma::attn_combine_kernel<<<g2, attn_mma::NT, 0, st>>>(a);
-    }
-    return launch_status();
+    count_launches(1);
+    const int rc = launch_status();
+    if (rc != GRAFT_OK) return rc;
+    return attn_combine_launch(a, st);
 }
 
 }  // namespace graft

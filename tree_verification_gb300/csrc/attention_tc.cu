@@ -1,0 +1,484 @@
+// Tree-masked GQA attention on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
+//
+// Graft article, architecture paragraph: the hybrid tree is verified on the
+// standard tree-attention path in one target forward; Graft abstract: large
+// draft trees cost VRAM bandwidth and compute.  Each query row (tree node i,
+// query head h) attends to its request's L prefix keys and to the tree keys
+// in node i's ancestor-or-self mask, with KV head h / group.
+//
+// One CTA computes up to 256 query rows (two 128-row tiles: all query heads
+// of one KV head for 256 / group tree nodes) against one key chunk, so every
+// K/V byte fetched from HBM feeds 256 rows of tensor-core work.
+//
+// Warp roles (12 warps):
+//   warp 0      TMA producer: Q tiles once, then 64-key K/V blocks into a
+//               3-stage ring (128-byte swizzled boxes of 64 x 64 bf16)
+//   warp 1      MMA issuer (one lane): S_t = Q_t K^T into TMEM (double
+//               buffered per tile), then O_t += P_t V once softmax wrote P_t
+//   warp 2      owns the TMEM allocation (512 columns)
+//   warps 4-7   softmax + epilogue for tile 0 (TMEM lanes 0-127, one row per thread)
+//   warps 8-11  softmax + epilogue for tile 1
+// TMEM columns: S_0 [0,128) and S_1 [128,256) as two 64-column buffers each,
+// O_0 [256,384), O_1 [384,512).  P_t goes to shared memory (bf16, 128-byte
+// swizzle, K-major) where the second MMA reads it.
+//
+// Softmax keeps a per-row running maximum that is only raised (and O
+// rescaled) when a block's maximum exceeds it by more than 2^8, so the
+// rescale of O in TMEM is rare; probabilities are then bounded by 256, which
+// bf16 P and fp32 sums carry without loss of range.  The row sum adds the
+// bf16-rounded probabilities, the same values the PV product consumes.  Masked keys (ragged
+// chunk tail, tree keys outside the ancestor mask) get probability 0, and
+// the V rows of a ragged tail are zeroed in shared memory so stale cache
+// rows cannot inject NaN.
+//
+// Every mbarrier wait is bounded; on timeout the CTA raises
+// GRAFT_STATUS_TIMEOUT in the status word, stops issuing work, drains what
+// it issued (again with a bound) and frees its TMEM before returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+
+#include "attention.cuh"
+#include "common.cuh"
+#include "tc_ptx.cuh"
+
+namespace graft {
+namespace attn_tc {
+
+using namespace tc;
+
+constexpr int HD = GRAFT_HEAD_DIM;
+constexpr int BN = 64;          // keys per block
+constexpr int STAGES = 3;       // K/V ring depth
+constexpr int NTHREADS = 384;
+constexpr uint32_t BOX_BYTES = 64 * 64 * 2;             // one 64 x 64 bf16 box
+constexpr uint32_t Q_TILE_BYTES = 2 * 128 * 64 * 2;     // 128 rows x 128 dims
+constexpr uint32_t KV_STAGE_BYTES = 4 * BOX_BYTES;      // K and V, two boxes each
+constexpr uint32_t P_TILE_BYTES = 128 * BN * 2;         // 128 rows x 64 keys
+// shared memory map (offsets from a 1024-byte aligned base)
+constexpr uint32_t OFF_Q = 0;
+constexpr uint32_t OFF_KV = OFF_Q + 2 * Q_TILE_BYTES;
+constexpr uint32_t OFF_P = OFF_KV + STAGES * KV_STAGE_BYTES;
+constexpr uint32_t OFF_BAR = OFF_P + 2 * P_TILE_BYTES;
+// barriers: q_full, kv_full[3], kv_empty[3], s_full[2][2], p_full[2], pv_done[2], mma_done
+constexpr int BAR_Q = 0, BAR_KVF = 1, BAR_KVE = 4, BAR_S = 7, BAR_P = 11, BAR_PV = 13, BAR_DONE = 15, N_BARS = 16;
+constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;  // tmem slot, abort flag, counters
+constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+
+constexpr uint32_t TM_S = 0;    // + tile * 128 + buf * 64
+constexpr uint32_t TM_O = 256;  // + tile * 128
+constexpr float RESCALE_LOG2 = 8.f;
+constexpr uint64_t kWaitNs = 500000000ull;   // bound on any single wait (the kernel runs for microseconds)
+constexpr uint64_t kDrainNs = 100000000ull;  // bound on draining in-flight loads after an abort
+
+struct Maps {
+    CUtensorMap q, kc, vc, kt, vt;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ bool aborted(const volatile uint32_t* flag) { return *flag != 0; }
+
+__device__ __forceinline__ void raise_abort(volatile uint32_t* flag, int32_t* status) {
+    *flag = 1;
+    flag_status(status, GRAFT_STATUS_TIMEOUT);
+}
+
+template <int TILES>
+__global__ void __launch_bounds__(NTHREADS, 1)
+attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(gbase + OFF_MISC);
+    volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + OFF_MISC + 4);
+    auto bar = [&](int i) { return base + OFF_BAR + 8u * (uint32_t)i; };
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nrb = (a.nRB + 1) / 2;  // 256-row blocks
+    const int rb = blockIdx.x % nrb;
+    const int kvh = blockIdx.x / nrb;
+    const int c = blockIdx.y;
+    const int b = blockIdx.z;
+
+    const int Lb = a.L[b];
+    if (Lb < 0 || Lb > a.Lcap) {
+        if (tid == 0 && c == 0 && rb == 0 && kvh == 0) flag_status(a.status, GRAFT_STATUS_LENGTH);
+        return;
+    }
+    const int nck = Lb > 0 ? (Lb + a.C - 1) / a.C : 1;
+    if (c >= nck) return;
+    const int k0 = c * a.C;
+    const int k1 = min(Lb, k0 + a.C);
+    const int nb_prefix = (k1 - k0 + BN - 1) / BN;
+    const bool has_tree = (c == nck - 1);
+    const int nb = nb_prefix + (has_tree ? 1 : 0);
+    const int ragged_block = ((k1 - k0) % BN) != 0 ? nb_prefix - 1 : -1;
+    const int ragged_valid = (k1 - k0) % BN;
+
+    if (tid == 0) {
+        for (int i = 0; i < N_BARS; ++i) {
+            uint32_t cnt = 1;
+            if (i == BAR_P || i == BAR_P + 1) cnt = 128;
+            mbar_init(bar(i), cnt);
+        }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {
+        tmem_alloc(base + OFF_MISC, 512);
+        tmem_relinquish();
+        tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    int loads_issued = 0;  // K/V blocks the producer lane has armed
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            tma_prefetch_desc(&maps.q);
+            tma_prefetch_desc(&maps.kc);
+            tma_prefetch_desc(&maps.vc);
+            const int node0 = (rb * 256) / a.G;
+            const int nodes_per_tile = 128 / a.G;
+            mbar_expect_tx(bar(BAR_Q), TILES * Q_TILE_BYTES);
+            for (int t = 0; t < TILES; ++t) {
+                const int nz = b * a.Kmax + node0 + t * nodes_per_tile;
+                for (int h = 0; h < 2; ++h)
+                    tma_load_3d(base + OFF_Q + t * Q_TILE_BYTES + h * (Q_TILE_BYTES / 2), &maps.q, bar(BAR_Q), h * 64,
+                                kvh * a.G, nz);
+            }
+            for (int j = 0; j < nb; ++j) {
+                const int st = j % STAGES;
+                if (j >= STAGES) {
+                    if (!mbar_wait(bar(BAR_KVE + st), ((j / STAGES) - 1) & 1, kWaitNs)) {
+                        raise_abort(abort_flag, a.status);
+                        break;
+                    }
+                }
+                if (aborted(abort_flag)) break;
+                const uint32_t dst = base + OFF_KV + st * KV_STAGE_BYTES;
+                mbar_expect_tx(bar(BAR_KVF + st), KV_STAGE_BYTES);
+                ++loads_issued;
+                if (j < nb_prefix) {
+                    const int key = k0 + j * BN;
+                    for (int h = 0; h < 2; ++h) {
+                        tma_load_4d(dst + h * BOX_BYTES, &maps.kc, bar(BAR_KVF + st), h * 64, kvh, key, b);
+                        tma_load_4d(dst + 2 * BOX_BYTES + h * BOX_BYTES, &maps.vc, bar(BAR_KVF + st), h * 64, kvh, key, b);
+                    }
+                } else {
+                    for (int h = 0; h < 2; ++h) {
+                        tma_load_4d(dst + h * BOX_BYTES, &maps.kt, bar(BAR_KVF + st), h * 64, kvh, 0, b);
+                        tma_load_4d(dst + 2 * BOX_BYTES + h * BOX_BYTES, &maps.vt, bar(BAR_KVF + st), h * 64, kvh, 0, b);
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        const uint32_t idS = idesc_bf16(128, BN, false, false);
+        const uint32_t idO = idesc_bf16(128, HD, false, true);
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), 0, kWaitNs));
+        if (!ok) raise_abort(abort_flag, a.status);
+        auto issue_S = [&](int j) -> bool {
+            const int st = j % STAGES;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KVF + st), (j / STAGES) & 1, kWaitNs))) return false;
+            const uint32_t kv = base + OFF_KV + st * KV_STAGE_BYTES;
+            if (j == ragged_block) {
+                // zero the V rows past the chunk end (both 64-dim boxes)
+                uint8_t* v0 = gbase + OFF_KV + st * KV_STAGE_BYTES + 2 * BOX_BYTES;
+                for (int i = lane; i < (BN - ragged_valid) * 16; i += 32) {
+                    const int r = ragged_valid + i / 16, q = i % 16;
+                    *reinterpret_cast<uint4*>(v0 + (q >= 8 ? BOX_BYTES : 0) + r * 128 + (q & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            tc_fence_after();
+            if (lane == 0) {
+                for (int t = 0; t < TILES; ++t) {
+                    const uint32_t q = base + OFF_Q + t * Q_TILE_BYTES;
+                    const uint32_t d = tmem + TM_S + t * 128 + (j & 1) * 64;
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        const uint32_t off = (kk & 3) * 32;
+                        const uint64_t ad = sdesc_sw128(q + (kk >> 2) * (Q_TILE_BYTES / 2) + off, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(kv + (kk >> 2) * BOX_BYTES + off, 16, 1024);
+                        mma_bf16_ss(d, ad, bd, idS, kk > 0);
+                    }
+                    mma_commit(bar(BAR_S + t * 2 + (j & 1)));
+                }
+            }
+            __syncwarp();
+            return true;
+        };
+        if (ok) {
+            for (int j = 0; j < 2 && j < nb && ok; ++j) ok = issue_S(j);
+            if (!ok) raise_abort(abort_flag, a.status);
+        }
+        for (int j = 0; j < nb && ok; ++j) {
+            const int st = j % STAGES;
+            const uint32_t v = base + OFF_KV + st * KV_STAGE_BYTES + 2 * BOX_BYTES;
+            for (int t = 0; t < TILES && ok; ++t) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_P + t), j & 1, kWaitNs) && !aborted(abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t p = base + OFF_P + t * P_TILE_BYTES;
+                    const uint32_t d = tmem + TM_O + t * 128;
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint64_t ad = sdesc_sw128(p + kk * 32, 16, 1024);
+                        const uint64_t bd = sdesc_sw128(v + kk * 2048, BOX_BYTES, 1024);
+                        mma_bf16_ss(d, ad, bd, idO, (j > 0) || (kk > 0));
+                    }
+                    mma_commit(bar(BAR_PV + t));
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) mma_commit(bar(BAR_KVE + st));
+            __syncwarp();
+            if (j + 2 < nb) {
+                if (!issue_S(j + 2)) { ok = false; break; }
+            }
+        }
+        if (!ok && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
+        if (lane == 0) mma_commit(bar(BAR_DONE));
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int t = (warp - 4) >> 2;
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;  // row within the tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const int gr = rb * 256 + t * 128 + r;
+        const bool row_ok = (t < TILES) && gr < a.R;
+        const int node = row_ok ? gr / a.G : 0;
+        const uint64_t anc = row_ok ? a.mask[(size_t)b * a.Kmax + node] : 0ull;
+        const float sl2 = a.scale * 1.4426950408889634f;
+        float m_used = -INFINITY, l_sum = 0.f;
+        bool ok = true;
+        uint8_t* prow = gbase + OFF_P + t * P_TILE_BYTES + r * 128;
+        for (int j = 0; j < nb && t < TILES; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + t * 2 + (j & 1)), (j >> 1) & 1, kWaitNs) &&
+                                             !aborted(abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            float s[BN];
+            tmem_ld32(tmem + lane_base + TM_S + t * 128 + (j & 1) * 64, s);
+            tmem_ld32(tmem + lane_base + TM_S + t * 128 + (j & 1) * 64 + 32, s + 32);
+            tmem_wait_ld();
+            const bool tree_blk = j >= nb_prefix;
+            const int valid = tree_blk ? a.Kmax : (j == ragged_block ? ragged_valid : BN);
+            float mx = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < BN; ++i) {
+                bool keep = i < valid;
+                if (tree_blk) keep = keep && ((anc >> i) & 1ull);
+                s[i] = keep ? s[i] * sl2 : -INFINITY;
+                mx = fmaxf(mx, s[i]);
+            }
+            bool waited_pv = false;
+            if (j == 0) {
+                m_used = mx;
+            } else if (__any_sync(0xffffffffu, mx > m_used + RESCALE_LOG2)) {
+                // raise the running maximum of the rows that need it and rescale their O by
+                // 2^(m_used - m_new); the previous PV must have landed first (whole warp)
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + t), (j - 1) & 1, kWaitNs));
+                waited_pv = true;
+                if (!ok) break;
+                tc_fence_after();
+                const float m_new = fmaxf(mx, m_used);
+                const float alpha = (m_used == -INFINITY) ? 1.f : ex2(m_used - m_new);
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_base + TM_O + t * 128 + c0, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                    tmem_st32(tmem + lane_base + TM_O + t * 128 + c0, o);
+                }
+                tmem_wait_st();
+                l_sum *= alpha;
+                m_used = m_new;
+            }
+            const float mb = (m_used == -INFINITY) ? 0.f : m_used;
+            uint32_t packed[BN / 2];
+#pragma unroll
+            for (int i = 0; i < BN; i += 2) {
+                const float p0 = ex2(s[i] - mb), p1 = ex2(s[i + 1] - mb);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+                // the row sum uses the same rounded weights the PV product uses, so the
+                // output is an exact weighted mean of V under those weights
+                l_sum += __low2float(h2) + __high2float(h2);
+                packed[i / 2] = *reinterpret_cast<uint32_t*>(&h2);
+            }
+            if (j > 0 && !waited_pv) {
+                // P_t is still being read by the previous PV
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + t), (j - 1) & 1, kWaitNs));
+                if (!ok) break;
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) << 4)) =
+                    make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(bar(BAR_P + t));
+        }
+        if (!ok && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
+        // ------------------------------------------------------------ epilogue
+        if (ok && t < TILES && nb > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + t), (nb - 1) & 1, kWaitNs));
+            if (!ok) raise_abort(abort_flag, a.status);
+        }
+        if (ok && t < TILES && nb > 0) {
+            tc_fence_after();
+            const float inv = row_ok ? 1.f / l_sum : 0.f;
+            const int h = kvh * a.G + gr % a.G;
+            const bool direct = (nck == 1);
+            __nv_bfloat16* dst_o =
+                reinterpret_cast<__nv_bfloat16*>(a.O) + (((size_t)b * a.Kmax + node) * a.Hq + h) * HD;
+            const int tile = rb * 2 + t;  // 128-row tile index within (b, kvh)
+            const size_t pi = ((((size_t)b * a.Hkv + kvh) * a.nRB + tile) * a.nchunk + c) * 128 + r;
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                float o[32];
+                tmem_ld32(tmem + lane_base + TM_O + t * 128 + c0, o);
+                tmem_wait_ld();
+                if (!row_ok) continue;
+                if (direct) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 8) {
+                        uint4 v;
+                        __nv_bfloat162 x0 = __floats2bfloat162_rn(o[i] * inv, o[i + 1] * inv);
+                        __nv_bfloat162 x1 = __floats2bfloat162_rn(o[i + 2] * inv, o[i + 3] * inv);
+                        __nv_bfloat162 x2 = __floats2bfloat162_rn(o[i + 4] * inv, o[i + 5] * inv);
+                        __nv_bfloat162 x3 = __floats2bfloat162_rn(o[i + 6] * inv, o[i + 7] * inv);
+                        v.x = *reinterpret_cast<uint32_t*>(&x0);
+                        v.y = *reinterpret_cast<uint32_t*>(&x1);
+                        v.z = *reinterpret_cast<uint32_t*>(&x2);
+                        v.w = *reinterpret_cast<uint32_t*>(&x3);
+                        *reinterpret_cast<uint4*>(dst_o + c0 + i) = v;
+                    }
+                } else {
+                    float* dst = a.part_o + pi * HD;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(dst + c0 + i) =
+                            make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+                }
+            }
+            if (row_ok && !direct) a.part_lse[pi] = m_used + log2f(l_sum);
+        }
+    }
+    // ---------------------------------------------------------------- teardown
+    if (warp == 0 && lane == 0 && aborted(abort_flag)) {
+        // loads still in flight write into this CTA's shared memory: wait for each stage's
+        // last armed phase (and the Q load) before the CTA may exit
+        mbar_wait(bar(BAR_Q), 0, kDrainNs);
+        for (int st = 0; st < STAGES; ++st) {
+            const int n_issued = (loads_issued - st + STAGES - 1) / STAGES;
+            if (n_issued > 0) mbar_wait(bar(BAR_KVF + st), (n_issued - 1) & 1, kDrainNs);
+        }
+    }
+    if (warp == 2 && lane == 0) {
+        // every issued MMA has completed before TMEM is released
+        mbar_wait(bar(BAR_DONE), 0, kWaitNs);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 2) tmem_dealloc(tmem, 512);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+bool encode(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
+            const cuuint32_t* box) {
+    auto enc = encoder();
+    if (enc == nullptr) return false;
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace attn_tc
+
+bool attn_tc_supported(int G) { return G >= 1 && G <= 128 && (128 % G) == 0; }
+
+int attn_tc_launch(const AttnArgs& a, cudaStream_t st) {
+    using namespace attn_tc;
+    Maps m;
+    const cuuint64_t es = 2;
+    // Q: (dim, head, node) over [B*Kmax][Hq][128]
+    {
+        cuuint64_t dims[3] = {HD, (cuuint64_t)a.Hq, (cuuint64_t)a.B * a.Kmax};
+        cuuint64_t strides[2] = {HD * es, (cuuint64_t)a.Hq * HD * es};
+        cuuint32_t box[3] = {64, (cuuint32_t)a.G, (cuuint32_t)(128 / a.G)};
+        if (!encode(&m.q, a.Q, 3, dims, strides, box)) return GRAFT_ERR_CUDA;
+    }
+    // caches: (dim, kv head, position, request) over [B][Lcap][Hkv][128]
+    {
+        const cuuint64_t Lc = a.Lcap > 0 ? (cuuint64_t)a.Lcap : 1;
+        cuuint64_t dims[4] = {HD, (cuuint64_t)a.Hkv, Lc, (cuuint64_t)a.B};
+        cuuint64_t strides[3] = {HD * es, (cuuint64_t)a.Hkv * HD * es, Lc * a.Hkv * HD * es};
+        cuuint32_t box[4] = {64, 1, BN, 1};
+        const void* kc = a.Kc ? a.Kc : a.Kt;  // an empty cache is never read
+        const void* vc = a.Vc ? a.Vc : a.Vt;
+        if (!encode(&m.kc, kc, 4, dims, strides, box)) return GRAFT_ERR_CUDA;
+        if (!encode(&m.vc, vc, 4, dims, strides, box)) return GRAFT_ERR_CUDA;
+    }
+    // tree KV: (dim, kv head, node, request) over [B][Kmax][Hkv][128]; nodes >= Kmax read as zeros
+    {
+        cuuint64_t dims[4] = {HD, (cuuint64_t)a.Hkv, (cuuint64_t)a.Kmax, (cuuint64_t)a.B};
+        cuuint64_t strides[3] = {HD * es, (cuuint64_t)a.Hkv * HD * es, (cuuint64_t)a.Kmax * a.Hkv * HD * es};
+        cuuint32_t box[4] = {64, 1, BN, 1};
+        if (!encode(&m.kt, a.Kt, 4, dims, strides, box)) return GRAFT_ERR_CUDA;
+        if (!encode(&m.vt, a.Vt, 4, dims, strides, box)) return GRAFT_ERR_CUDA;
+    }
+    const bool two = a.nRB > 1;
+    static bool attr_set[2][64] = {{false}};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < 64 && !attr_set[two][dev]) {
+        cudaError_t e = two ? cudaFuncSetAttribute(attn_tc_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)SMEM_BYTES)
+                            : cudaFuncSetAttribute(attn_tc_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   (int)SMEM_BYTES);
+        if (e != cudaSuccess) return GRAFT_ERR_CUDA;
+        attr_set[two][dev] = true;
+    }
+    const int nrb = (a.nRB + 1) / 2;
+    dim3 grid(nrb * a.Hkv, a.nchunk, a.B);
+    if (two)
+        attn_tc_kernel<2><<<grid, NTHREADS, SMEM_BYTES, st>>>(m, a);
+    else
+        attn_tc_kernel<1><<<grid, NTHREADS, SMEM_BYTES, st>>>(m, a);
+    count_launches(1);
+    const int rc = launch_status();
+    if (rc != GRAFT_OK) return rc;
+    return attn_combine_launch(a, st);
+}
+
+}  // namespace graft
