@@ -207,6 +207,8 @@ def _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed, layer=0):
     (2, 64, 4, 64, [2000, 63], 2048),          # group 16: eight row blocks
     (4, 16, 16, 5, [300, 64, 65, 129], 320),   # no grouping, Kmax not a multiple of 8
     (1, 8, 1, 1, [999], 1024),                 # single-node tree: decode attention
+    (2, 16, 2, 48, [1500, 300], 1536),         # 384 rows: an odd tile count, split keys
+    (1, 64, 4, 5, [700], 768),                 # group 16, 80 rows: one partial tile
     (2, 12, 4, 64, [1000, 3000], 3072),        # group 3: the mma.sync path
     (3, 24, 4, 40, [0, 129, 700], 768),        # group 6, 240 rows: the mma.sync path
 ])

@@ -11,25 +11,35 @@
 // K/V byte fetched from HBM feeds 256 rows of tensor-core work.
 //
 // Warp roles (12 warps):
-//   warp 0      TMA producer: Q tiles once, then 64-key K/V blocks into a
-//               3-stage ring (128-byte swizzled boxes of 64 x 64 bf16)
+//   warp 0      TMA producer: Q tiles once, then 64-key K blocks into a
+//               5-stage ring (128-byte swizzled boxes of 64 x 64 bf16);
+//               a K stage is released as soon as its S product has run
+//   warp 3      TMA producer: V blocks into their own 5-stage ring, a stage
+//               released once both tiles' PV products have run; with K
+//               freed early the K loads run ahead of the V loads
 //   warp 1      MMA issuer (one lane): S_t = Q_t K^T into TMEM (double
-//               buffered per tile), then O_t += P_t V once softmax wrote P_t
+//               buffered per tile), then O_t += P_t V with P_t read from TMEM;
+//               shared-memory descriptors are built once and offset per MMA
 //   warp 2      owns the TMEM allocation (512 columns)
 //   warps 4-7   softmax + epilogue for tile 0 (TMEM lanes 0-127, one row per thread)
 //   warps 8-11  softmax + epilogue for tile 1
 // TMEM columns: S_0 [0,128) and S_1 [128,256) as two 64-column buffers each,
-// O_0 [256,384), O_1 [384,512).  P_t goes to shared memory (bf16, 128-byte
-// swizzle, K-major) where the second MMA reads it.
+// O_0 [256,384), O_1 [384,512).  Softmax overwrites the first 32 columns of
+// its S buffer with P as packed bf16 pairs; the PV MMA takes that as its A
+// operand straight from TMEM, so P never touches shared memory and the two
+// S buffers double-buffer P as well.
 //
 // Softmax keeps a per-row running maximum that is only raised (and O
 // rescaled) when a block's maximum exceeds it by more than 2^8, so the
 // rescale of O in TMEM is rare; probabilities are then bounded by 256, which
 // bf16 P and fp32 sums carry without loss of range.  The row sum adds the
-// bf16-rounded probabilities, the same values the PV product consumes.  Masked keys (ragged
-// chunk tail, tree keys outside the ancestor mask) get probability 0, and
-// the V rows of a ragged tail are zeroed in shared memory so stale cache
-// rows cannot inject NaN.
+// bf16-rounded probabilities, the same values the PV product consumes.
+// Masked keys (ragged chunk tail, tree keys outside the ancestor mask) get
+// probability 0, and the V rows of a ragged tail are zeroed in shared memory
+// so stale cache rows cannot inject NaN.
+//
+// The epilogue stages each tile's rows through the freed K/V ring memory and
+// writes them out along contiguous rows.
 //
 // Every mbarrier wait is bounded; on timeout the CTA raises
 // GRAFT_STATUS_TIMEOUT in the status word, stops issuing work, drains what
@@ -50,21 +60,37 @@ using namespace tc;
 
 constexpr int HD = GRAFT_HEAD_DIM;
 constexpr int BN = 64;          // keys per block
-constexpr int STAGES = 3;       // K/V ring depth
+constexpr int SK = 5;           // K ring depth
+constexpr int SV = 5;           // V ring depth
 constexpr int NTHREADS = 384;
 constexpr uint32_t BOX_BYTES = 64 * 64 * 2;             // one 64 x 64 bf16 box
 constexpr uint32_t Q_TILE_BYTES = 2 * 128 * 64 * 2;     // 128 rows x 128 dims
-constexpr uint32_t KV_STAGE_BYTES = 4 * BOX_BYTES;      // K and V, two boxes each
-constexpr uint32_t P_TILE_BYTES = 128 * BN * 2;         // 128 rows x 64 keys
+constexpr uint32_t BLK_BYTES = 2 * BOX_BYTES;           // one K or V block (64 keys x 128 dims)
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_KV = OFF_Q + 2 * Q_TILE_BYTES;
-constexpr uint32_t OFF_P = OFF_KV + STAGES * KV_STAGE_BYTES;
-constexpr uint32_t OFF_BAR = OFF_P + 2 * P_TILE_BYTES;
-// barriers: q_full, kv_full[3], kv_empty[3], s_full[2][2], p_full[2], pv_done[2], mma_done
-constexpr int BAR_Q = 0, BAR_KVF = 1, BAR_KVE = 4, BAR_S = 7, BAR_P = 11, BAR_PV = 13, BAR_DONE = 15, N_BARS = 16;
-constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;  // tmem slot, abort flag, counters
+constexpr uint32_t OFF_K = OFF_Q + 2 * Q_TILE_BYTES;
+constexpr uint32_t OFF_V = OFF_K + SK * BLK_BYTES;
+constexpr uint32_t OFF_BAR = OFF_V + SV * BLK_BYTES;
+constexpr uint32_t OFF_STAGE = OFF_K;  // epilogue staging reuses the rings once every MMA has run
+// barriers
+constexpr int BAR_Q = 0;
+constexpr int BAR_KF = BAR_Q + 1;     // [SK] K block landed
+constexpr int BAR_KE = BAR_KF + SK;   // [SK] K block consumed by its S product
+constexpr int BAR_VF = BAR_KE + SK;   // [SV] V block landed
+constexpr int BAR_VE = BAR_VF + SV;   // [SV] V block consumed by both PV products
+constexpr int BAR_S = BAR_VE + SV;    // [tile][buf] S ready in TMEM
+// p_full is per S/P buffer: softmax may finish block j + 1 before the MMA thread has consumed
+// block j, and a single barrier per tile could then complete two phases unobserved.  Block
+// j + 2 cannot be written before S(j + 2) is issued, which follows the consumption of block j.
+constexpr int BAR_P = BAR_S + 4;      // [tile][buf] P written to TMEM (128 arrivals)
+constexpr int BAR_PV = BAR_P + 4;     // [tile] PV product completed
+constexpr int BAR_DONE = BAR_PV + 2;  // every MMA completed (one-shot)
+constexpr int BAR_EPI = BAR_DONE + 1; // [tile] staging written (128 arrivals, one-shot)
+constexpr int N_BARS = BAR_EPI + 2;
+constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;  // tmem slot, abort flag
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+static_assert(2 * 128 * 128 * 4 <= SK * BLK_BYTES + SV * BLK_BYTES, "staging fits in the rings");
 
 constexpr uint32_t TM_S = 0;    // + tile * 128 + buf * 64
 constexpr uint32_t TM_O = 256;  // + tile * 128
@@ -125,7 +151,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     if (tid == 0) {
         for (int i = 0; i < N_BARS; ++i) {
             uint32_t cnt = 1;
-            if (i == BAR_P || i == BAR_P + 1) cnt = 128;
+            if ((i >= BAR_P && i < BAR_P + 4) || i == BAR_EPI || i == BAR_EPI + 1) cnt = 128;
             mbar_init(bar(i), cnt);
         }
         *abort_flag = 0;
@@ -140,13 +166,22 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    int loads_issued = 0;  // K/V blocks the producer lane has armed
+    int k_issued = 0, v_issued = 0;  // blocks the producer lanes have armed
+    auto load_block = [&](int j, const CUtensorMap* prefix_map, const CUtensorMap* tree_map, uint32_t dst,
+                          uint32_t full) {
+        mbar_expect_tx(full, BLK_BYTES);
+        for (int h = 0; h < 2; ++h) {
+            if (j < nb_prefix)
+                tma_load_4d(dst + h * BOX_BYTES, prefix_map, full, h * 64, kvh, k0 + j * BN, b);
+            else
+                tma_load_4d(dst + h * BOX_BYTES, tree_map, full, h * 64, kvh, 0, b);
+        }
+    };
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer
+        // ------------------------------------------------------------ TMA producer: Q, then K blocks
         if (lane == 0) {
             tma_prefetch_desc(&maps.q);
             tma_prefetch_desc(&maps.kc);
-            tma_prefetch_desc(&maps.vc);
             const int node0 = (rb * 256) / a.G;
             const int nodes_per_tile = 128 / a.G;
             mbar_expect_tx(bar(BAR_Q), TILES * Q_TILE_BYTES);
@@ -157,44 +192,71 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                                 kvh * a.G, nz);
             }
             for (int j = 0; j < nb; ++j) {
-                const int st = j % STAGES;
-                if (j >= STAGES) {
-                    if (!mbar_wait(bar(BAR_KVE + st), ((j / STAGES) - 1) & 1, kWaitNs)) {
-                        raise_abort(abort_flag, a.status);
-                        break;
-                    }
+                // a K stage frees as soon as its S product has run
+                if (j >= SK && !mbar_wait(bar(BAR_KE + j % SK), ((j / SK) - 1) & 1, kWaitNs)) {
+                    raise_abort(abort_flag, a.status);
+                    break;
                 }
                 if (aborted(abort_flag)) break;
-                const uint32_t dst = base + OFF_KV + st * KV_STAGE_BYTES;
-                mbar_expect_tx(bar(BAR_KVF + st), KV_STAGE_BYTES);
-                ++loads_issued;
-                if (j < nb_prefix) {
-                    const int key = k0 + j * BN;
-                    for (int h = 0; h < 2; ++h) {
-                        tma_load_4d(dst + h * BOX_BYTES, &maps.kc, bar(BAR_KVF + st), h * 64, kvh, key, b);
-                        tma_load_4d(dst + 2 * BOX_BYTES + h * BOX_BYTES, &maps.vc, bar(BAR_KVF + st), h * 64, kvh, key, b);
-                    }
-                } else {
-                    for (int h = 0; h < 2; ++h) {
-                        tma_load_4d(dst + h * BOX_BYTES, &maps.kt, bar(BAR_KVF + st), h * 64, kvh, 0, b);
-                        tma_load_4d(dst + 2 * BOX_BYTES + h * BOX_BYTES, &maps.vt, bar(BAR_KVF + st), h * 64, kvh, 0, b);
-                    }
+                load_block(j, &maps.kc, &maps.kt, base + OFF_K + (j % SK) * BLK_BYTES, bar(BAR_KF + j % SK));
+                ++k_issued;
+            }
+        }
+    } else if (warp == 3) {
+        // ------------------------------------------------------------ TMA producer: V blocks
+        if (lane == 0) {
+            tma_prefetch_desc(&maps.vc);
+            for (int j = 0; j < nb; ++j) {
+                // a V stage frees once both tiles' PV products have run
+                if (j >= SV && !mbar_wait(bar(BAR_VE + j % SV), ((j / SV) - 1) & 1, kWaitNs)) {
+                    raise_abort(abort_flag, a.status);
+                    break;
                 }
+                if (aborted(abort_flag)) break;
+                load_block(j, &maps.vc, &maps.vt, base + OFF_V + (j % SV) * BLK_BYTES, bar(BAR_VF + j % SV));
+                ++v_issued;
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        // ------------------------------------------------------------ MMA issuer (lane 0 issues)
         const uint32_t idS = idesc_bf16(128, BN, false, false);
         const uint32_t idO = idesc_bf16(128, HD, false, true);
         bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), 0, kWaitNs));
-        if (!ok) raise_abort(abort_flag, a.status);
+        // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
+        // start-address field, which sits in the low bits and cannot carry out of them here
+        // (every shared-memory address is below 256 KB).
+        const uint64_t q_desc = sdesc_sw128(base + OFF_Q, 16, 1024);
+        const uint64_t k_desc = sdesc_sw128(base + OFF_K, 16, 1024);
+        const uint64_t v_desc = sdesc_sw128(base + OFF_V, BOX_BYTES, 1024);
+        // S(j) for every tile into S/P buffer j % 2, then release K(j)
         auto issue_S = [&](int j) -> bool {
-            const int st = j % STAGES;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KVF + st), (j / STAGES) & 1, kWaitNs))) return false;
-            const uint32_t kv = base + OFF_KV + st * KV_STAGE_BYTES;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KF + j % SK), (j / SK) & 1, kWaitNs))) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint64_t kd = k_desc + (((j % SK) * BLK_BYTES) >> 4);
+#pragma unroll
+                for (int t = 0; t < TILES; ++t) {
+                    const uint32_t d = tmem + TM_S + t * 128 + (j & 1) * 64;
+#pragma unroll
+                    for (int kk = 0; kk < HD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
+                        const uint32_t qoff = t * Q_TILE_BYTES + (kk >> 2) * (Q_TILE_BYTES / 2) + (kk & 3) * 32;
+                        mma_bf16_ss(d, q_desc + (qoff >> 4), kd + (off >> 4), idS, kk > 0);
+                    }
+                    mma_commit(bar(BAR_S + t * 2 + (j & 1)));
+                }
+                mma_commit(bar(BAR_KE + j % SK));
+            }
+            __syncwarp();
+            return true;
+        };
+        for (int j = 0; j < 2 && j < nb && ok; ++j) ok = issue_S(j);
+        for (int j = 0; j < nb && ok; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + j % SV), (j / SV) & 1, kWaitNs));
+            if (!ok) break;
             if (j == ragged_block) {
-                // zero the V rows past the chunk end (both 64-dim boxes)
-                uint8_t* v0 = gbase + OFF_KV + st * KV_STAGE_BYTES + 2 * BOX_BYTES;
+                // zero the V rows past the chunk end (both 64-dim boxes) before any PV reads them
+                uint8_t* v0 = gbase + OFF_V + (j % SV) * BLK_BYTES;
                 for (int i = lane; i < (BN - ragged_valid) * 16; i += 32) {
                     const int r = ragged_valid + i / 16, q = i % 16;
                     *reinterpret_cast<uint4*>(v0 + (q >= 8 ? BOX_BYTES : 0) + r * 128 + (q & 7) * 16) =
@@ -203,54 +265,28 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            tc_fence_after();
-            if (lane == 0) {
-                for (int t = 0; t < TILES; ++t) {
-                    const uint32_t q = base + OFF_Q + t * Q_TILE_BYTES;
-                    const uint32_t d = tmem + TM_S + t * 128 + (j & 1) * 64;
-                    for (int kk = 0; kk < HD / 16; ++kk) {
-                        const uint32_t off = (kk & 3) * 32;
-                        const uint64_t ad = sdesc_sw128(q + (kk >> 2) * (Q_TILE_BYTES / 2) + off, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(kv + (kk >> 2) * BOX_BYTES + off, 16, 1024);
-                        mma_bf16_ss(d, ad, bd, idS, kk > 0);
-                    }
-                    mma_commit(bar(BAR_S + t * 2 + (j & 1)));
-                }
-            }
-            __syncwarp();
-            return true;
-        };
-        if (ok) {
-            for (int j = 0; j < 2 && j < nb && ok; ++j) ok = issue_S(j);
-            if (!ok) raise_abort(abort_flag, a.status);
-        }
-        for (int j = 0; j < nb && ok; ++j) {
-            const int st = j % STAGES;
-            const uint32_t v = base + OFF_KV + st * KV_STAGE_BYTES + 2 * BOX_BYTES;
             for (int t = 0; t < TILES && ok; ++t) {
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_P + t), j & 1, kWaitNs) && !aborted(abort_flag));
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(bar(BAR_P + t * 2 + (j & 1)), (j >> 1) & 1, kWaitNs) && !aborted(abort_flag));
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
-                    const uint32_t p = base + OFF_P + t * P_TILE_BYTES;
+                    const uint32_t p = tmem + TM_S + t * 128 + (j & 1) * 64;  // P as packed bf16 pairs
                     const uint32_t d = tmem + TM_O + t * 128;
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t ad = sdesc_sw128(p + kk * 32, 16, 1024);
-                        const uint64_t bd = sdesc_sw128(v + kk * 2048, BOX_BYTES, 1024);
-                        mma_bf16_ss(d, ad, bd, idO, (j > 0) || (kk > 0));
-                    }
+                    const uint64_t vd = v_desc + (((j % SV) * BLK_BYTES) >> 4);
+                    mma_bf16_ts(d, p, vd, idO, j > 0);
+#pragma unroll
+                    for (int kk = 1; kk < BN / 16; ++kk) mma_bf16_ts(d, p + kk * 8, vd + ((kk * 2048) >> 4), idO, true);
                     mma_commit(bar(BAR_PV + t));
                 }
                 __syncwarp();
             }
             if (!ok) break;
-            if (lane == 0) mma_commit(bar(BAR_KVE + st));
+            if (lane == 0) mma_commit(bar(BAR_VE + j % SV));
             __syncwarp();
-            if (j + 2 < nb) {
-                if (!issue_S(j + 2)) { ok = false; break; }
-            }
+            if (j + 2 < nb) ok = issue_S(j + 2);
         }
-        if (!ok && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
+        if (!ok && lane == 0 && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
         if (lane == 0) mma_commit(bar(BAR_DONE));
         __syncwarp();
     } else if (warp >= 4) {
@@ -264,36 +300,41 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         const int node = row_ok ? gr / a.G : 0;
         const uint64_t anc = row_ok ? a.mask[(size_t)b * a.Kmax + node] : 0ull;
         const float sl2 = a.scale * 1.4426950408889634f;
-        float m_used = -INFINITY, l_sum = 0.f;
+        float m_used = -INFINITY, l_sum = 0.f;  // running max (log2 units) and row sum
         bool ok = true;
-        uint8_t* prow = gbase + OFF_P + t * P_TILE_BYTES + r * 128;
         for (int j = 0; j < nb && t < TILES; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + t * 2 + (j & 1)), (j >> 1) & 1, kWaitNs) &&
                                              !aborted(abort_flag));
             if (!ok) break;
             tc_fence_after();
+            const uint32_t sbuf = tmem + lane_base + TM_S + t * 128 + (j & 1) * 64;
             float s[BN];
-            tmem_ld32(tmem + lane_base + TM_S + t * 128 + (j & 1) * 64, s);
-            tmem_ld32(tmem + lane_base + TM_S + t * 128 + (j & 1) * 64 + 32, s + 32);
+            tmem_ld32(sbuf, s);
+            tmem_ld32(sbuf + 32, s + 32);
             tmem_wait_ld();
             const bool tree_blk = j >= nb_prefix;
-            const int valid = tree_blk ? a.Kmax : (j == ragged_block ? ragged_valid : BN);
-            float mx = -INFINITY;
+            if (tree_blk || j == ragged_block) {
+                // only the ragged tail and the tree block need masking
+                const int valid = tree_blk ? a.Kmax : ragged_valid;
 #pragma unroll
-            for (int i = 0; i < BN; ++i) {
-                bool keep = i < valid;
-                if (tree_blk) keep = keep && ((anc >> i) & 1ull);
-                s[i] = keep ? s[i] * sl2 : -INFINITY;
-                mx = fmaxf(mx, s[i]);
+                for (int i = 0; i < BN; ++i) {
+                    bool keep = i < valid;
+                    if (tree_blk) keep = keep && ((anc >> i) & 1ull);
+                    s[i] = keep ? s[i] : -INFINITY;
+                }
             }
-            bool waited_pv = false;
+            float mx = fmaxf(s[0], s[1]);
+#pragma unroll
+            for (int i = 2; i < BN; i += 2) mx = fmaxf(mx, fmaxf(s[i], s[i + 1]));
+            mx *= sl2;  // sl2 > 0: the maximum commutes with the scale
             if (j == 0) {
                 m_used = mx;
             } else if (__any_sync(0xffffffffu, mx > m_used + RESCALE_LOG2)) {
                 // raise the running maximum of the rows that need it and rescale their O by
-                // 2^(m_used - m_new); the previous PV must have landed first (whole warp)
+                // 2^(m_used - m_new); the previous PV must have landed first (whole warp).
+                // S(j) was committed after PV(j - 2) was issued, so pv_done has completed phase
+                // j - 2 and cannot have completed phase j yet: its parity names phase j - 1.
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + t), (j - 1) & 1, kWaitNs));
-                waited_pv = true;
                 if (!ok) break;
                 tc_fence_after();
                 const float m_new = fmaxf(mx, m_used);
@@ -310,84 +351,118 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 l_sum *= alpha;
                 m_used = m_new;
             }
-            const float mb = (m_used == -INFINITY) ? 0.f : m_used;
-            uint32_t packed[BN / 2];
+            const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+            const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
+            float2 acc = make_float2(0.f, 0.f);
+            float packed[BN / 2];
 #pragma unroll
             for (int i = 0; i < BN; i += 2) {
-                const float p0 = ex2(s[i] - mb), p1 = ex2(s[i + 1] - mb);
-                __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
-                // the row sum uses the same rounded weights the PV product uses, so the
-                // output is an exact weighted mean of V under those weights
-                l_sum += __low2float(h2) + __high2float(h2);
-                packed[i / 2] = *reinterpret_cast<uint32_t*>(&h2);
+                const float2 x = __ffma2_rn(make_float2(s[i], s[i + 1]), sc2, nm2);
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2(x.x), ex2(x.y));
+                // the row sum adds the same rounded weights the PV product uses
+                acc = __fadd2_rn(acc, make_float2(__low2float(h2), __high2float(h2)));
+                packed[i / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&h2));
             }
-            if (j > 0 && !waited_pv) {
-                // P_t is still being read by the previous PV
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + t), (j - 1) & 1, kWaitNs));
-                if (!ok) break;
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                *reinterpret_cast<uint4*>(prow + ((q ^ (r & 7)) << 4)) =
-                    make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-            }
-            fence_proxy_async_smem();
+            l_sum += acc.x + acc.y;
+            tmem_st32(sbuf, packed);  // P over the first 32 columns of its S buffer
+            tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(BAR_P + t));
+            mbar_arrive(bar(BAR_P + t * 2 + (j & 1)));
         }
         if (!ok && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
         // ------------------------------------------------------------ epilogue
-        if (ok && t < TILES && nb > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + t), (nb - 1) & 1, kWaitNs));
-            if (!ok) raise_abort(abort_flag, a.status);
-        }
-        if (ok && t < TILES && nb > 0) {
-            tc_fence_after();
-            const float inv = row_ok ? 1.f / l_sum : 0.f;
-            const int h = kvh * a.G + gr % a.G;
+        if (t < TILES) {
+            if (ok && nb > 0) {
+                // every MMA, the last PV included, has completed (one-shot barrier: no phase ambiguity)
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_DONE), 0, kWaitNs));
+                if (!ok) raise_abort(abort_flag, a.status);
+            }
             const bool direct = (nck == 1);
-            __nv_bfloat16* dst_o =
-                reinterpret_cast<__nv_bfloat16*>(a.O) + (((size_t)b * a.Kmax + node) * a.Hq + h) * HD;
-            const int tile = rb * 2 + t;  // 128-row tile index within (b, kvh)
-            const size_t pi = ((((size_t)b * a.Hkv + kvh) * a.nRB + tile) * a.nchunk + c) * 128 + r;
-            for (int c0 = 0; c0 < HD; c0 += 32) {
-                float o[32];
-                tmem_ld32(tmem + lane_base + TM_O + t * 128 + c0, o);
-                tmem_wait_ld();
-                if (!row_ok) continue;
-                if (direct) {
+            const float inv = (row_ok && l_sum > 0.f) ? 1.f / l_sum : 0.f;
+            if (ok) {
+                tc_fence_after();
+                // stage this thread's row, 16-byte chunks permuted by the row index so a warp's
+                // 32 rows spread over all banks
+                uint8_t* srow = gbase + OFF_STAGE + t * (128 * 512) + r * (direct ? 256 : 512);
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_base + TM_O + t * 128 + c0, o);
+                    tmem_wait_ld();
+                    if (direct) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        uint4 v;
-                        __nv_bfloat162 x0 = __floats2bfloat162_rn(o[i] * inv, o[i + 1] * inv);
-                        __nv_bfloat162 x1 = __floats2bfloat162_rn(o[i + 2] * inv, o[i + 3] * inv);
-                        __nv_bfloat162 x2 = __floats2bfloat162_rn(o[i + 4] * inv, o[i + 5] * inv);
-                        __nv_bfloat162 x3 = __floats2bfloat162_rn(o[i + 6] * inv, o[i + 7] * inv);
-                        v.x = *reinterpret_cast<uint32_t*>(&x0);
-                        v.y = *reinterpret_cast<uint32_t*>(&x1);
-                        v.z = *reinterpret_cast<uint32_t*>(&x2);
-                        v.w = *reinterpret_cast<uint32_t*>(&x3);
-                        *reinterpret_cast<uint4*>(dst_o + c0 + i) = v;
+                        for (int i = 0; i < 32; i += 8) {
+                            uint4 v;
+                            __nv_bfloat162 x0 = __floats2bfloat162_rn(o[i] * inv, o[i + 1] * inv);
+                            __nv_bfloat162 x1 = __floats2bfloat162_rn(o[i + 2] * inv, o[i + 3] * inv);
+                            __nv_bfloat162 x2 = __floats2bfloat162_rn(o[i + 4] * inv, o[i + 5] * inv);
+                            __nv_bfloat162 x3 = __floats2bfloat162_rn(o[i + 6] * inv, o[i + 7] * inv);
+                            v.x = *reinterpret_cast<uint32_t*>(&x0);
+                            v.y = *reinterpret_cast<uint32_t*>(&x1);
+                            v.z = *reinterpret_cast<uint32_t*>(&x2);
+                            v.w = *reinterpret_cast<uint32_t*>(&x3);
+                            const int chunk = (c0 + i) / 8;  // 0..15
+                            *reinterpret_cast<uint4*>(srow + ((chunk ^ (r & 15)) << 4)) = v;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const int chunk = (c0 + i) / 4;  // 0..31
+                            *reinterpret_cast<float4*>(srow + ((chunk ^ (r & 31)) << 4)) =
+                                make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+                        }
                     }
-                } else {
-                    float* dst = a.part_o + pi * HD;
-#pragma unroll
-                    for (int i = 0; i < 32; i += 4)
-                        *reinterpret_cast<float4*>(dst + c0 + i) =
-                            make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
                 }
             }
-            if (row_ok && !direct) a.part_lse[pi] = m_used + log2f(l_sum);
+            mbar_arrive(bar(BAR_EPI + t));
+            const bool staged = __all_sync(0xffffffffu, mbar_wait(bar(BAR_EPI + t), 0, kWaitNs));
+            if (!staged) {
+                raise_abort(abort_flag, a.status);
+                ok = false;
+            }
+            if (ok) {
+                // write the tile out along contiguous rows; 128 threads of this tile
+                const int tix = quad * 32 + lane;
+                const uint8_t* stile = gbase + OFF_STAGE + t * (128 * 512);
+                if (direct) {
+                    for (int k = tix; k < 128 * 16; k += 128) {
+                        const int row = k >> 4, cc = k & 15;
+                        const int g = rb * 256 + t * 128 + row;
+                        if (g >= a.R) continue;
+                        const int nd = g / a.G, hh = kvh * a.G + g % a.G;
+                        const uint4 v = *reinterpret_cast<const uint4*>(stile + row * 256 + ((cc ^ (row & 15)) << 4));
+                        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.O) +
+                                             (((size_t)b * a.Kmax + nd) * a.Hq + hh) * HD + cc * 8;
+                        *reinterpret_cast<uint4*>(dst) = v;
+                    }
+                } else if (rb * 2 + t < a.nRB) {  // an odd tile count leaves the last block's second tile empty
+                    const int tile = rb * 2 + t;  // 128-row tile index within (b, kvh)
+                    const size_t pbase = ((((size_t)b * a.Hkv + kvh) * a.nRB + tile) * a.nchunk + c) * 128;
+                    float* dst = a.part_o + pbase * HD;
+                    for (int k = tix; k < 128 * 32; k += 128) {
+                        const int row = k >> 5, cc = k & 31;
+                        const float4 v = *reinterpret_cast<const float4*>(stile + row * 512 + ((cc ^ (row & 31)) << 4));
+                        *reinterpret_cast<float4*>(dst + row * HD + cc * 4) = v;
+                    }
+                    if (row_ok) a.part_lse[pbase + r] = m_used + log2f(l_sum);
+                }
+            }
         }
     }
     // ---------------------------------------------------------------- teardown
-    if (warp == 0 && lane == 0 && aborted(abort_flag)) {
-        // loads still in flight write into this CTA's shared memory: wait for each stage's
-        // last armed phase (and the Q load) before the CTA may exit
-        mbar_wait(bar(BAR_Q), 0, kDrainNs);
-        for (int st = 0; st < STAGES; ++st) {
-            const int n_issued = (loads_issued - st + STAGES - 1) / STAGES;
-            if (n_issued > 0) mbar_wait(bar(BAR_KVF + st), (n_issued - 1) & 1, kDrainNs);
+    if (lane == 0 && (warp == 0 || warp == 3) && aborted(abort_flag)) {
+        // loads still in flight write into this CTA's shared memory: each producer waits for
+        // the last armed phase of every stage it used (and the Q load) before the CTA may exit
+        if (warp == 0) {
+            mbar_wait(bar(BAR_Q), 0, kDrainNs);
+            for (int st = 0; st < SK; ++st) {
+                const int n = (k_issued - st + SK - 1) / SK;
+                if (n > 0) mbar_wait(bar(BAR_KF + st), (n - 1) & 1, kDrainNs);
+            }
+        } else {
+            for (int st = 0; st < SV; ++st) {
+                const int n = (v_issued - st + SV - 1) / SV;
+                if (n > 0) mbar_wait(bar(BAR_VF + st), (n - 1) & 1, kDrainNs);
+            }
         }
     }
     if (warp == 2 && lane == 0) {
