@@ -224,6 +224,25 @@ def test_attention_parity(B, Hq, Hkv, Kmax, Ls, Lcap):
     assert_attention_close(to_np(O), ref)
 
 
+@pytest.mark.parametrize("tiles", ["1", "2"])
+@pytest.mark.parametrize("B,Hq,Hkv,Kmax,Ls,Lcap", [
+    (2, 32, 8, 64, [4096, 777], 4160),
+    (3, 16, 2, 48, [0, 1500, 300], 1536),
+])
+def test_attention_parity_both_tilings(monkeypatch, tiles, B, Hq, Hkv, Kmax, Ls, Lcap):
+    """The tcgen05 path with one and with two 128-row tiles per CTA."""
+    monkeypatch.setenv("GRAFT_ATTN_TILES", tiles)
+    Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed=7 * B + Kmax)
+    status = _status()
+    O = gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), torch.from_numpy(masks.view(np.int64)).to(DEV),
+                                  1 / math.sqrt(128), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oatt.tree_attention(to_np(Q), to_np(Kc), to_np(Vc), to_np(Kt), to_np(Vt), L.numpy(), masks,
+                              1 / math.sqrt(128))
+    assert_attention_close(to_np(O), ref)
+
+
 def test_attention_length_past_capacity_is_flagged():
     Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(1, 8, 2, 32, [700], 640, seed=3)
     status = _status()

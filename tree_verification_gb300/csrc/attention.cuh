@@ -9,6 +9,7 @@ namespace graft {
 struct AttnArgs {
     int B, Hq, Hkv, G, Kmax, R;  // R = Kmax * G query rows per (request, KV head)
     int nRB;                      // 128-row blocks per (request, KV head)
+    int tiles;                    // 128-row tiles per CTA on the tcgen05 path (1 or 2)
     int C;                        // prefix keys per chunk (multiple of 64)
     int nchunk;                   // chunks per (request, KV head) allowed by Lcap
     int Lcap;

@@ -6,9 +6,10 @@
 // query head h) attends to its request's L prefix keys and to the tree keys
 // in node i's ancestor-or-self mask, with KV head h / group.
 //
-// One CTA computes up to 256 query rows (two 128-row tiles: all query heads
-// of one KV head for 256 / group tree nodes) against one key chunk, so every
-// K/V byte fetched from HBM feeds 256 rows of tensor-core work.
+// One CTA computes one or two 128-row tiles of query rows (all query heads of
+// one KV head for 128 / group tree nodes per tile) against one key chunk;
+// with two tiles every K/V byte fetched from HBM feeds 256 rows of
+// tensor-core work, with one tile small problems spread over more CTAs.
 //
 // Warp roles (12 warps):
 //   warp 0      TMA producer: Q tiles once, then 64-key K blocks into a
@@ -78,13 +79,13 @@ constexpr int BAR_KF = BAR_Q + 1;     // [SK] K block landed
 constexpr int BAR_KE = BAR_KF + SK;   // [SK] K block consumed by its S product
 constexpr int BAR_VF = BAR_KE + SK;   // [SV] V block landed
 constexpr int BAR_VE = BAR_VF + SV;   // [SV] V block consumed by both PV products
-constexpr int BAR_S = BAR_VE + SV;    // [tile][buf] S ready in TMEM
+constexpr int BAR_S = BAR_VE + SV;    // [buf] S of both tiles ready in TMEM
+// s_full is per S/P buffer and covers both tiles (one commit per block).
 // p_full is per S/P buffer: softmax may finish block j + 1 before the MMA thread has consumed
 // block j, and a single barrier per tile could then complete two phases unobserved.  Block
 // j + 2 cannot be written before S(j + 2) is issued, which follows the consumption of block j.
-constexpr int BAR_P = BAR_S + 4;      // [tile][buf] P written to TMEM (128 arrivals)
-constexpr int BAR_PV = BAR_P + 4;     // [tile] PV product completed
-constexpr int BAR_DONE = BAR_PV + 2;  // every MMA completed (one-shot)
+constexpr int BAR_P = BAR_S + 2;      // [tile][buf] P written to TMEM (128 arrivals)
+constexpr int BAR_DONE = BAR_P + 4;   // every MMA completed (one-shot)
 constexpr int BAR_EPI = BAR_DONE + 1; // [tile] staging written (128 arrivals, one-shot)
 constexpr int N_BARS = BAR_EPI + 2;
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;  // tmem slot, abort flag
@@ -127,7 +128,8 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     auto bar = [&](int i) { return base + OFF_BAR + 8u * (uint32_t)i; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nrb = (a.nRB + 1) / 2;  // 256-row blocks
+    constexpr int ROWS = TILES * 128;           // query rows per CTA
+    const int nrb = (a.nRB + TILES - 1) / TILES;  // row blocks of ROWS rows
     const int rb = blockIdx.x % nrb;
     const int kvh = blockIdx.x / nrb;
     const int c = blockIdx.y;
@@ -182,7 +184,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         if (lane == 0) {
             tma_prefetch_desc(&maps.q);
             tma_prefetch_desc(&maps.kc);
-            const int node0 = (rb * 256) / a.G;
+            const int node0 = (rb * ROWS) / a.G;
             const int nodes_per_tile = 128 / a.G;
             mbar_expect_tx(bar(BAR_Q), TILES * Q_TILE_BYTES);
             for (int t = 0; t < TILES; ++t) {
@@ -243,8 +245,8 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                         const uint32_t qoff = t * Q_TILE_BYTES + (kk >> 2) * (Q_TILE_BYTES / 2) + (kk & 3) * 32;
                         mma_bf16_ss(d, q_desc + (qoff >> 4), kd + (off >> 4), idS, kk > 0);
                     }
-                    mma_commit(bar(BAR_S + t * 2 + (j & 1)));
                 }
+                mma_commit(bar(BAR_S + (j & 1)));
                 mma_commit(bar(BAR_KE + j % SK));
             }
             __syncwarp();
@@ -277,7 +279,6 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                     mma_bf16_ts(d, p, vd, idO, j > 0);
 #pragma unroll
                     for (int kk = 1; kk < BN / 16; ++kk) mma_bf16_ts(d, p + kk * 8, vd + ((kk * 2048) >> 4), idO, true);
-                    mma_commit(bar(BAR_PV + t));
                 }
                 __syncwarp();
             }
@@ -295,7 +296,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         const int quad = warp & 3;
         const int r = quad * 32 + lane;  // row within the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const int gr = rb * 256 + t * 128 + r;
+        const int gr = rb * ROWS + t * 128 + r;
         const bool row_ok = (t < TILES) && gr < a.R;
         const int node = row_ok ? gr / a.G : 0;
         const uint64_t anc = row_ok ? a.mask[(size_t)b * a.Kmax + node] : 0ull;
@@ -303,7 +304,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         float m_used = -INFINITY, l_sum = 0.f;  // running max (log2 units) and row sum
         bool ok = true;
         for (int j = 0; j < nb && t < TILES; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + t * 2 + (j & 1)), (j >> 1) & 1, kWaitNs) &&
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + (j & 1)), (j >> 1) & 1, kWaitNs) &&
                                              !aborted(abort_flag));
             if (!ok) break;
             tc_fence_after();
@@ -331,10 +332,13 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 m_used = mx;
             } else if (__any_sync(0xffffffffu, mx > m_used + RESCALE_LOG2)) {
                 // raise the running maximum of the rows that need it and rescale their O by
-                // 2^(m_used - m_new); the previous PV must have landed first (whole warp).
-                // S(j) was committed after PV(j - 2) was issued, so pv_done has completed phase
-                // j - 2 and cannot have completed phase j yet: its parity names phase j - 1.
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_PV + t), (j - 1) & 1, kWaitNs));
+                // 2^(m_used - m_new); the previous PV must have landed first (whole warp).  Its
+                // completion is the V-release barrier of block j - 1 (committed after both tiles'
+                // PV).  S(j) was committed after PV(j - 2), so that barrier's earlier phase (block
+                // j - 1 - SV) has completed, and PV(j - 1 + SV) cannot have completed before this
+                // softmax hands over block j: the parity names block j - 1 unambiguously.
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(bar(BAR_VE + (j - 1) % SV), ((j - 1) / SV) & 1, kWaitNs));
                 if (!ok) break;
                 tc_fence_after();
                 const float m_new = fmaxf(mx, m_used);
@@ -426,7 +430,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 if (direct) {
                     for (int k = tix; k < 128 * 16; k += 128) {
                         const int row = k >> 4, cc = k & 15;
-                        const int g = rb * 256 + t * 128 + row;
+                        const int g = rb * ROWS + t * 128 + row;
                         if (g >= a.R) continue;
                         const int nd = g / a.G, hh = kvh * a.G + g % a.G;
                         const uint4 v = *reinterpret_cast<const uint4*>(stile + row * 256 + ((cc ^ (row & 15)) << 4));
@@ -434,8 +438,8 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                                              (((size_t)b * a.Kmax + nd) * a.Hq + hh) * HD + cc * 8;
                         *reinterpret_cast<uint4*>(dst) = v;
                     }
-                } else if (rb * 2 + t < a.nRB) {  // an odd tile count leaves the last block's second tile empty
-                    const int tile = rb * 2 + t;  // 128-row tile index within (b, kvh)
+                } else if (rb * TILES + t < a.nRB) {  // an odd tile count leaves the last block's second tile empty
+                    const int tile = rb * TILES + t;  // 128-row tile index within (b, kvh)
                     const size_t pbase = ((((size_t)b * a.Hkv + kvh) * a.nRB + tile) * a.nchunk + c) * 128;
                     float* dst = a.part_o + pbase * HD;
                     for (int k = tix; k < 128 * 32; k += 128) {
@@ -532,7 +536,7 @@ int attn_tc_launch(const AttnArgs& a, cudaStream_t st) {
         if (!encode(&m.kt, a.Kt, 4, dims, strides, box)) return GRAFT_ERR_CUDA;
         if (!encode(&m.vt, a.Vt, 4, dims, strides, box)) return GRAFT_ERR_CUDA;
     }
-    const bool two = a.nRB > 1;
+    const bool two = a.tiles == 2;
     static bool attr_set[2][64] = {{false}};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -544,7 +548,7 @@ int attn_tc_launch(const AttnArgs& a, cudaStream_t st) {
         if (e != cudaSuccess) return GRAFT_ERR_CUDA;
         attr_set[two][dev] = true;
     }
-    const int nrb = (a.nRB + 1) / 2;
+    const int nrb = (a.nRB + a.tiles - 1) / a.tiles;
     dim3 grid(nrb * a.Hkv, a.nchunk, a.B);
     if (two)
         attn_tc_kernel<2><<<grid, NTHREADS, SMEM_BYTES, st>>>(m, a);
