@@ -43,6 +43,7 @@ __device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
 
 __global__ void __launch_bounds__(kArgThreads)
 argmax_part_kernel(const float* __restrict__ logits, int V, int S, int chunk, ArgPart* __restrict__ parts) {
+    griddep_enter();
     const int s = blockIdx.x;
     const size_t row = blockIdx.y;
     const float* r = logits + row * (size_t)V;
@@ -93,6 +94,7 @@ accept_kernel(int Kmax, int S, int64_t Lcap, const ArgPart* __restrict__ parts, 
               const int32_t* __restrict__ tree_parent, const int32_t* __restrict__ tree_depth, int32_t* L,
               int32_t* argmax, int32_t* acc_len, int32_t* path, int32_t* out_tok, int32_t* bonus, AcceptWs w,
               int32_t* status) {
+    griddep_enter();
     const int b = blockIdx.x, i = threadIdx.x;
     __shared__ int g_s[GRAFT_MAX_KMAX], tok_s[GRAFT_MAX_KMAX], par_s[GRAFT_MAX_KMAX];
     __shared__ int key_s[GRAFT_MAX_KMAX / 32];
@@ -158,6 +160,7 @@ __global__ void __launch_bounds__(256)
 compact_kernel(int Kmax, int64_t Lcap, int row_bytes, void* const* __restrict__ Kc_layers,
                void* const* __restrict__ Vc_layers, const void* const* __restrict__ Kt_layers,
                const void* const* __restrict__ Vt_layers, const int32_t* __restrict__ path, AcceptWs w) {
+    griddep_enter();
     const int l = blockIdx.x, b = blockIdx.y;
     const int n = w.ncopy[b];
     if (n == 0) return;
@@ -243,12 +246,12 @@ extern "C" int graft_accept_compact(int B, int Kmax, int V, int n_layers, const 
     WsCarver c(ws);
     AcceptWs w = carve_accept(c, B, Kmax, V);
     cudaStream_t st = (cudaStream_t)stream;
-    argmax_part_kernel<<<dim3(S, (unsigned)rows), kArgThreads, 0, st>>>(target_logits, V, S, kChunk, w.parts);
-    accept_kernel<<<B, GRAFT_MAX_KMAX, 0, st>>>(Kmax, S, Lcap, w.parts, tree_tok, tree_parent, tree_depth, L, argmax,
+    launch_pdl(argmax_part_kernel, dim3(S, (unsigned)rows), dim3(kArgThreads), 0, st, target_logits, V, S, kChunk, w.parts);
+    launch_pdl(accept_kernel, dim3(B), dim3(GRAFT_MAX_KMAX), 0, st, Kmax, S, Lcap, w.parts, tree_tok, tree_parent, tree_depth, L, argmax,
                                                  acc_len, path, out_tok, bonus, w, status);
     count_launches(n_layers > 0 ? 3 : 2);
     if (n_layers > 0)
-        compact_kernel<<<dim3(n_layers, B), 256, 0, st>>>(Kmax, Lcap, (int)row_bytes, Kc_layers, Vc_layers, Kt_layers,
+        launch_pdl(compact_kernel, dim3(n_layers, B), dim3(256), 0, st, Kmax, Lcap, (int)row_bytes, Kc_layers, Vc_layers, Kt_layers,
                                                           Vt_layers, path, w);
     return launch_status();
 }

@@ -73,6 +73,7 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __global__ void __launch_bounds__(NT)
 attn_partial_kernel(AttnArgs a) {
+    griddep_enter();
     extern __shared__ __align__(128) unsigned char smem[];
     const int nRB = a.nRB;
     const int rb = blockIdx.x % nRB;
@@ -305,6 +306,7 @@ attn_partial_kernel(AttnArgs a) {
 // lse = log2 sum_c 2^lse_c.  One warp per output row, four dims per lane.
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(AttnArgs a) {
+    griddep_enter();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const long long row = (long long)blockIdx.x * 8 + warp;
     const long long total = (long long)a.B * a.Hkv * a.nRB * 128;
@@ -351,7 +353,7 @@ attn_combine_kernel(AttnArgs a) {
 int attn_combine_launch(const AttnArgs& a, cudaStream_t st) {
     if (a.nchunk <= 1) return GRAFT_OK;
     const long long rows = (long long)a.B * a.Hkv * a.nRB * 128;
-    attn_combine_kernel<<<(unsigned)((rows + 7) / 8), 256, 0, st>>>(a);
+    launch_pdl(attn_combine_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, a);
     count_launches(1);
     return launch_status();
 }
@@ -370,7 +372,7 @@ int attn_mma_launch(const AttnArgs& a, cudaStream_t st) {
         attr_set[dev] = true;
     }
     dim3 grid(a.nRB * a.Hkv, a.nchunk, a.B);
-    attn_mma::attn_partial_kernel<<<grid, attn_mma::NT, attn_mma::SMEM, st>>>(a);
+    launch_pdl(attn_mma::attn_partial_kernel, dim3(grid), dim3(attn_mma::NT), attn_mma::SMEM, st, a);
     count_launches(1);
     const int rc = launch_status();
     if (rc != GRAFT_OK) return rc;

@@ -135,21 +135,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     const int c = blockIdx.y;
     const int b = blockIdx.z;
 
-    const int Lb = a.L[b];
-    if (Lb < 0 || Lb > a.Lcap) {
-        if (tid == 0 && c == 0 && rb == 0 && kvh == 0) flag_status(a.status, GRAFT_STATUS_LENGTH);
-        return;
-    }
-    const int nck = Lb > 0 ? (Lb + a.C - 1) / a.C : 1;
-    if (c >= nck) return;
-    const int k0 = c * a.C;
-    const int k1 = min(Lb, k0 + a.C);
-    const int nb_prefix = (k1 - k0 + BN - 1) / BN;
-    const bool has_tree = (c == nck - 1);
-    const int nb = nb_prefix + (has_tree ? 1 : 0);
-    const int ragged_block = ((k1 - k0) % BN) != 0 ? nb_prefix - 1 : -1;
-    const int ragged_valid = (k1 - k0) % BN;
-
+    // Prologue that touches no global memory: it overlaps the previous kernel's tail.
     if (tid == 0) {
         for (int i = 0; i < N_BARS; ++i) {
             uint32_t cnt = 1;
@@ -158,15 +144,40 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         }
         *abort_flag = 0;
         fence_mbar_init();
+    } else if (tid == 32 * 3) {
+        tma_prefetch_desc(&maps.vc);
+        tma_prefetch_desc(&maps.vt);
+    } else if (tid == 32 * 4) {
+        tma_prefetch_desc(&maps.q);
+        tma_prefetch_desc(&maps.kc);
+        tma_prefetch_desc(&maps.kt);
     }
     if (warp == 2) {
         tmem_alloc(base + OFF_MISC, 512);
         tmem_relinquish();
         tc_fence_before();
     }
+    griddep_wait();
+    griddep_launch_dependents();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+
+    const int Lb = a.L[b];
+    const bool bad_len = Lb < 0 || Lb > a.Lcap;
+    const int nck = (Lb > 0 && !bad_len) ? (Lb + a.C - 1) / a.C : 1;
+    if (bad_len || c >= nck) {  // uniform over the CTA
+        if (bad_len && tid == 0 && c == 0 && rb == 0 && kvh == 0) flag_status(a.status, GRAFT_STATUS_LENGTH);
+        if (warp == 2) tmem_dealloc(tmem, 512);
+        return;
+    }
+    const int k0 = c * a.C;
+    const int k1 = min(Lb, k0 + a.C);
+    const int nb_prefix = (k1 - k0 + BN - 1) / BN;
+    const bool has_tree = (c == nck - 1);
+    const int nb = nb_prefix + (has_tree ? 1 : 0);
+    const int ragged_block = ((k1 - k0) % BN) != 0 ? nb_prefix - 1 : -1;
+    const int ragged_valid = (k1 - k0) % BN;
 
     int k_issued = 0, v_issued = 0;  // blocks the producer lanes have armed
     auto load_block = [&](int j, const CUtensorMap* prefix_map, const CUtensorMap* tree_map, uint32_t dst,
@@ -182,8 +193,6 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer: Q, then K blocks
         if (lane == 0) {
-            tma_prefetch_desc(&maps.q);
-            tma_prefetch_desc(&maps.kc);
             const int node0 = (rb * ROWS) / a.G;
             const int nodes_per_tile = 128 / a.G;
             mbar_expect_tx(bar(BAR_Q), TILES * Q_TILE_BYTES);
@@ -207,7 +216,6 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     } else if (warp == 3) {
         // ------------------------------------------------------------ TMA producer: V blocks
         if (lane == 0) {
-            tma_prefetch_desc(&maps.vc);
             for (int j = 0; j < nb; ++j) {
                 // a V stage frees once both tiles' PV products have run
                 if (j >= SV && !mbar_wait(bar(BAR_VE + j % SV), ((j / SV) - 1) & 1, kWaitNs)) {
@@ -551,9 +559,9 @@ int attn_tc_launch(const AttnArgs& a, cudaStream_t st) {
     const int nrb = (a.nRB + a.tiles - 1) / a.tiles;
     dim3 grid(nrb * a.Hkv, a.nchunk, a.B);
     if (two)
-        attn_tc_kernel<2><<<grid, NTHREADS, SMEM_BYTES, st>>>(m, a);
+        launch_pdl(attn_tc_kernel<2>, dim3(grid), dim3(NTHREADS), SMEM_BYTES, st, m, a);
     else
-        attn_tc_kernel<1><<<grid, NTHREADS, SMEM_BYTES, st>>>(m, a);
+        launch_pdl(attn_tc_kernel<1>, dim3(grid), dim3(NTHREADS), SMEM_BYTES, st, m, a);
     count_launches(1);
     const int rc = launch_status();
     if (rc != GRAFT_OK) return rc;

@@ -106,6 +106,7 @@ template <int KT>
 __global__ void __launch_bounds__(kRowThreads)
 draft_rows_kernel(const float* __restrict__ logits, int D, int k, int V, int d_lo, int S,
                   int chunk, const int32_t* __restrict__ state, RowPart* __restrict__ parts) {
+    griddep_enter();
     const int s = blockIdx.x;
     const int r = blockIdx.y;
     const int b = blockIdx.z;
@@ -202,6 +203,7 @@ struct BuildWs {
 
 __global__ void __launch_bounds__(kSelThreads)
 draft_select_kernel(SelectParams p, int d_lo, int d_hi, BuildWs w) {
+    griddep_enter();
     const int b = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     constexpr int NW = kSelThreads / 32;
@@ -321,6 +323,7 @@ __global__ void __launch_bounds__(kMergeThreads)
 draft_merge_kernel(MergeParams p, const int32_t* __restrict__ root_tok, const int32_t* __restrict__ L,
                    BuildWs w, int32_t* tree_tok, int32_t* tree_parent, int32_t* tree_depth,
                    int32_t* tree_pos, uint64_t* tree_mask, int32_t* stage_out, int32_t* status) {
+    griddep_enter();
     const int b = blockIdx.x, tid = threadIdx.x;
     const int k = p.k, KK = k * k, Kmax = p.Kmax;
     extern __shared__ float sm_pool[];  // [P] scores
@@ -416,6 +419,7 @@ struct TmplParams {
 __global__ void __launch_bounds__(GRAFT_MAX_KMAX)
 retrieve_kernel(int V, int W, const int32_t* __restrict__ root_tok, const int32_t* __restrict__ M_succ,
                 TmplParams tp, int32_t* __restrict__ out, int out_stride, int32_t* status) {
+    griddep_enter();
     const int b = blockIdx.x, j = threadIdx.x;
     __shared__ int tok[GRAFT_MAX_KMAX];
     const int root = root_tok[b];
@@ -476,7 +480,7 @@ template <int KT>
 void launch_rows(const float* logits, const GraftConfig* cfg, int B, int d_lo, int d_hi, int S, int chunk,
                  const int32_t* state, RowPart* parts, cudaStream_t st) {
     dim3 grid(S, (d_hi - d_lo + 1) * cfg->k, B);
-    draft_rows_kernel<KT><<<grid, kRowThreads, 0, st>>>(logits, cfg->D, cfg->k, cfg->V, d_lo, S, chunk, state, parts);
+    launch_pdl(draft_rows_kernel<KT>, dim3(grid), dim3(kRowThreads), 0, st, logits, cfg->D, cfg->k, cfg->V, d_lo, S, chunk, state, parts);
     count_launches(1);
 }
 
@@ -503,7 +507,7 @@ extern "C" int graft_retrieve(const GraftConfig* cfg, int B, const int32_t* root
     if (B == 0 || cfg->n_tmpl == 0) return GRAFT_OK;
     if (root_tok == nullptr || M_succ == nullptr || ret_tok == nullptr) return GRAFT_ERR_INVALID_ARG;
     const TmplParams tp = make_tmpl(cfg);
-    retrieve_kernel<<<B, GRAFT_MAX_KMAX, 0, (cudaStream_t)stream>>>(cfg->V, cfg->W, root_tok, M_succ, tp,
+    launch_pdl(retrieve_kernel, dim3(B), dim3(GRAFT_MAX_KMAX), 0, (cudaStream_t)stream, cfg->V, cfg->W, root_tok, M_succ, tp,
                                                                      ret_tok, cfg->n_tmpl, status);
     count_launches(1);
     return launch_status();
@@ -537,7 +541,7 @@ extern "C" int graft_build_tree(const GraftConfig* cfg, int B, const float* draf
 
     const TmplParams tp = make_tmpl(cfg);
     if (cfg->n_tmpl > 0) {
-        retrieve_kernel<<<B, GRAFT_MAX_KMAX, 0, st>>>(cfg->V, cfg->W, root_tok, M_succ, tp, w.ret,
+        launch_pdl(retrieve_kernel, dim3(B), dim3(GRAFT_MAX_KMAX), 0, st, cfg->V, cfg->W, root_tok, M_succ, tp, w.ret,
                                                        GRAFT_MAX_KMAX, status);
         count_launches(1);
     }
@@ -559,7 +563,7 @@ extern "C" int graft_build_tree(const GraftConfig* cfg, int B, const float* draf
         if (cfg->k <= 4) launch_rows<4>(draft_logits, cfg, B, d_lo, d_hi, S, chunk, gate, w.parts, st);
         else if (cfg->k <= 8) launch_rows<8>(draft_logits, cfg, B, d_lo, d_hi, S, chunk, gate, w.parts, st);
         else launch_rows<16>(draft_logits, cfg, B, d_lo, d_hi, S, chunk, gate, w.parts, st);
-        draft_select_kernel<<<B, kSelThreads, 0, st>>>(sp, d_lo, d_hi, w);
+        launch_pdl(draft_select_kernel, dim3(B), dim3(kSelThreads), 0, st, sp, d_lo, d_hi, w);
         count_launches(1);
         d_lo = d_hi + 1;
     }
@@ -578,7 +582,7 @@ extern "C" int graft_build_tree(const GraftConfig* cfg, int B, const float* draf
         if (cudaFuncSetAttribute(draft_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
             return GRAFT_ERR_CUDA;
     }
-    draft_merge_kernel<<<B, kMergeThreads, smem, st>>>(mp, root_tok, L, w, tree_tok, tree_parent, tree_depth,
+    launch_pdl(draft_merge_kernel, dim3(B), dim3(kMergeThreads), smem, st, mp, root_tok, L, w, tree_tok, tree_parent, tree_depth,
                                                       tree_pos, tree_mask, stage, status);
     count_launches(1);
     return launch_status();

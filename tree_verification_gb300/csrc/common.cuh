@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "graft.h"
 
 namespace graft {
@@ -46,6 +48,40 @@ inline int launch_status() {
 
 // Counts kernel launches enqueued by the library (graft_launch_count).
 void count_launches(int n);
+
+// Programmatic dependent launch.  Every library kernel is launched with
+// programmatic stream serialisation: it may become resident while its
+// predecessor in the stream is still running, does only work that touches
+// no global memory (barrier set-up, tensor-memory allocation) before
+// griddep_wait(), which returns once the predecessor has completed and its
+// writes are visible, and then lets its own successor launch early.  Waits
+// chain, so a kernel also sees everything earlier kernels wrote.  After an
+// ordinary launch both instructions are no-ops.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Both at once, for kernels with no prologue worth overlapping.
+__device__ __forceinline__ void griddep_enter() {
+    griddep_wait();
+    griddep_launch_dependents();
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Number of SMs of the current device (cached per device ordinal).
 int device_sm_count();

@@ -54,6 +54,7 @@ __device__ __forceinline__ uint32_t hash64(unsigned long long x) {
 }
 
 __global__ void clear_kernel(UpdWs w) {
+    griddep_enter();
     for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < w.cap; i += gridDim.x * blockDim.x) {
         w.pair_key[i] = kEmptyPair;
         w.pair_mult[i] = 0;
@@ -67,6 +68,7 @@ __global__ void clear_kernel(UpdWs w) {
 __global__ void pairs_kernel(int32_t* __restrict__ succ, int32_t* __restrict__ cnt, int V, int W,
                              const int32_t* __restrict__ src, const int32_t* __restrict__ dst, int64_t n, UpdWs w,
                              int32_t* status) {
+    griddep_enter();
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const int s = src[i], t = dst[i];
@@ -121,6 +123,7 @@ __device__ __forceinline__ unsigned long long pack_slot(int c, int tok) {
 }
 
 __global__ void rerank_kernel(int32_t* __restrict__ succ, int32_t* __restrict__ cnt, int W, UpdWs w) {
+    griddep_enter();
     const int warps = blockDim.x >> 5;
     const int wid = blockIdx.x * warps + (threadIdx.x >> 5);
     const int lane = threadIdx.x & 31;
@@ -209,9 +212,9 @@ extern "C" int graft_update_M(int32_t* M_succ, int32_t* M_cnt, int V, int W, con
     UpdWs w = carve_update(c, n);
     cudaStream_t st = (cudaStream_t)stream;
     const int cb = (int)((w.cap + 255) / 256);
-    clear_kernel<<<cb < 1024 ? cb : 1024, 256, 0, st>>>(w);
-    pairs_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(M_succ, M_cnt, V, W, src, dst, n, w, status);
-    rerank_kernel<<<(unsigned)((n + 7) / 8), 256, 0, st>>>(M_succ, M_cnt, W, w);
+    launch_pdl(clear_kernel, dim3(cb < 1024 ? cb : 1024), dim3(256), 0, st, w);
+    launch_pdl(pairs_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, M_succ, M_cnt, V, W, src, dst, n, w, status);
+    launch_pdl(rerank_kernel, dim3((unsigned)((n + 7) / 8)), dim3(256), 0, st, M_succ, M_cnt, W, w);
     count_launches(3);
     return launch_status();
 }
@@ -274,9 +277,9 @@ extern "C" int graft_update_M_noalloc(int32_t* M_succ, int32_t* M_cnt, int V, in
     // clear_kernel resets every table the other two kernels read, so whatever
     // the previous call left in the shared array does not leak into this one
     const int cb = (int)((w.cap + 255) / 256);
-    clear_kernel<<<cb < 1024 ? cb : 1024, 256, 0, st>>>(w);
-    pairs_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(M_succ, M_cnt, V, W, src, dst, n, w, status);
-    rerank_kernel<<<(unsigned)((n + 7) / 8), 256, 0, st>>>(M_succ, M_cnt, W, w);
+    launch_pdl(clear_kernel, dim3(cb < 1024 ? cb : 1024), dim3(256), 0, st, w);
+    launch_pdl(pairs_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, M_succ, M_cnt, V, W, src, dst, n, w, status);
+    launch_pdl(rerank_kernel, dim3((unsigned)((n + 7) / 8)), dim3(256), 0, st, M_succ, M_cnt, W, w);
     count_launches(3);
     return launch_status();
 }
