@@ -6,11 +6,13 @@
 
 namespace graft {
 
+// Keys per block of the tcgen05 path; key chunks are multiples of it.
+constexpr int ATTN_TC_BLOCK_KEYS = 128;
+
 struct AttnArgs {
     int B, Hq, Hkv, G, Kmax, R;  // R = Kmax * G query rows per (request, KV head)
     int nRB;                      // 128-row blocks per (request, KV head)
-    int tiles;                    // 128-row tiles per CTA on the tcgen05 path (1 or 2)
-    int C;                        // prefix keys per chunk (multiple of 64)
+    int C;                        // prefix keys per chunk (multiple of 128)
     int nchunk;                   // chunks per (request, KV head) allowed by Lcap
     int Lcap;
     float scale;
@@ -29,7 +31,7 @@ struct AttnArgs {
 
 // Warp-level mma.sync path: any group size; 128-row CTAs.
 int attn_mma_launch(const AttnArgs& a, cudaStream_t st);
-// tcgen05 path: group sizes dividing 128; 256-row CTAs.
+// tcgen05 path: group sizes dividing 128; 128-row CTAs.
 bool attn_tc_supported(int G);
 int attn_tc_launch(const AttnArgs& a, cudaStream_t st);
 // Merges split-key partials (no-op when every request fits one chunk).

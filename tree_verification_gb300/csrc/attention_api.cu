@@ -13,18 +13,16 @@ namespace graft {
 namespace {
 
 struct AttnPlan {
-    int G, R, nRB, C, nchunk, tiles;
+    int G, R, nRB, C, nchunk;
     bool tc;
 };
 
-// Key-chunk policy: split the keys of each (request, KV head, row block)
+// Key-chunk policy: split the keys of each (request, KV head, 128-row tile)
 // into as many chunks as keep one CTA per SM busy (no partial second wave),
 // but never below kMinChunk keys so partial outputs stay a modest share of
-// the KV bytes.  On the tcgen05 path a CTA takes two 128-row tiles unless
-// that would leave each CTA fewer than 1024 keys, then one.
-// GRAFT_ATTN_MIN_CHUNK (multiple of 64) and GRAFT_ATTN_TILES (1 or 2)
-// override the policy for tuning; the workspace size and the launch read the
-// same values.
+// the KV bytes.  Chunks are whole 128-key blocks.  GRAFT_ATTN_MIN_CHUNK
+// overrides the minimum for tuning; the workspace size and the launch read
+// the same value.
 AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
     AttnPlan p;
     p.G = Hq / Hkv;
@@ -33,31 +31,17 @@ AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
     p.tc = attn_tc_supported(p.G);
     int sms = device_sm_count();
     if (sms <= 0) sms = 148;
-    p.tiles = 1;
-    if (p.tc && p.nRB > 1) {
-        // two tiles halve the K/V traffic per row; one tile doubles the CTAs, which pays
-        // when two-tile chunks would be short and per-CTA fixed costs would dominate
-        const long long units2 = (long long)B * Hkv * ((p.nRB + 1) / 2);
-        long long per_sm = sms / units2;
-        if (per_sm < 1) per_sm = 1;
-        const long long keys_per_cta = (Lcap + per_sm - 1) / per_sm;
-        p.tiles = keys_per_cta >= 1024 ? 2 : 1;
-        if (const char* env = getenv("GRAFT_ATTN_TILES")) {
-            const int v = atoi(env);
-            if (v == 1 || v == 2) p.tiles = v;
-        }
-    }
-    const long long rows_per_cta = p.tc ? 128LL * p.tiles : 128;
-    const long long units = (long long)B * Hkv * ((p.R + rows_per_cta - 1) / rows_per_cta);
+    const long long units = (long long)B * Hkv * p.nRB;
+    constexpr long long blk = ATTN_TC_BLOCK_KEYS;
     long long min_chunk = 256;
     if (const char* env = getenv("GRAFT_ATTN_MIN_CHUNK")) {
         const long long v = atoll(env);
-        if (v >= 64) min_chunk = (v + 63) / 64 * 64;
+        if (v >= blk) min_chunk = (v + blk - 1) / blk * blk;
     }
     long long target = sms / units;
     if (target < 1) target = 1;
     long long C = (Lcap + target - 1) / target;
-    C = (C + 63) / 64 * 64;
+    C = (C + blk - 1) / blk * blk;
     if (C < min_chunk) C = min_chunk;
     if (C > (1LL << 30)) C = 1LL << 30;
     p.C = (int)C;
@@ -129,7 +113,6 @@ extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Km
     a.Kmax = Kmax;
     a.R = p.R;
     a.nRB = p.nRB;
-    a.tiles = p.tiles;
     a.C = p.C;
     a.nchunk = p.nchunk;
     a.Lcap = (int)Lcap;
