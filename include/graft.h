@@ -268,6 +268,14 @@ int graft_version(void);
  */
 uint64_t graft_launch_count(void);
 
+/*
+ * graft_last_cuda_error — name of the most recent CUDA runtime error that an
+ * entry point of this library observed on the calling host thread (the cause
+ * behind a GRAFT_ERR_CUDA return), or "cudaSuccess" if there was none.  The
+ * string is static; the caller does not free it.
+ */
+const char* graft_last_cuda_error(void);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,6 +18,7 @@ import torch
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libgraft.so")
 
 GRAFT_OK = 0
+ERR_CUDA = -4
 STATUS_TOKEN_RANGE = 1
 STATUS_CACHE_OVERFLOW = 2
 STATUS_LENGTH = 4
@@ -79,6 +80,7 @@ _SIGNATURES = {
     "graft_status_string": [_I],
     "graft_version": [],
     "graft_launch_count": [],
+    "graft_last_cuda_error": [],
 }
 
 
@@ -96,7 +98,7 @@ def lib():
         for name, args in _SIGNATURES.items():
             fn = getattr(L, name)
             fn.argtypes = args
-            fn.restype = {"graft_status_string": ctypes.c_char_p,
+            fn.restype = {"graft_status_string": ctypes.c_char_p, "graft_last_cuda_error": ctypes.c_char_p,
                           "graft_launch_count": ctypes.c_uint64}.get(name, ctypes.c_int)
         _lib = L
     return _lib
@@ -104,7 +106,10 @@ def lib():
 
 def _check(rc: int, what: str) -> None:
     if rc != GRAFT_OK:
-        raise GraftError(f"{what}: {lib().graft_status_string(rc).decode()} ({rc})")
+        msg = f"{what}: {lib().graft_status_string(rc).decode()} ({rc})"
+        if rc == ERR_CUDA:
+            msg += f" [{lib().graft_last_cuda_error().decode()}]"
+        raise GraftError(msg)
 
 
 def _ptr(t: Optional[torch.Tensor]):

@@ -19,6 +19,10 @@ static std::atomic<unsigned long long> g_launches{0};
 
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
 
+static thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+void note_cuda_error(cudaError_t e) { g_last_cuda_error = e; }
+
 int device_sm_count() {
     static int cached[64] = {0};
     int dev = 0;
@@ -201,3 +205,5 @@ extern "C" const char* graft_status_string(int code) {
 extern "C" int graft_version(void) { return 100; }
 
 extern "C" uint64_t graft_launch_count(void) { return graft::g_launches.load(std::memory_order_relaxed); }
+
+extern "C" const char* graft_last_cuda_error(void) { return cudaGetErrorName(graft::g_last_cuda_error); }

@@ -12,6 +12,7 @@ constexpr int ATTN_TC_BLOCK_KEYS = 128;
 struct AttnArgs {
     int B, Hq, Hkv, G, Kmax, R;  // R = Kmax * G query rows per (request, KV head)
     int nRB;                      // 128-row blocks per (request, KV head)
+    int tiles;                    // tcgen05 path: 128-row tiles per CTA (1 or 2)
     int C;                        // prefix keys per chunk (multiple of 128)
     int nchunk;                   // chunks per (request, KV head) allowed by Lcap
     int Lcap;
@@ -31,9 +32,11 @@ struct AttnArgs {
 
 // Warp-level mma.sync path: any group size; 128-row CTAs.
 int attn_mma_launch(const AttnArgs& a, cudaStream_t st);
-// tcgen05 path: group sizes dividing 128; 128-row CTAs.
+// tcgen05 path: group sizes dividing 128; CTAs of two 128-row tiles
+// (attn_tc_launch) or of one (attn_tc1_launch), as a.tiles says.
 bool attn_tc_supported(int G);
 int attn_tc_launch(const AttnArgs& a, cudaStream_t st);
+int attn_tc1_launch(const AttnArgs& a, cudaStream_t st);
 // Merges split-key partials (no-op when every request fits one chunk).
 int attn_combine_launch(const AttnArgs& a, cudaStream_t st);
 

@@ -13,16 +13,32 @@ namespace graft {
 namespace {
 
 struct AttnPlan {
-    int G, R, nRB, C, nchunk;
+    int G, R, nRB, C, nchunk, tiles;
     bool tc;
 };
 
-// Key-chunk policy: split the keys of each (request, KV head, 128-row tile)
+// Key-chunk policy: split the keys of each (request, KV head, row block)
 // into as many chunks as keep one CTA per SM busy (no partial second wave),
 // but never below kMinChunk keys so partial outputs stay a modest share of
-// the KV bytes.  Chunks are whole 128-key blocks.  GRAFT_ATTN_MIN_CHUNK
-// overrides the minimum for tuning; the workspace size and the launch read
-// the same value.
+// the KV bytes.  Chunks are whole 128-key blocks.
+//
+// Row blocks: on the tcgen05 path a CTA takes two 128-row tiles that share
+// every K/V block, unless that plan would leave each CTA fewer than 1024
+// keys; then one tile per CTA (twice the CTAs, a shorter prologue) does
+// better.  A single row block always goes to the two-tile kernel.
+// GRAFT_ATTN_MIN_CHUNK and GRAFT_ATTN_TILES (1 or 2) override the policy for
+// tuning and tests; the workspace size and the launch read the same values.
+long long chunk_keys(long long Lcap, long long units, int sms, long long min_chunk) {
+    constexpr long long blk = ATTN_TC_BLOCK_KEYS;
+    long long target = sms / units;
+    if (target < 1) target = 1;
+    long long C = (Lcap + target - 1) / target;
+    C = (C + blk - 1) / blk * blk;
+    if (C < min_chunk) C = min_chunk;
+    if (C > (1LL << 30)) C = 1LL << 30;
+    return C;
+}
+
 AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
     AttnPlan p;
     p.G = Hq / Hkv;
@@ -31,21 +47,25 @@ AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
     p.tc = attn_tc_supported(p.G);
     int sms = device_sm_count();
     if (sms <= 0) sms = 148;
-    const long long units = (long long)B * Hkv * p.nRB;
     constexpr long long blk = ATTN_TC_BLOCK_KEYS;
     long long min_chunk = 256;
     if (const char* env = getenv("GRAFT_ATTN_MIN_CHUNK")) {
         const long long v = atoll(env);
         if (v >= blk) min_chunk = (v + blk - 1) / blk * blk;
     }
-    long long target = sms / units;
-    if (target < 1) target = 1;
-    long long C = (Lcap + target - 1) / target;
-    C = (C + blk - 1) / blk * blk;
-    if (C < min_chunk) C = min_chunk;
-    if (C > (1LL << 30)) C = 1LL << 30;
-    p.C = (int)C;
-    p.nchunk = Lcap > 0 ? (int)((Lcap + C - 1) / C) : 1;
+    p.tiles = 1;
+    if (p.tc) {
+        const long long units2 = (long long)B * Hkv * ((p.nRB + 1) / 2);
+        // with a single row block both kernels run the same grid; the two-tile kernel is quicker
+        p.tiles = (p.nRB == 1 || chunk_keys(Lcap, units2, sms, min_chunk) >= 1024) ? 2 : 1;
+        if (const char* env = getenv("GRAFT_ATTN_TILES")) {
+            const int v = atoi(env);
+            if (v == 1 || v == 2) p.tiles = v;
+        }
+    }
+    const long long units = (long long)B * Hkv * ((p.nRB + p.tiles - 1) / p.tiles);
+    p.C = (int)chunk_keys(Lcap, units, sms, min_chunk);
+    p.nchunk = Lcap > 0 ? (int)((Lcap + p.C - 1) / p.C) : 1;
     if (p.nchunk < 1) p.nchunk = 1;
     return p;
 }
@@ -113,6 +133,7 @@ extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Km
     a.Kmax = Kmax;
     a.R = p.R;
     a.nRB = p.nRB;
+    a.tiles = p.tiles;
     a.C = p.C;
     a.nchunk = p.nchunk;
     a.Lcap = (int)Lcap;
@@ -128,6 +149,6 @@ extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Km
     a.status = status;
     attn_ws(p, B, Hkv, &a, ws);
     if ((long long)p.nRB * Hkv > 65535LL || p.nchunk > 65535) return GRAFT_ERR_UNSUPPORTED_SHAPE;
-    if (p.tc) return attn_tc_launch(a, (cudaStream_t)stream);
+    if (p.tc) return p.tiles == 2 ? attn_tc_launch(a, (cudaStream_t)stream) : attn_tc1_launch(a, (cudaStream_t)stream);
     return attn_mma_launch(a, (cudaStream_t)stream);
 }

@@ -366,8 +366,8 @@ int attn_mma_launch(const AttnArgs& a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(attn_mma::attn_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 attn_mma::SMEM) != cudaSuccess)
+        if (!cuda_ok(cudaFuncSetAttribute(attn_mma::attn_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 attn_mma::SMEM)))
             return GRAFT_ERR_CUDA;
         attr_set[dev] = true;
     }

@@ -6,28 +6,30 @@
 // query head h) attends to its request's L prefix keys and to the tree keys
 // in node i's ancestor-or-self mask, with KV head h / group.
 //
-// One CTA computes one 128-row tile of query rows (all query heads of one KV
-// head for 128 / group tree nodes) against one key chunk, in 128-key blocks.
+// One CTA computes two 128-row tiles of query rows (all query heads of one
+// KV head for 256 / group tree nodes) against one key chunk, in 128-key
+// blocks: every K/V byte brought into shared memory feeds 256 rows.
 //
-// Warp roles (8 warps):
-//   warp 0      TMA producer: the Q tile once, then K blocks into a 3-stage
-//               ring (128-byte swizzled boxes of 128 keys x 64 dims); a K
-//               stage is released as soon as its S product has run
-//   warp 3      TMA producer: V blocks into their own 3-stage ring, a stage
-//               released once its PV product has run
-//   warp 1      MMA issuer (one lane): S = Q K^T with Q read from TMEM, then
-//               O += P V with P read from TMEM; shared-memory descriptors
-//               are built once and offset per MMA
-//   warp 2      owns the TMEM allocation (512 columns)
-//   warps 4-7   copy Q into TMEM, then softmax + epilogue (TMEM lanes
-//               0-127, one query row per thread)
-// TMEM columns: S/P double buffer [0,128) and [128,256), O [256,384), Q as
-// packed bf16 pairs [384,448).  Keeping Q in TMEM leaves the K block as the
-// only shared-memory operand of the S product, so that product is bound by
-// the tensor pipe rather than by shared-memory bandwidth.  Softmax
-// overwrites the first 64 columns of its S buffer with P as packed bf16
+// Warp roles (10 warps):
+//   warp 0      TMA producer (one lane): both Q tiles, then K blocks into a
+//               2-stage ring and V blocks into a 3-stage ring (128-byte
+//               swizzled boxes of 128 keys x 64 dims); a K stage is released
+//               once both tiles' S products have run, a V stage once both
+//               tiles' PV products have run
+//   warp 1      owns the TMEM allocation (512 columns); MMA issuer (one
+//               lane): S_t = Q_t K^T, O_t += P_t V.  The two tiles
+//               ping-pong: as soon as tile t's P arrives its PV and its next
+//               S are issued, so the tensor pipe works on one tile while the
+//               other tile's softmax runs
+//   warps 2-5   softmax + epilogue of tile 0 (one row per thread; warp w
+//               reaches TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31)
+//   warps 6-9   softmax + epilogue of tile 1
+// TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
+// Softmax overwrites the first 64 columns of S_t with P_t as packed bf16
 // pairs; the PV MMA takes that as its A operand straight from TMEM, so P
-// never touches shared memory.
+// never touches shared memory.  S_t(j + 1) is issued after PV_t(j) on the
+// same in-order tensor pipe, so it cannot overwrite P_t(j) early, and its
+// completion also certifies that O_t holds every block before j + 1.
 //
 // Softmax keeps a per-row running maximum that is only raised (and O
 // rescaled) when a block's maximum exceeds it by more than 2^8, so the
@@ -38,7 +40,7 @@
 // probability 0, and the V rows of a ragged tail are zeroed in shared memory
 // so stale cache rows cannot inject NaN.
 //
-// The epilogue stages the tile's rows through the freed K/V ring memory and
+// The epilogue stages each tile's rows through the freed K/V ring memory and
 // writes them out along contiguous rows.
 //
 // Every mbarrier wait is bounded; on timeout the CTA raises
@@ -60,42 +62,41 @@ using namespace tc;
 
 constexpr int HD = GRAFT_HEAD_DIM;
 constexpr int BN = ATTN_TC_BLOCK_KEYS;  // keys per block
-constexpr int SK = 3;                   // K ring depth
-constexpr int SV = 3;                   // V ring depth
-constexpr int NTHREADS = 256;
-constexpr uint32_t BOX_BYTES = BN * 64 * 2;             // one box: BN keys (or 128 rows) x 64 dims bf16
+#ifndef ATTN_K_STAGES
+#define ATTN_K_STAGES 2
+#define ATTN_V_STAGES 3
+#endif
+constexpr int SK = ATTN_K_STAGES;       // K ring depth
+constexpr int SV = ATTN_V_STAGES;       // V ring depth
+constexpr int NTHREADS = 320;
+constexpr uint32_t BOX_BYTES = BN * 64 * 2;             // one box: 128 keys (or rows) x 64 dims bf16
+constexpr uint32_t BLK_BYTES = 2 * BOX_BYTES;           // one K or V block (128 keys x 128 dims)
 constexpr uint32_t Q_TILE_BYTES = 2 * 128 * 64 * 2;     // 128 rows x 128 dims
-constexpr uint32_t BLK_BYTES = 2 * BOX_BYTES;           // one K or V block (BN keys x 128 dims)
 // shared memory map (offsets from a 1024-byte aligned base)
 constexpr uint32_t OFF_Q = 0;
-constexpr uint32_t OFF_K = OFF_Q + Q_TILE_BYTES;
+constexpr uint32_t OFF_K = OFF_Q + 2 * Q_TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + SK * BLK_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + SV * BLK_BYTES;
 constexpr uint32_t OFF_STAGE = OFF_K;  // epilogue staging reuses the rings once every MMA has run
 // barriers
-constexpr int BAR_Q = 0;              // Q tile landed in shared memory
-constexpr int BAR_QT = 1;             // Q copied into TMEM (128 arrivals)
-constexpr int BAR_KF = 2;             // [SK] K block landed
-constexpr int BAR_KE = BAR_KF + SK;   // [SK] K block consumed by its S product
+constexpr int BAR_Q = 0;              // Q tiles landed
+constexpr int BAR_KF = 1;             // [SK] K block landed
+constexpr int BAR_KE = BAR_KF + SK;   // [SK] K block consumed by both S products
 constexpr int BAR_VF = BAR_KE + SK;   // [SV] V block landed
-constexpr int BAR_VE = BAR_VF + SV;   // [SV] V block consumed by its PV product
-constexpr int BAR_S = BAR_VE + SV;    // [buf] S ready in TMEM
-// p_full is per S/P buffer: softmax may finish block j + 1 before the MMA thread has consumed
-// block j, and a single barrier could then complete two phases unobserved.  Block j + 2 cannot
-// be written before S(j + 2) is issued, which follows the consumption of block j.
-constexpr int BAR_P = BAR_S + 2;      // [buf] P written to TMEM (128 arrivals)
+constexpr int BAR_VE = BAR_VF + SV;   // [SV] V block consumed by both PV products
+constexpr int BAR_S = BAR_VE + SV;    // [tile] S_t ready in TMEM
+constexpr int BAR_P = BAR_S + 2;      // [tile] P_t written to TMEM (128 arrivals)
 constexpr int BAR_DONE = BAR_P + 2;   // every MMA completed (one-shot)
-constexpr int BAR_EPI = BAR_DONE + 1; // staging written (128 arrivals, one-shot)
-constexpr int N_BARS = BAR_EPI + 1;
+constexpr int BAR_EPI = BAR_DONE + 1; // [tile] staging written (128 arrivals, one-shot)
+constexpr int BAR_TURN = BAR_EPI + 2; // [tile] the other tile's exponentials of a block are done (128)
+constexpr int N_BARS = BAR_TURN + 2;
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;  // tmem slot, abort flag
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(128 * 128 * 4 <= SK * BLK_BYTES + SV * BLK_BYTES, "staging fits in the rings");
-static_assert(BN == 128, "one S/P buffer is 128 columns, P its first 64");
+static_assert(2 * 128 * 128 * 4 <= (SK + SV) * BLK_BYTES, "staging of both tiles fits in the rings");
 
-constexpr uint32_t TM_S = 0;    // + buf * 128
-constexpr uint32_t TM_O = 256;
-constexpr uint32_t TM_Q = 384;
+constexpr uint32_t TM_S = 0;    // + tile * 128
+constexpr uint32_t TM_O = 256;  // + tile * 128
 constexpr float RESCALE_LOG2 = 8.f;
 constexpr uint64_t kWaitNs = 500000000ull;   // bound on any single wait (the kernel runs for microseconds)
 constexpr uint64_t kDrainNs = 100000000ull;  // bound on draining in-flight loads after an abort
@@ -128,29 +129,34 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     auto bar = [&](int i) { return base + OFF_BAR + 8u * (uint32_t)i; };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int rb = blockIdx.x % a.nRB;  // 128-row tile within (request, KV head)
-    const int kvh = blockIdx.x / a.nRB;
+    const int nrb2 = (a.nRB + 1) / 2;           // CTAs (pairs of 128-row tiles) per (request, KV head)
+    const int rb = blockIdx.x % nrb2;
+    const int kvh = blockIdx.x / nrb2;
     const int c = blockIdx.y;
     const int b = blockIdx.z;
+    const int ntile = (2 * rb + 1 < a.nRB) ? 2 : 1;  // the last pair of an odd tile count has one
 
     // Prologue that touches no global memory: it overlaps the previous kernel's tail.
     if (tid == 0) {
         for (int i = 0; i < N_BARS; ++i) {
             uint32_t cnt = 1;
-            if (i == BAR_QT || i == BAR_P || i == BAR_P + 1 || i == BAR_EPI) cnt = 128;
+            if (i == BAR_P || i == BAR_P + 1 || i == BAR_EPI || i == BAR_EPI + 1 || i == BAR_TURN ||
+                i == BAR_TURN + 1)
+                cnt = 128;
             mbar_init(bar(i), cnt);
         }
         *abort_flag = 0;
         fence_mbar_init();
-    } else if (tid == 32 * 3) {
+    } else if (tid == 32) {
         tma_prefetch_desc(&maps.vc);
         tma_prefetch_desc(&maps.vt);
-    } else if (tid == 32 * 4) {
+    } else if (tid == 64) {
         tma_prefetch_desc(&maps.q);
         tma_prefetch_desc(&maps.kc);
         tma_prefetch_desc(&maps.kt);
     }
-    if (warp == 2) {
+    if (warp == 1) {
+        __syncwarp();
         tmem_alloc(base + OFF_MISC, 512);
         tmem_relinquish();
         tc_fence_before();
@@ -166,7 +172,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     const int nck = (Lb > 0 && !bad_len) ? (Lb + a.C - 1) / a.C : 1;
     if (bad_len || c >= nck) {  // uniform over the CTA
         if (bad_len && tid == 0 && c == 0 && rb == 0 && kvh == 0) flag_status(a.status, GRAFT_STATUS_LENGTH);
-        if (warp == 2) tmem_dealloc(tmem, 512);
+        if (warp == 1) tmem_dealloc(tmem, 512);
         return;
     }
     const int k0 = c * a.C;
@@ -189,67 +195,84 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         }
     };
     if (warp == 0) {
-        // ------------------------------------------------------------ TMA producer: Q, then K blocks
+        // ------------------------------------------------------------ TMA producer (lane 0)
+        // Q tiles, then K and V blocks in the order their stages free up.  Stages are released
+        // in the tensor pipe's order S_1(0), PV_1(0), S_1(1), PV_1(1), ..., so one thread that
+        // waits for each release in turn never waits behind a later one.
         if (lane == 0) {
-            const int nz = b * a.Kmax + (rb * 128) / a.G;
-            mbar_expect_tx(bar(BAR_Q), Q_TILE_BYTES);
-            for (int h = 0; h < 2; ++h)
-                tma_load_3d(base + OFF_Q + h * (Q_TILE_BYTES / 2), &maps.q, bar(BAR_Q), h * 64, kvh * a.G, nz);
-            for (int j = 0; j < nb; ++j) {
-                // a K stage frees as soon as its S product has run
-                if (j >= SK && !mbar_wait(bar(BAR_KE + j % SK), ((j / SK) - 1) & 1, kWaitNs)) {
-                    raise_abort(abort_flag, a.status);
-                    break;
-                }
-                if (aborted(abort_flag)) break;
+            mbar_expect_tx(bar(BAR_Q), ntile * Q_TILE_BYTES);
+            for (int t = 0; t < ntile; ++t) {
+                const int nz = b * a.Kmax + (rb * 256 + t * 128) / a.G;
+                for (int h = 0; h < 2; ++h)
+                    tma_load_3d(base + OFF_Q + t * Q_TILE_BYTES + h * (Q_TILE_BYTES / 2), &maps.q, bar(BAR_Q),
+                                h * 64, kvh * a.G, nz);
+            }
+            auto load_k = [&](int j) {
                 load_block(j, &maps.kc, &maps.kt, base + OFF_K + (j % SK) * BLK_BYTES, bar(BAR_KF + j % SK));
                 ++k_issued;
-            }
-        }
-    } else if (warp == 3) {
-        // ------------------------------------------------------------ TMA producer: V blocks
-        if (lane == 0) {
-            for (int j = 0; j < nb; ++j) {
-                // a V stage frees once its PV product has run
-                if (j >= SV && !mbar_wait(bar(BAR_VE + j % SV), ((j / SV) - 1) & 1, kWaitNs)) {
-                    raise_abort(abort_flag, a.status);
-                    break;
-                }
-                if (aborted(abort_flag)) break;
+            };
+            auto load_v = [&](int j) {
                 load_block(j, &maps.vc, &maps.vt, base + OFF_V + (j % SV) * BLK_BYTES, bar(BAR_VF + j % SV));
                 ++v_issued;
+            };
+            for (int j = 0; j < SK || j < SV; ++j) {
+                if (j < SK && j < nb) load_k(j);
+                if (j < SV && j < nb) load_v(j);
+            }
+            for (int i = 0; i < nb; ++i) {
+                // K(i + SK) reuses the stage S_1(i) released; V(i + SV) the one PV_1(i) released
+                if (i + SK < nb) {
+                    if (!mbar_wait(bar(BAR_KE + i % SK), (i / SK) & 1, kWaitNs)) {
+                        raise_abort(abort_flag, a.status);
+                        break;
+                    }
+                    if (aborted(abort_flag)) break;
+                    load_k(i + SK);
+                }
+                if (i + SV < nb) {
+                    if (!mbar_wait(bar(BAR_VE + i % SV), (i / SV) & 1, kWaitNs)) {
+                        raise_abort(abort_flag, a.status);
+                        break;
+                    }
+                    if (aborted(abort_flag)) break;
+                    load_v(i + SV);
+                }
             }
         }
+        __syncwarp();
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer (lane 0 issues)
         const uint32_t idS = idesc_bf16(128, BN, false, false);
         const uint32_t idO = idesc_bf16(128, HD, false, true);
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_QT), 0, kWaitNs));
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), 0, kWaitNs));
         // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
         // start-address field, which sits in the low bits and cannot carry out of them here
         // (every shared-memory address is below 256 KB).
+        const uint64_t q_desc = sdesc_sw128(base + OFF_Q, 16, 1024);
         const uint64_t k_desc = sdesc_sw128(base + OFF_K, 16, 1024);
         const uint64_t v_desc = sdesc_sw128(base + OFF_V, BOX_BYTES, 1024);
-        // S(j) into S/P buffer j % 2, then release K(j)
-        auto issue_S = [&](int j) -> bool {
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KF + j % SK), (j / SK) & 1, kWaitNs))) return false;
-            tc_fence_after();
+        // S_t(j) = Q_t K(j)^T into S_t; the last tile's product releases K(j)
+        auto issue_S = [&](int t, int j) -> bool {
+            if (t == 0) {
+                if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KF + j % SK), (j / SK) & 1, kWaitNs))) return false;
+                tc_fence_after();
+            }
             if (lane == 0) {
                 const uint64_t kd = k_desc + (((j % SK) * BLK_BYTES) >> 4);
-                const uint32_t d = tmem + TM_S + (j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-                    mma_bf16_ts(d, tmem + TM_Q + kk * 8, kd + (off >> 4), idS, kk > 0);
+                    const uint32_t qoff = t * Q_TILE_BYTES + (kk >> 2) * (Q_TILE_BYTES / 2) + (kk & 3) * 32;
+                    mma_bf16_ss(tmem + TM_S + t * 128, q_desc + (qoff >> 4), kd + (off >> 4), idS, kk > 0);
                 }
-                mma_commit(bar(BAR_S + (j & 1)));
-                mma_commit(bar(BAR_KE + j % SK));
+                mma_commit(bar(BAR_S + t));
+                if (t == ntile - 1) mma_commit(bar(BAR_KE + j % SK));
             }
             __syncwarp();
             return true;
         };
         if (ok) tc_fence_after();
-        for (int j = 0; j < 2 && j < nb && ok; ++j) ok = issue_S(j);
+        for (int t = 0; t < ntile && ok && nb > 0; ++t) ok = issue_S(t, 0);
         for (int j = 0; j < nb && ok; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + j % SV), (j / SV) & 1, kWaitNs));
             if (!ok) break;
@@ -264,228 +287,233 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_P + (j & 1)), (j >> 1) & 1, kWaitNs) && !aborted(abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint32_t p = tmem + TM_S + (j & 1) * 128;  // P as packed bf16 pairs
-                const uint64_t vd = v_desc + (((j % SV) * BLK_BYTES) >> 4);
+            for (int t = 0; t < ntile && ok; ++t) {
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(bar(BAR_P + t), j & 1, kWaitNs) && !aborted(abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint32_t p = tmem + TM_S + t * 128;  // P_t as packed bf16 pairs
+                    const uint64_t vd = v_desc + (((j % SV) * BLK_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_bf16_ts(tmem + TM_O, p + kk * 8, vd + ((kk * 2048) >> 4), idO, j > 0 || kk > 0);
-                mma_commit(bar(BAR_VE + j % SV));
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        mma_bf16_ts(tmem + TM_O + t * 128, p + kk * 8, vd + ((kk * 2048) >> 4), idO, j > 0 || kk > 0);
+                    if (t == ntile - 1) mma_commit(bar(BAR_VE + j % SV));
+                }
+                __syncwarp();
+                // this tile's next S right behind its PV: the other tile's softmax overlaps both
+                if (j + 1 < nb) ok = issue_S(t, j + 1);
             }
-            __syncwarp();
-            if (j + 2 < nb) ok = issue_S(j + 2);
         }
         if (!ok && lane == 0 && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
         if (lane == 0) mma_commit(bar(BAR_DONE));
         __syncwarp();
-    } else if (warp >= 4) {
-        // ------------------------------------------------------------ Q into TMEM, softmax, epilogue
+    } else {
+        // ------------------------------------------------------------ softmax + epilogue
+        const int t = (warp - 2) >> 2;
         const int quad = warp & 3;
         const int r = quad * 32 + lane;  // row within the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-        const int gr = rb * 128 + r;
-        const bool row_ok = gr < a.R;
+        const int gr = rb * 256 + t * 128 + r;
+        const bool row_ok = t < ntile && gr < a.R;
         const int node = row_ok ? gr / a.G : 0;
         const uint64_t anc = row_ok ? a.mask[(size_t)b * a.Kmax + node] : 0ull;
         const float sl2 = a.scale * 1.4426950408889634f;
         float m_used = -INFINITY, l_sum = 0.f;  // running max (log2 units) and row sum
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), 0, kWaitNs) && !aborted(abort_flag));
-        if (ok) {
-            // this thread's Q row: 16-byte chunk q of a 128-byte swizzled row sits at q ^ (row & 7)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint8_t* qrow = gbase + OFF_Q + h * (Q_TILE_BYTES / 2) + r * 128;
-                float w[32];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((q ^ (r & 7)) << 4));
-                    w[4 * q] = __uint_as_float(v.x);
-                    w[4 * q + 1] = __uint_as_float(v.y);
-                    w[4 * q + 2] = __uint_as_float(v.z);
-                    w[4 * q + 3] = __uint_as_float(v.w);
-                }
-                tmem_st32(tmem + lane_base + TM_Q + h * 32, w);
-            }
-            tmem_wait_st();
-        }
-        tc_fence_before();
-        mbar_arrive(bar(BAR_QT));
-        for (int j = 0; j < nb && ok; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + (j & 1)), (j >> 1) & 1, kWaitNs) &&
-                                             !aborted(abort_flag));
+        bool ok = true;
+        const uint32_t sbuf = tmem + lane_base + TM_S + t * 128;
+        for (int j = 0; j < nb && t < ntile; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + t), j & 1, kWaitNs) && !aborted(abort_flag));
             if (!ok) break;
             tc_fence_after();
-            const uint32_t sbuf = tmem + lane_base + TM_S + (j & 1) * 128;
             float s[BN];
 #pragma unroll
             for (int q = 0; q < BN / 32; ++q) tmem_ld32(sbuf + q * 32, s + q * 32);
             tmem_wait_ld();
             const bool tree_blk = j >= nb_prefix;
             if (tree_blk || j == ragged_block) {
-                // only the ragged tail and the tree block need masking; tree keys are < 64
+                // only the ragged tail and the tree block need masking: keep-bits for the
+                // block's keys as four 32-bit words (tree keys are < 64, in the ancestor mask)
                 const int valid = tree_blk ? a.Kmax : ragged_valid;
+                uint32_t w[4];
 #pragma unroll
-                for (int i = 0; i < BN; ++i) {
-                    bool keep = i < valid;
-                    if (tree_blk) keep = keep && i < 64 && ((anc >> (i & 63)) & 1ull);
-                    s[i] = keep ? s[i] : -INFINITY;
+                for (int q = 0; q < 4; ++q) {
+                    const int n = valid - 32 * q;
+                    w[q] = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
                 }
-            }
-            float mx = fmaxf(s[0], s[1]);
+                if (tree_blk) {
+                    w[0] &= (uint32_t)anc;
+                    w[1] &= (uint32_t)(anc >> 32);
+                    w[2] = w[3] = 0u;
+                }
 #pragma unroll
-            for (int i = 2; i < BN; i += 2) mx = fmaxf(mx, fmaxf(s[i], s[i + 1]));
-            mx *= sl2;  // sl2 > 0: the maximum commutes with the scale
+                for (int i = 0; i < BN; ++i) s[i] = ((w[i >> 5] >> (i & 31)) & 1u) ? s[i] : -INFINITY;
+            }
+            // block maximum by a tree of pairwise maxima (short dependency chains)
+            float m8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float m = fmaxf(s[i], s[i + 8]);
+#pragma unroll
+                for (int k = 16; k < BN; k += 16) m = fmaxf(m, fmaxf(s[i + k], s[i + k + 8]));
+                m8[i] = m;
+            }
+            const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                   fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;  // sl2 > 0
+            // raise the running maximum of the rows that need it; their O and row sum are
+            // rescaled by 2^(m_used - m_new) below, once the S values are no longer live
+            float alpha = 1.f;
+            bool rescale = false;
             if (j == 0) {
                 m_used = mx;
             } else if (__any_sync(0xffffffffu, mx > m_used + RESCALE_LOG2)) {
-                // raise the running maximum of the rows that need it and rescale their O by
-                // 2^(m_used - m_new); the previous PV must have landed first (whole warp).  Its
-                // completion is the V-release barrier of block j - 1.  S(j) was committed after
-                // PV(j - 2), so that barrier's earlier phase (block j - 1 - SV) has completed, and
-                // PV(j - 1 + SV) cannot have completed before this softmax hands over block j: the
-                // parity names block j - 1 unambiguously.
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(bar(BAR_VE + (j - 1) % SV), ((j - 1) / SV) & 1, kWaitNs));
-                if (!ok) break;
-                tc_fence_after();
                 const float m_new = fmaxf(mx, m_used);
-                const float alpha = (m_used == -INFINITY) ? 1.f : ex2(m_used - m_new);
-                for (int c0 = 0; c0 < HD; c0 += 32) {
-                    float o[32];
-                    tmem_ld32(tmem + lane_base + TM_O + c0, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    tmem_st32(tmem + lane_base + TM_O + c0, o);
-                }
-                tmem_wait_st();
-                l_sum *= alpha;
+                alpha = (m_used == -INFINITY) ? 1.f : ex2(m_used - m_new);
                 m_used = m_new;
+                rescale = true;
             }
             const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
             const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
             float2 acc = make_float2(0.f, 0.f);
+            // The two tiles take turns at the exponentials (tile 0 first in every block), so
+            // one tile's P is ready early and its PV and next S run on the tensor pipe while
+            // the other tile's exponentials run, instead of both P arriving together.
+            if (ntile == 2 && (t == 1 || j > 0)) {
+                const int ph = t == 1 ? (j & 1) : ((j - 1) & 1);
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_TURN + t), ph, kWaitNs) && !aborted(abort_flag));
+                if (!ok) break;
+            }
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float packed[32];
+            for (int hh = 0; hh < 4; ++hh) {
+                float packed[16];
 #pragma unroll
-                for (int i = 0; i < 64; i += 2) {
-                    const float2 x = __ffma2_rn(make_float2(s[hh * 64 + i], s[hh * 64 + i + 1]), sc2, nm2);
+                for (int i = 0; i < 32; i += 2) {
+                    const float2 x = __ffma2_rn(make_float2(s[hh * 32 + i], s[hh * 32 + i + 1]), sc2, nm2);
                     __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2(x.x), ex2(x.y));
                     // the row sum adds the same rounded weights the PV product uses
                     acc = __fadd2_rn(acc, make_float2(__low2float(h2), __high2float(h2)));
                     packed[i / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&h2));
                 }
-                tmem_st32(sbuf + hh * 32, packed);  // P over the first 64 columns of its S buffer
+                tmem_st16(sbuf + hh * 16, packed);  // P over the first 64 columns of S_t
             }
-            l_sum += acc.x + acc.y;
+            if (ntile == 2) mbar_arrive(bar(BAR_TURN + (1 - t)));
+            if (rescale) {
+                // S_t(j) was issued after PV_t(j - 1) on the in-order tensor pipe, so its
+                // completion means O_t already holds every earlier block; PV_t(j) waits for P_t(j)
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_base + TM_O + t * 128 + c0, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                    tmem_st32(tmem + lane_base + TM_O + t * 128 + c0, o);
+                }
+            }
+            l_sum = l_sum * alpha + (acc.x + acc.y);
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar(BAR_P + (j & 1)));
+            mbar_arrive(bar(BAR_P + t));
         }
         if (!ok && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
         // ------------------------------------------------------------ epilogue
-        if (ok && nb > 0) {
-            // every MMA, the last PV included, has completed (one-shot barrier: no phase ambiguity)
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_DONE), 0, kWaitNs));
-            if (!ok) raise_abort(abort_flag, a.status);
-        }
-        const bool direct = (nck == 1);
-        const float inv = (row_ok && l_sum > 0.f) ? 1.f / l_sum : 0.f;
-        if (ok) {
-            tc_fence_after();
-            // stage this thread's row, 16-byte chunks permuted by the row index so a warp's
-            // 32 rows spread over all banks
-            uint8_t* srow = gbase + OFF_STAGE + r * (direct ? 256 : 512);
-            for (int c0 = 0; c0 < HD; c0 += 32) {
-                float o[32];
-                tmem_ld32(tmem + lane_base + TM_O + c0, o);
-                tmem_wait_ld();
-                if (direct) {
+        if (t < ntile) {
+            if (ok && nb > 0) {
+                // every MMA, the last PV included, has completed (one-shot barrier: no phase ambiguity)
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_DONE), 0, kWaitNs));
+                if (!ok) raise_abort(abort_flag, a.status);
+            }
+            const bool direct = (nck == 1);
+            const float inv = (row_ok && l_sum > 0.f) ? 1.f / l_sum : 0.f;
+            uint8_t* stile = gbase + OFF_STAGE + t * (128 * 512);
+            if (ok) {
+                tc_fence_after();
+                // stage this thread's row, 16-byte chunks permuted by the row index so a warp's
+                // 32 rows spread over all banks
+                uint8_t* srow = stile + r * (direct ? 256 : 512);
+                for (int c0 = 0; c0 < HD; c0 += 32) {
+                    float o[32];
+                    tmem_ld32(tmem + lane_base + TM_O + t * 128 + c0, o);
+                    tmem_wait_ld();
+                    if (direct) {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 8) {
-                        uint4 v;
-                        __nv_bfloat162 x0 = __floats2bfloat162_rn(o[i] * inv, o[i + 1] * inv);
-                        __nv_bfloat162 x1 = __floats2bfloat162_rn(o[i + 2] * inv, o[i + 3] * inv);
-                        __nv_bfloat162 x2 = __floats2bfloat162_rn(o[i + 4] * inv, o[i + 5] * inv);
-                        __nv_bfloat162 x3 = __floats2bfloat162_rn(o[i + 6] * inv, o[i + 7] * inv);
-                        v.x = *reinterpret_cast<uint32_t*>(&x0);
-                        v.y = *reinterpret_cast<uint32_t*>(&x1);
-                        v.z = *reinterpret_cast<uint32_t*>(&x2);
-                        v.w = *reinterpret_cast<uint32_t*>(&x3);
-                        const int chunk = (c0 + i) / 8;  // 0..15
-                        *reinterpret_cast<uint4*>(srow + ((chunk ^ (r & 15)) << 4)) = v;
-                    }
-                } else {
+                        for (int i = 0; i < 32; i += 8) {
+                            uint4 v;
+                            __nv_bfloat162 x0 = __floats2bfloat162_rn(o[i] * inv, o[i + 1] * inv);
+                            __nv_bfloat162 x1 = __floats2bfloat162_rn(o[i + 2] * inv, o[i + 3] * inv);
+                            __nv_bfloat162 x2 = __floats2bfloat162_rn(o[i + 4] * inv, o[i + 5] * inv);
+                            __nv_bfloat162 x3 = __floats2bfloat162_rn(o[i + 6] * inv, o[i + 7] * inv);
+                            v.x = *reinterpret_cast<uint32_t*>(&x0);
+                            v.y = *reinterpret_cast<uint32_t*>(&x1);
+                            v.z = *reinterpret_cast<uint32_t*>(&x2);
+                            v.w = *reinterpret_cast<uint32_t*>(&x3);
+                            const int chunk = (c0 + i) / 8;  // 0..15
+                            *reinterpret_cast<uint4*>(srow + ((chunk ^ (r & 15)) << 4)) = v;
+                        }
+                    } else {
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const int chunk = (c0 + i) / 4;  // 0..31
-                        *reinterpret_cast<float4*>(srow + ((chunk ^ (r & 31)) << 4)) =
-                            make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+                        for (int i = 0; i < 32; i += 4) {
+                            const int chunk = (c0 + i) / 4;  // 0..31
+                            *reinterpret_cast<float4*>(srow + ((chunk ^ (r & 31)) << 4)) =
+                                make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+                        }
                     }
                 }
             }
-        }
-        mbar_arrive(bar(BAR_EPI));
-        const bool staged = __all_sync(0xffffffffu, mbar_wait(bar(BAR_EPI), 0, kWaitNs));
-        if (!staged) {
-            raise_abort(abort_flag, a.status);
-            ok = false;
-        }
-        if (ok) {
-            // write the tile out along contiguous rows; 128 threads
-            const uint8_t* stile = gbase + OFF_STAGE;
-            if (direct) {
-                for (int k = r; k < 128 * 16; k += 128) {
-                    const int row = k >> 4, cc = k & 15;
-                    const int g = rb * 128 + row;
-                    if (g >= a.R) continue;
-                    const int nd = g / a.G, hh = kvh * a.G + g % a.G;
-                    const uint4 v = *reinterpret_cast<const uint4*>(stile + row * 256 + ((cc ^ (row & 15)) << 4));
-                    __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.O) +
-                                         (((size_t)b * a.Kmax + nd) * a.Hq + hh) * HD + cc * 8;
-                    *reinterpret_cast<uint4*>(dst) = v;
+            mbar_arrive(bar(BAR_EPI + t));
+            const bool staged = __all_sync(0xffffffffu, mbar_wait(bar(BAR_EPI + t), 0, kWaitNs));
+            if (!staged) {
+                raise_abort(abort_flag, a.status);
+                ok = false;
+            }
+            if (ok) {
+                // write the tile out along contiguous rows; 128 threads of this tile
+                const int tile = rb * 2 + t;  // 128-row tile index within (b, kvh)
+                if (direct) {
+                    for (int k = r; k < 128 * 16; k += 128) {
+                        const int row = k >> 4, cc = k & 15;
+                        const int g = tile * 128 + row;
+                        if (g >= a.R) continue;
+                        const int nd = g / a.G, hh = kvh * a.G + g % a.G;
+                        const uint4 v = *reinterpret_cast<const uint4*>(stile + row * 256 + ((cc ^ (row & 15)) << 4));
+                        __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(a.O) +
+                                             (((size_t)b * a.Kmax + nd) * a.Hq + hh) * HD + cc * 8;
+                        *reinterpret_cast<uint4*>(dst) = v;
+                    }
+                } else {
+                    const size_t pbase = ((((size_t)b * a.Hkv + kvh) * a.nRB + tile) * a.nchunk + c) * 128;
+                    float* dst = a.part_o + pbase * HD;
+                    for (int k = r; k < 128 * 32; k += 128) {
+                        const int row = k >> 5, cc = k & 31;
+                        const float4 v = *reinterpret_cast<const float4*>(stile + row * 512 + ((cc ^ (row & 31)) << 4));
+                        *reinterpret_cast<float4*>(dst + row * HD + cc * 4) = v;
+                    }
+                    if (row_ok) a.part_lse[pbase + r] = m_used + log2f(l_sum);
                 }
-            } else {
-                const size_t pbase = ((((size_t)b * a.Hkv + kvh) * a.nRB + rb) * a.nchunk + c) * 128;
-                float* dst = a.part_o + pbase * HD;
-                for (int k = r; k < 128 * 32; k += 128) {
-                    const int row = k >> 5, cc = k & 31;
-                    const float4 v = *reinterpret_cast<const float4*>(stile + row * 512 + ((cc ^ (row & 31)) << 4));
-                    *reinterpret_cast<float4*>(dst + row * HD + cc * 4) = v;
-                }
-                if (row_ok) a.part_lse[pbase + r] = m_used + log2f(l_sum);
             }
         }
     }
     // ---------------------------------------------------------------- teardown
-    if (lane == 0 && (warp == 0 || warp == 3) && aborted(abort_flag)) {
-        // loads still in flight write into this CTA's shared memory: each producer waits for
-        // the last armed phase of every stage it used (and the Q load) before the CTA may exit
-        if (warp == 0) {
-            mbar_wait(bar(BAR_Q), 0, kDrainNs);
-            for (int st = 0; st < SK; ++st) {
-                const int n = (k_issued - st + SK - 1) / SK;
-                if (n > 0) mbar_wait(bar(BAR_KF + st), (n - 1) & 1, kDrainNs);
-            }
-        } else {
-            for (int st = 0; st < SV; ++st) {
-                const int n = (v_issued - st + SV - 1) / SV;
-                if (n > 0) mbar_wait(bar(BAR_VF + st), (n - 1) & 1, kDrainNs);
-            }
+    if (warp == 0 && lane == 0 && aborted(abort_flag)) {
+        // loads still in flight write into this CTA's shared memory: the producer waits for the
+        // last armed phase of every stage it used (and the Q load) before the CTA may exit
+        mbar_wait(bar(BAR_Q), 0, kDrainNs);
+        for (int st = 0; st < SK; ++st) {
+            const int n = (k_issued - st + SK - 1) / SK;
+            if (n > 0) mbar_wait(bar(BAR_KF + st), (n - 1) & 1, kDrainNs);
+        }
+        for (int st = 0; st < SV; ++st) {
+            const int n = (v_issued - st + SV - 1) / SV;
+            if (n > 0) mbar_wait(bar(BAR_VF + st), (n - 1) & 1, kDrainNs);
         }
     }
-    if (warp == 2 && lane == 0) {
+    if (warp == 1 && lane == 0) {
         // every issued MMA has completed before TMEM is released
         mbar_wait(bar(BAR_DONE), 0, kWaitNs);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 2) tmem_dealloc(tmem, 512);
+    if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -549,13 +577,11 @@ int attn_tc_launch(const AttnArgs& a, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES) !=
-            cudaSuccess)
+        if (!cuda_ok(cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES)))
             return GRAFT_ERR_CUDA;
         attr_set[dev] = true;
     }
-    dim3 grid(a.nRB * a.Hkv, a.nchunk, a.B);
-    launch_pdl(attn_tc_kernel, grid, dim3(NTHREADS), SMEM_BYTES, st, m, a);
+    launch_pdl(attn_tc_kernel, dim3(((a.nRB + 1) / 2) * a.Hkv, a.nchunk, a.B), dim3(NTHREADS), SMEM_BYTES, st, m, a);
     count_launches(1);
     const int rc = launch_status();
     if (rc != GRAFT_OK) return rc;

@@ -579,7 +579,7 @@ extern "C" int graft_build_tree(const GraftConfig* cfg, int B, const float* draf
     const int max_pool = cfg->k + (cfg->D - 1) * cfg->k * cfg->k;
     const size_t smem = (size_t)max_pool * sizeof(float);
     if (smem > 48 * 1024) {
-        if (cudaFuncSetAttribute(draft_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        if (!cuda_ok(cudaFuncSetAttribute(draft_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)))
             return GRAFT_ERR_CUDA;
     }
     launch_pdl(draft_merge_kernel, dim3(B), dim3(kMergeThreads), smem, st, mp, root_tok, L, w, tree_tok, tree_parent, tree_depth,

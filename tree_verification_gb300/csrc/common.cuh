@@ -42,8 +42,20 @@ inline bool ws_ok(const void* ws, size_t have, size_t need) {
     return (reinterpret_cast<uintptr_t>(ws) % kWsAlign) == 0;
 }
 
+// Records a CUDA runtime error for graft_last_cuda_error (per host thread).
+void note_cuda_error(cudaError_t e);
+
+inline bool cuda_ok(cudaError_t e) {
+    if (e == cudaSuccess) return true;
+    note_cuda_error(e);
+    return false;
+}
+
 inline int launch_status() {
-    return cudaGetLastError() == cudaSuccess ? GRAFT_OK : GRAFT_ERR_CUDA;
+    const cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) return GRAFT_OK;
+    note_cuda_error(e);
+    return GRAFT_ERR_CUDA;
 }
 
 // Counts kernel launches enqueued by the library (graft_launch_count).
