@@ -35,7 +35,8 @@ if ROOT not in sys.path:
 METRIC = "tree-verify steps/s; tree-attention HBM GB/s vs GB300 peak; retrieval fill µs"
 UNIT = "steps/s"
 FALLBACK_HBM_GBS = 6800.0
-ATTN_SOURCES = ["attention_mma.cu", "attention.cuh", "attention_api.cu"]
+ATTN_SOURCES = ["attention_tc.cu", "attention_tc1.cu", "attention_mma.cu", "attention.cuh", "attention_api.cu",
+                "tc_ptx.cuh", "common.cuh"]
 
 
 def parse_args():

@@ -224,16 +224,18 @@ def test_attention_parity(B, Hq, Hkv, Kmax, Ls, Lcap):
     assert_attention_close(to_np(O), ref)
 
 
-@pytest.mark.parametrize("tiles", ["1", "2"])
+@pytest.mark.parametrize("tiles,cluster", [("1", "0"), ("1", "1"), ("2", "1")])
 @pytest.mark.parametrize("min_chunk", ["128", "384", "1000000"])
 @pytest.mark.parametrize("B,Hq,Hkv,Kmax,Ls,Lcap", [
     (2, 32, 8, 64, [4096, 777], 4160),
     (3, 16, 2, 48, [0, 1500, 300], 1536),      # three tiles: the last CTA pair has one
 ])
-def test_attention_parity_tilings_chunkings(monkeypatch, tiles, min_chunk, B, Hq, Hkv, Kmax, Ls, Lcap):
-    """Both tcgen05 kernels (one and two 128-row tiles per CTA) with key chunks of one block, of
-    three blocks, and one chunk per request (no combine)."""
+def test_attention_parity_tilings_chunkings(monkeypatch, tiles, cluster, min_chunk, B, Hq, Hkv, Kmax, Ls, Lcap):
+    """Both tcgen05 kernels (one and two 128-row tiles per CTA; the one-tile kernel with its split-key
+    partials merged by the merge kernel or inside a cluster) with key chunks of one block, of three
+    blocks, and one chunk per request."""
     monkeypatch.setenv("GRAFT_ATTN_TILES", tiles)
+    monkeypatch.setenv("GRAFT_ATTN_CLUSTER", cluster)
     monkeypatch.setenv("GRAFT_ATTN_MIN_CHUNK", min_chunk)
     Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed=7 * B + Kmax)
     status = _status()

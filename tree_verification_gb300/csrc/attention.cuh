@@ -13,6 +13,7 @@ struct AttnArgs {
     int B, Hq, Hkv, G, Kmax, R;  // R = Kmax * G query rows per (request, KV head)
     int nRB;                      // 128-row blocks per (request, KV head)
     int tiles;                    // tcgen05 path: 128-row tiles per CTA (1 or 2)
+    int cluster;                  // one-tile kernel: chunks reduced in a thread-block cluster (0: off)
     int C;                        // prefix keys per chunk (multiple of 128)
     int nchunk;                   // chunks per (request, KV head) allowed by Lcap
     int Lcap;
@@ -37,7 +38,8 @@ int attn_mma_launch(const AttnArgs& a, cudaStream_t st);
 bool attn_tc_supported(int G);
 int attn_tc_launch(const AttnArgs& a, cudaStream_t st);
 int attn_tc1_launch(const AttnArgs& a, cudaStream_t st);
-// Merges split-key partials (no-op when every request fits one chunk).
+// Merges split-key partials (no-op when every request fits one chunk or a
+// cluster reduced them).
 int attn_combine_launch(const AttnArgs& a, cudaStream_t st);
 
 }  // namespace graft

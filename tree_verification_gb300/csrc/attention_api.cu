@@ -13,7 +13,7 @@ namespace graft {
 namespace {
 
 struct AttnPlan {
-    int G, R, nRB, C, nchunk, tiles;
+    int G, R, nRB, C, nchunk, tiles, cluster;
     bool tc;
 };
 
@@ -26,6 +26,13 @@ struct AttnPlan {
 // every K/V block, unless that plan would leave each CTA fewer than 1024
 // keys; then one tile per CTA (twice the CTAs, a shorter prologue) does
 // better.  A single row block always goes to the two-tile kernel.
+//
+// GRAFT_ATTN_CLUSTER=1 makes the chunks of a row tile (one tile per CTA,
+// split keys) run as one thread-block cluster (at most 8 CTAs, so the chunk
+// count is capped at 8) that merges its partials in distributed shared
+// memory instead of the merge kernel.  It is off by default: clusters of
+// single-SM CTAs did not all fit at once on the measured shapes and ran
+// slower than the merge kernel.
 // GRAFT_ATTN_MIN_CHUNK and GRAFT_ATTN_TILES (1 or 2) override the policy for
 // tuning and tests; the workspace size and the launch read the same values.
 long long chunk_keys(long long Lcap, long long units, int sms, long long min_chunk) {
@@ -67,12 +74,24 @@ AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
     p.C = (int)chunk_keys(Lcap, units, sms, min_chunk);
     p.nchunk = Lcap > 0 ? (int)((Lcap + p.C - 1) / p.C) : 1;
     if (p.nchunk < 1) p.nchunk = 1;
+    p.cluster = 0;
+    const char* cenv = getenv("GRAFT_ATTN_CLUSTER");
+    if (p.tc && p.tiles == 1 && p.nchunk > 1 && cenv && atoi(cenv) == 1) {
+        if (p.nchunk > 8) {
+            long long C = (Lcap + 7) / 8;
+            C = (C + blk - 1) / blk * blk;
+            if (C < min_chunk) C = min_chunk;
+            p.C = (int)C;
+            p.nchunk = (int)((Lcap + C - 1) / C);
+        }
+        if (p.nchunk > 1) p.cluster = p.nchunk;
+    }
     return p;
 }
 
 size_t attn_ws(const AttnPlan& p, int B, int Hkv, AttnArgs* a, void* ws) {
     WsCarver c(ws);
-    const size_t parts = p.nchunk > 1 ? (size_t)B * Hkv * p.nRB * p.nchunk * 128 : 0;
+    const size_t parts = (p.nchunk > 1 && p.cluster == 0) ? (size_t)B * Hkv * p.nRB * p.nchunk * 128 : 0;
     float* po = c.take<float>(parts * GRAFT_HEAD_DIM);
     float* pl = c.take<float>(parts);
     if (a) {
@@ -134,6 +153,7 @@ extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Km
     a.R = p.R;
     a.nRB = p.nRB;
     a.tiles = p.tiles;
+    a.cluster = p.cluster;
     a.C = p.C;
     a.nchunk = p.nchunk;
     a.Lcap = (int)Lcap;

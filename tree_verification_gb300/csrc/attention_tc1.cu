@@ -43,7 +43,12 @@
 // so stale cache rows cannot inject NaN.
 //
 // The epilogue stages the tile's rows through the freed K/V ring memory and
-// writes them out along contiguous rows.
+// writes them out along contiguous rows.  When the key chunks of a row tile
+// run as one thread-block cluster (a.cluster > 0: the chunk count, at most
+// 8), each CTA stages its normalised partial rows and their log2-sum-exp in
+// shared memory instead, and after a cluster barrier every CTA merges a
+// slice of the rows across the cluster through distributed shared memory
+// and writes them: no partials reach global memory and no merge kernel runs.
 //
 // Every mbarrier wait is bounded; on timeout the CTA raises
 // GRAFT_STATUS_TIMEOUT in the status word, stops issuing work, drains what
@@ -76,6 +81,7 @@ constexpr uint32_t OFF_K = OFF_Q + Q_TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + SK * BLK_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + SV * BLK_BYTES;
 constexpr uint32_t OFF_STAGE = OFF_K;  // epilogue staging reuses the rings once every MMA has run
+constexpr uint32_t OFF_LSE = OFF_STAGE + 128 * 512;  // cluster mode: the staged rows' log2-sum-exp
 // barriers
 constexpr int BAR_Q = 0;              // Q tile landed in shared memory
 constexpr int BAR_QT = 1;             // Q copied into TMEM (128 arrivals)
@@ -94,7 +100,7 @@ constexpr int N_BARS = BAR_EPI + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;  // tmem slot, abort flag
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
-static_assert(128 * 128 * 4 <= SK * BLK_BYTES + SV * BLK_BYTES, "staging fits in the rings");
+static_assert(128 * 128 * 4 + 128 * 4 <= SK * BLK_BYTES + SV * BLK_BYTES, "staging fits in the rings");
 static_assert(BN == 128, "one S/P buffer is 128 columns, P its first 64");
 
 constexpr uint32_t TM_S = 0;    // + buf * 128
@@ -136,6 +142,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     const int kvh = blockIdx.x / a.nRB;
     const int c = blockIdx.y;
     const int b = blockIdx.z;
+    const int ncl = a.cluster;  // > 0: the chunks of this row tile form one cluster (rank = c)
 
     // Prologue that touches no global memory: it overlaps the previous kernel's tail.
     if (tid == 0) {
@@ -168,15 +175,17 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     const int Lb = a.L[b];
     const bool bad_len = Lb < 0 || Lb > a.Lcap;
     const int nck = (Lb > 0 && !bad_len) ? (Lb + a.C - 1) / a.C : 1;
-    if (bad_len || c >= nck) {  // uniform over the CTA
+    if (bad_len || (c >= nck && ncl == 0)) {  // uniform over the CTA (and over a cluster: same b)
         if (bad_len && tid == 0 && c == 0 && rb == 0 && kvh == 0) flag_status(a.status, GRAFT_STATUS_LENGTH);
         if (warp == 2) tmem_dealloc(tmem, 512);
         return;
     }
+    // in a cluster a chunk past the request's keys stays for the merge and contributes nothing
+    const bool empty = c >= nck;
     const int k0 = c * a.C;
-    const int k1 = min(Lb, k0 + a.C);
+    const int k1 = empty ? k0 : min(Lb, k0 + a.C);
     const int nb_prefix = (k1 - k0 + BN - 1) / BN;
-    const bool has_tree = (c == nck - 1);
+    const bool has_tree = !empty && (c == nck - 1);
     const int nb = nb_prefix + (has_tree ? 1 : 0);
     const int ragged_block = ((k1 - k0) % BN) != 0 ? nb_prefix - 1 : -1;
     const int ragged_valid = (k1 - k0) % BN;
@@ -397,7 +406,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_DONE), 0, kWaitNs));
             if (!ok) raise_abort(abort_flag, a.status);
         }
-        const bool direct = (nck == 1);
+        const bool direct = (nck == 1) && ncl == 0;
         const float inv = (row_ok && l_sum > 0.f) ? 1.f / l_sum : 0.f;
         if (ok) {
             tc_fence_after();
@@ -406,8 +415,13 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             uint8_t* srow = gbase + OFF_STAGE + r * (direct ? 256 : 512);
             for (int c0 = 0; c0 < HD; c0 += 32) {
                 float o[32];
-                tmem_ld32(tmem + lane_base + TM_O + c0, o);
-                tmem_wait_ld();
+                if (nb > 0) {
+                    tmem_ld32(tmem + lane_base + TM_O + c0, o);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) o[i] = 0.f;  // no block ran: O was never written
+                }
                 if (direct) {
 #pragma unroll
                     for (int i = 0; i < 32; i += 8) {
@@ -432,6 +446,9 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                     }
                 }
             }
+            if (ncl > 0)
+                reinterpret_cast<float*>(gbase + OFF_LSE)[r] =
+                    (row_ok && l_sum > 0.f) ? m_used + log2f(l_sum) : -INFINITY;
         }
         mbar_arrive(bar(BAR_EPI));
         const bool staged = __all_sync(0xffffffffu, mbar_wait(bar(BAR_EPI), 0, kWaitNs));
@@ -439,7 +456,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             raise_abort(abort_flag, a.status);
             ok = false;
         }
-        if (ok) {
+        if (ok && ncl == 0) {
             // write the tile out along contiguous rows; 128 threads
             const uint8_t* stile = gbase + OFF_STAGE;
             if (direct) {
@@ -490,6 +507,50 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     __syncthreads();
     tc_fence_after();
     if (warp == 2) tmem_dealloc(tmem, 512);
+    if (ncl > 0) {
+        // ------------------------------------------------------------ merge across the cluster
+        // every CTA's staged rows and log2-sum-exp are complete and visible cluster-wide; this
+        // CTA merges rows [r0, r1): O = sum_k 2^(lse_k - lse) O_k with lse = log2 sum_k 2^lse_k,
+        // one warp per row, four dims per lane, partials read from the other CTAs' shared memory
+        cluster_sync();
+        const int rows_per = (128 + ncl - 1) / ncl;
+        const int r0 = c * rows_per, r1 = min(128, r0 + rows_per);
+        const uint32_t stage_l = base + OFF_STAGE, lse_l = base + OFF_LSE;
+        for (int row = r0 + warp; row < r1; row += NTHREADS / 32) {
+            const int g = rb * 128 + row;
+            if (g >= a.R) continue;
+            const float lk = lane < ncl ? dsmem_ld_f32(dsmem_addr(lse_l + row * 4, (uint32_t)lane)) : -INFINITY;
+            float mx = lk;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float wk = (lk == -INFINITY) ? 0.f : ex2(lk - mx);
+            float wsum = wk;
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            const uint32_t src = stage_l + row * 512 + ((lane ^ (row & 31)) << 4);
+            for (int k = 0; k < ncl; ++k) {
+                const float w = __shfl_sync(0xffffffffu, wk, k);
+                if (w == 0.f) continue;  // uniform over the warp
+                const float4 v = dsmem_ld_f32x4(dsmem_addr(src, (uint32_t)k));
+                acc.x += w * v.x;
+                acc.y += w * v.y;
+                acc.z += w * v.z;
+                acc.w += w * v.w;
+            }
+            const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+            const int nd = g / a.G, hh = kvh * a.G + g % a.G;
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+            uint2 v;
+            v.x = *reinterpret_cast<uint32_t*>(&lo);
+            v.y = *reinterpret_cast<uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.O) +
+                                      (((size_t)b * a.Kmax + nd) * a.Hq + hh) * HD + lane * 4) = v;
+        }
+        // no CTA leaves (and frees its shared memory) while another still reads it
+        cluster_sync();
+    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -556,7 +617,27 @@ int attn_tc1_launch(const AttnArgs& a, cudaStream_t st) {
         attr_set[dev] = true;
     }
     dim3 grid(a.nRB * a.Hkv, a.nchunk, a.B);
-    launch_pdl(attn_tc_kernel, grid, dim3(NTHREADS), SMEM_BYTES, st, m, a);
+    if (a.cluster > 0) {
+        // the chunks of one row tile form a cluster along y; portable cluster sizes only
+        if (a.cluster > 8 || a.cluster != a.nchunk) return GRAFT_ERR_INVALID_ARG;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = grid;
+        cfg.blockDim = dim3(NTHREADS);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[2];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = 1;
+        attr[1].val.clusterDim.y = (unsigned)a.cluster;
+        attr[1].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 2;
+        cudaLaunchKernelEx(&cfg, attn_tc_kernel, m, a);
+    } else {
+        launch_pdl(attn_tc_kernel, grid, dim3(NTHREADS), SMEM_BYTES, st, m, a);
+    }
     count_launches(1);
     const int rc = launch_status();
     if (rc != GRAFT_OK) return rc;
