@@ -22,7 +22,13 @@ import numpy as np
 def accept(target_logits_b: np.ndarray, tok: Sequence[int], parent: Sequence[int], depth: Sequence[int]):
     """One request: returns (argmax [Kmax], acc_len, path [acc_len], out_tok [acc_len], bonus)."""
     Kmax = len(tok)
-    g = [int(np.argmax(target_logits_b[i])) for i in range(Kmax)]
+    return accept_from_argmax([int(np.argmax(target_logits_b[i])) for i in range(Kmax)], tok, parent, depth)
+
+
+def accept_from_argmax(g: Sequence[int], tok: Sequence[int], parent: Sequence[int], depth: Sequence[int]):
+    """The same acceptance given the target's argmax g[i] at every node directly."""
+    Kmax = len(tok)
+    g = [int(x) for x in g]
     ok = [False] * Kmax
     ok[0] = True
     for i in range(1, Kmax):
