@@ -33,7 +33,9 @@ def argmax_rows(lg: np.ndarray):
 
 
 def margins(lg: np.ndarray) -> np.ndarray:
-    """Gap between each row's largest and second-largest logit (0 for a tie)."""
+    """Gap between each row's largest and second-largest logit (0 for a tie; infinite with one token)."""
+    if lg.shape[1] < 2:
+        return np.full(lg.shape[0], np.inf)
     top2 = np.partition(lg, -2, axis=1)[:, -2:]
     return top2[:, 1] - top2[:, 0]
 

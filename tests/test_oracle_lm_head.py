@@ -66,3 +66,10 @@ def test_accept_from_argmax_matches_logits_path():
     b = oacc.accept_from_argmax(np.argmax(logits, axis=1), tok, parent, depth)
     assert a == b
     assert a[1] >= 2
+
+
+def test_single_token_vocabulary():
+    H = np.ones((3, 4))
+    W = np.full((1, 4), -2.0)
+    g, mx, mg = olm.lm_head_argmax(H, W)
+    assert g.tolist() == [0, 0, 0] and mx.tolist() == [-8.0] * 3 and np.all(np.isinf(mg))
