@@ -200,6 +200,10 @@ int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Kmax, const v
  * Cache row L[b] + t receives tree row path[b][t] for t < acc_len[b] in every
  * layer.  A request whose cache would overflow sets
  * GRAFT_STATUS_CACHE_OVERFLOW and is left uncompacted with L unchanged.
+ * target_logits may be NULL: argmax [B][Kmax] is then an INPUT holding the
+ * target's argmax per node (as graft_lm_head_argmax writes it; ids outside
+ * [0, V) set GRAFT_STATUS_TOKEN_RANGE and are treated as 0) and only the
+ * acceptance and compaction run.
  * Workspace: graft_accept_compact_workspace_size.
  */
 int graft_accept_compact_workspace_size(int B, int Kmax, int V, size_t* bytes);
@@ -211,6 +215,28 @@ int graft_accept_compact(int B, int Kmax, int V, int n_layers, const float* targ
                          int32_t* L, int32_t* argmax, int32_t* acc_len, int32_t* path,
                          int32_t* out_tok, int32_t* bonus, int32_t* status, void* ws,
                          size_t ws_bytes, graft_stream_t stream);
+
+/*
+ * graft_lm_head_argmax — the target's greedy token at every tree node
+ * straight from its final hidden states (Graft article, architecture
+ * paragraph: the tree is verified in one target forward; greedy acceptance
+ * needs only the argmax at each node).  g[n] = argmax_v sum_k H[n][k]
+ * W_lm[v][k] with ties to the lower id, computed on the tensor cores (bf16
+ * in, fp32 accumulation) without writing the [N][V] logits.
+ *
+ *   H [N][d_model] bf16      final hidden states of the N = B * Kmax nodes
+ *   W_lm [V][d_model] bf16   output embedding (lm_head) rows
+ * Outputs: argmax [N] i32; max_logit [N] f32 (the winning logit; may be
+ *   NULL).  d_model must be a multiple of 8; H and W_lm 16-byte aligned.
+ *   Rows whose two best logits differ by less than the fp32 rounding of the
+ *   sum may pick either (the rounding order is the kernel's).
+ * Feed argmax to graft_accept_compact with target_logits == NULL.
+ * Workspace: graft_lm_head_argmax_workspace_size (8 bytes per row).
+ */
+int graft_lm_head_argmax_workspace_size(int N, size_t* bytes);
+int graft_lm_head_argmax(int N, int d_model, int V, const void* H, const void* W_lm, int32_t* argmax,
+                         float* max_logit, int32_t* status, void* ws, size_t ws_bytes,
+                         graft_stream_t stream);
 
 /*
  * graft_update_M — online update of the adjacency table from verified

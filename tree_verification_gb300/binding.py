@@ -74,6 +74,8 @@ _SIGNATURES = {
     "graft_accept_compact_workspace_size": [_I, _I, _I, ctypes.POINTER(_SZ)],
     "graft_accept_compact": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I64, _P, _P, _P, _P, _P, _P,
                              _P, _P, _SZ, _P],
+    "graft_lm_head_argmax_workspace_size": [_I, ctypes.POINTER(_SZ)],
+    "graft_lm_head_argmax": [_I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P],
     "graft_update_M_workspace_size": [_I64, ctypes.POINTER(_SZ)],
     "graft_update_M": [_P, _P, _I, _I, _P, _P, _I64, _P, _P, _SZ, _P],
     "graft_update_M_noalloc": [_P, _P, _I, _I, _P, _P, _I64, _P, _P],
@@ -244,17 +246,24 @@ def layer_pointers(tensors: Sequence[torch.Tensor], device) -> torch.Tensor:
 
 def graft_accept_compact(target_logits, tree_tok, tree_parent, tree_depth, Kc_ptrs, Vc_ptrs, Kt_ptrs, Vt_ptrs,
                          n_layers: int, Hkv: int, Lcap: int, L, out: Optional[dict] = None, status=None, ws=None,
-                         stream=None, head_dim: int = HEAD_DIM) -> dict:
-    B, Kmax, V = target_logits.shape
-    _need(target_logits, "target_logits", torch.float32)
+                         stream=None, head_dim: int = HEAD_DIM, argmax=None, V: Optional[int] = None) -> dict:
+    """target_logits [B][Kmax][V] f32, or None with ``argmax`` [B][Kmax] i32 given (and V)."""
+    if target_logits is None:
+        if argmax is None or V is None:
+            raise ValueError("without target_logits pass argmax and V")
+        B, Kmax = argmax.shape
+        _need(argmax, "argmax", torch.int32, (B, Kmax))
+    else:
+        B, Kmax, V = target_logits.shape
+        _need(target_logits, "target_logits", torch.float32)
     for name, t in (("tree_tok", tree_tok), ("tree_parent", tree_parent), ("tree_depth", tree_depth)):
         _need(t, name, torch.int32, (B, Kmax))
     _need(L, "L", torch.int32, (B,))
     for name, t in (("Kc_ptrs", Kc_ptrs), ("Vc_ptrs", Vc_ptrs), ("Kt_ptrs", Kt_ptrs), ("Vt_ptrs", Vt_ptrs)):
         _need(t, name, torch.int64, (n_layers,))
-    dev = target_logits.device
+    dev = tree_tok.device
     if out is None:
-        out = dict(argmax=torch.empty(B, Kmax, dtype=torch.int32, device=dev),
+        out = dict(argmax=argmax if argmax is not None else torch.empty(B, Kmax, dtype=torch.int32, device=dev),
                    acc_len=torch.empty(B, dtype=torch.int32, device=dev),
                    path=torch.empty(B, Kmax, dtype=torch.int32, device=dev),
                    out_tok=torch.empty(B, Kmax, dtype=torch.int32, device=dev),
@@ -266,6 +275,29 @@ def graft_accept_compact(target_logits, tree_tok, tree_parent, tree_depth, Kc_pt
                                       _ptr(out["path"]), _ptr(out["out_tok"]), _ptr(out["bonus"]), _ptr(status),
                                       _ptr(ws), nws, _stream(stream)), "graft_accept_compact")
     return out
+
+
+def graft_lm_head_argmax_workspace_size(N: int) -> int:
+    n = _SZ()
+    _check(lib().graft_lm_head_argmax_workspace_size(N, ctypes.byref(n)), "workspace size")
+    return n.value
+
+
+def graft_lm_head_argmax(H, W_lm, argmax=None, max_logit=None, status=None, ws=None, stream=None):
+    """Greedy token per row of H [N][d] bf16 under the lm_head W_lm [V][d] bf16; returns (argmax, max_logit)."""
+    N, d = H.shape
+    V = W_lm.shape[0]
+    _need(H, "H", torch.bfloat16, (N, d))
+    _need(W_lm, "W_lm", torch.bfloat16, (V, d))
+    dev = H.device
+    if argmax is None:
+        argmax = torch.empty(N, dtype=torch.int32, device=dev)
+    if max_logit is None:
+        max_logit = torch.empty(N, dtype=torch.float32, device=dev)
+    ws, nws = _ws(graft_lm_head_argmax_workspace_size(N), dev, ws)
+    _check(lib().graft_lm_head_argmax(N, d, V, _ptr(H), _ptr(W_lm), _ptr(argmax), _ptr(max_logit), _ptr(status),
+                                      _ptr(ws), nws, _stream(stream)), "graft_lm_head_argmax")
+    return argmax, max_logit
 
 
 def graft_update_M_workspace_size(n: int) -> int:

@@ -11,7 +11,8 @@
 //   argmax_part_kernel  rows of B*Kmax fp32 logits split over CTAs; each CTA
 //                       streams its slice once (HBM bound) and keeps the
 //                       first maximum
-//   accept_kernel       one CTA per request: reduce the splits, test every
+//   accept_kernel       one CTA per request: reduce the splits (or read the
+//                       argmax the fused lm_head kernel wrote), test every
 //                       node's root path, pick the deepest accepted node,
 //                       write path / tokens / bonus and advance L
 //   compact_kernel      one CTA per (layer, request): copy the accepted
@@ -90,7 +91,7 @@ argmax_part_kernel(const float* __restrict__ logits, int V, int S, int chunk, Ar
 }
 
 __global__ void __launch_bounds__(GRAFT_MAX_KMAX)
-accept_kernel(int Kmax, int S, int64_t Lcap, const ArgPart* __restrict__ parts, const int32_t* __restrict__ tree_tok,
+accept_kernel(int Kmax, int S, int V, int64_t Lcap, const ArgPart* __restrict__ parts, const int32_t* __restrict__ tree_tok,
               const int32_t* __restrict__ tree_parent, const int32_t* __restrict__ tree_depth, int32_t* L,
               int32_t* argmax, int32_t* acc_len, int32_t* path, int32_t* out_tok, int32_t* bonus, AcceptWs w,
               int32_t* status) {
@@ -101,15 +102,22 @@ accept_kernel(int Kmax, int S, int64_t Lcap, const ArgPart* __restrict__ parts, 
     int key = -1;
     if (i < Kmax) {
         const size_t row = (size_t)b * Kmax + i;
-        float bv = -INFINITY;
-        int bi = INT_MAX;
-        for (int s = 0; s < S; ++s) {
-            const ArgPart p = parts[row * S + s];
-            if (better(p.v, p.id, bv, bi)) { bv = p.v; bi = p.id; }
+        int bi;
+        if (S == 0) {
+            // argmax given (from the fused lm_head kernel)
+            bi = argmax[row];
+            if (bi < 0 || bi >= V) { flag_status(status, GRAFT_STATUS_TOKEN_RANGE); bi = 0; }
+        } else {
+            float bv = -INFINITY;
+            bi = INT_MAX;
+            for (int s = 0; s < S; ++s) {
+                const ArgPart p = parts[row * S + s];
+                if (better(p.v, p.id, bv, bi)) { bv = p.v; bi = p.id; }
+            }
+            if (bi == INT_MAX) bi = 0;  // only NaNs in the row
+            argmax[row] = bi;
         }
-        if (bi == INT_MAX) bi = 0;  // only NaNs in the row
         g_s[i] = bi;
-        argmax[row] = bi;
         tok_s[i] = tree_tok[row];
         par_s[i] = tree_parent[row];
     }
@@ -229,14 +237,14 @@ extern "C" int graft_accept_compact(int B, int Kmax, int V, int n_layers, const 
         return GRAFT_ERR_INVALID_ARG;
     if (Kmax > GRAFT_MAX_KMAX) return GRAFT_ERR_UNSUPPORTED_SHAPE;
     if (B == 0) return GRAFT_OK;
-    if (target_logits == nullptr || tree_tok == nullptr || tree_parent == nullptr || tree_depth == nullptr ||
+    if (tree_tok == nullptr || tree_parent == nullptr || tree_depth == nullptr ||
         L == nullptr || argmax == nullptr || acc_len == nullptr || path == nullptr || out_tok == nullptr ||
         bonus == nullptr)
         return GRAFT_ERR_INVALID_ARG;
     if (n_layers > 0 && (Kc_layers == nullptr || Vc_layers == nullptr || Kt_layers == nullptr || Vt_layers == nullptr))
         return GRAFT_ERR_INVALID_ARG;
     const long long rows = (long long)B * Kmax;
-    const int S = arg_splits(V);
+    const int S = target_logits != nullptr ? arg_splits(V) : 0;  // 0: argmax is an input
     if (rows > 65535 || S > 65535 || B > 65535 || n_layers > 65535) return GRAFT_ERR_UNSUPPORTED_SHAPE;
     const long long row_bytes = (long long)Hkv * head_dim * 2;
     if (row_bytes > (1LL << 30)) return GRAFT_ERR_UNSUPPORTED_SHAPE;
@@ -246,10 +254,14 @@ extern "C" int graft_accept_compact(int B, int Kmax, int V, int n_layers, const 
     WsCarver c(ws);
     AcceptWs w = carve_accept(c, B, Kmax, V);
     cudaStream_t st = (cudaStream_t)stream;
-    launch_pdl(argmax_part_kernel, dim3(S, (unsigned)rows), dim3(kArgThreads), 0, st, target_logits, V, S, kChunk, w.parts);
-    launch_pdl(accept_kernel, dim3(B), dim3(GRAFT_MAX_KMAX), 0, st, Kmax, S, Lcap, w.parts, tree_tok, tree_parent, tree_depth, L, argmax,
-                                                 acc_len, path, out_tok, bonus, w, status);
-    count_launches(n_layers > 0 ? 3 : 2);
+    if (S > 0) {
+        launch_pdl(argmax_part_kernel, dim3(S, (unsigned)rows), dim3(kArgThreads), 0, st, target_logits, V, S, kChunk,
+                   w.parts);
+        count_launches(1);
+    }
+    launch_pdl(accept_kernel, dim3(B), dim3(GRAFT_MAX_KMAX), 0, st, Kmax, S, V, Lcap, w.parts, tree_tok, tree_parent,
+               tree_depth, L, argmax, acc_len, path, out_tok, bonus, w, status);
+    count_launches(n_layers > 0 ? 2 : 1);
     if (n_layers > 0)
         launch_pdl(compact_kernel, dim3(n_layers, B), dim3(256), 0, st, Kmax, Lcap, (int)row_bytes, Kc_layers, Vc_layers, Kt_layers,
                                                           Vt_layers, path, w);
