@@ -417,6 +417,27 @@ def run_graft(args):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         t_e2e = float(t.item())
 
+    # the fused lm_head argmax (greedy tokens straight from final hidden states) on this workload's rows
+    lmh = None
+    if args.secondary_reps > 0:
+        H, W_lm = synth.lm_head_inputs(wl, dev)
+        g_out = torch.empty(H.shape[0], dtype=torch.int32, device=dev)
+        m_out = torch.empty(H.shape[0], dtype=torch.float32, device=dev)
+        lws = torch.empty(max(1, gb.graft_lm_head_argmax_workspace_size(H.shape[0])), dtype=torch.uint8, device=dev)
+        lmh_graph = torch.cuda.CUDAGraph()
+        gb.graft_lm_head_argmax(H, W_lm, g_out, m_out, step.status, lws)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(lmh_graph):
+            gb.graft_lm_head_argmax(H, W_lm, g_out, m_out, step.status, lws)
+        for _ in range(3):
+            lmh_graph.replay()
+        t_lmh = timed(lmh_graph, args.secondary_reps) / args.secondary_reps
+        flops = 2.0 * H.shape[0] * wl.d_model * wl.V
+        nbytes = (H.numel() + W_lm.numel()) * 2 + H.shape[0] * 8
+        lmh = {"rows": H.shape[0], "d_model": wl.d_model, "vocab": wl.V, "us": t_lmh * 1e6,
+               "tflops": flops / t_lmh / 1e12, "gbs": nbytes / t_lmh / 1e9}
+        del H, W_lm
+
     bytes_call = attention_bytes_per_call(wl, L0.cpu())
     peak, peak_kind = measured_peaks()
     achieved = bytes_call / t_attn / 1e9
@@ -441,7 +462,8 @@ def run_graft(args):
         "clocks": clocks,
         "secondary": {"tree_attention_gbs": achieved, "tree_attention_frac_of_peak": achieved / peak,
                       "retrieval_fill_us": t_ret * 1e6, "build_tree_us": t_tree * 1e6,
-                      "launches_per_step": launches_per_step, "device_status": status},
+                      "launches_per_step": launches_per_step, "device_status": status,
+                      "lm_head_argmax": lmh},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inputs = (dl, tl, roots, L0, M_succ, M_cnt, layers[0])

@@ -250,12 +250,34 @@ int graft_lm_head_argmax(int N, int d_model, int V, const void* H, const void* W
  * new successors enter with their multiplicity; each touched row keeps its
  * top W by (count desc, token asc).  The result depends only on the
  * multiset, not on pair order, and is bit-exact.  Pairs with an id outside
- * [0, V) are skipped and flagged.  Workspace: graft_update_M_workspace_size.
+ * [0, V) are skipped and flagged; the pair (-1, -1) marks an empty slot and
+ * is skipped silently.  Workspace: graft_update_M_workspace_size.
+ * To seed M from a prompt's evidence, pass its bigrams: src = tokens,
+ * dst = tokens + 1, n = length - 1.
  */
 int graft_update_M_workspace_size(int64_t n, size_t* bytes);
 int graft_update_M(int32_t* M_succ, int32_t* M_cnt, int V, int W, const int32_t* src,
                    const int32_t* dst, int64_t n, int32_t* status, void* ws, size_t ws_bytes,
                    graft_stream_t stream);
+
+/*
+ * graft_update_M_emitted — refresh M from the bigrams of the tokens a verify
+ * step emitted (Graft article, method paragraph: retrieval draws on the
+ * evidence of the context itself; seeding M from the prompt's bigrams at
+ * prefill and adding each step's emitted bigrams keeps it current for long
+ * contexts).
+ *
+ *   tree_tok [B][Kmax] i32   the step's tree (node 0 = the last token
+ *                            emitted before the step)
+ *   out_tok [B][Kmax], acc_len [B] i32   graft_accept_compact's outputs
+ * Adds, as one multiset under graft_update_M's rule, the acc_len[b] pairs
+ * (tree_tok[b][0] -> out_tok[b][0]), (out_tok[b][t-1] -> out_tok[b][t]) for
+ * 0 < t < acc_len[b].  Workspace: graft_update_M_emitted_workspace_size.
+ */
+int graft_update_M_emitted_workspace_size(int B, int Kmax, size_t* bytes);
+int graft_update_M_emitted(int32_t* M_succ, int32_t* M_cnt, int V, int W, int B, int Kmax,
+                           const int32_t* tree_tok, const int32_t* out_tok, const int32_t* acc_len,
+                           int32_t* status, void* ws, size_t ws_bytes, graft_stream_t stream);
 
 /*
  * graft_update_M_noalloc — graft_update_M without a workspace argument.

@@ -16,6 +16,12 @@ M's layout and the update rule open; they are fixed here as:
 Reading for which pairs feed the update: every node i of every verified
 tree contributes (tree_tok[i], argmax_i), the target's greedy successor of
 that node's token in that context.
+
+Prompt-evidence policy (Graft article, method paragraph: retrieval uses the
+context's own evidence, which is what carries long contexts): M is seeded
+with the prompt's bigrams at prefill, and each step adds the bigrams of the
+tokens it emitted, starting from the last token emitted before the step
+(the tree's root); `emitted_pairs` forms them.
 """
 from __future__ import annotations
 
@@ -51,6 +57,18 @@ def update_M(succ: np.ndarray, cnt: np.ndarray, src: np.ndarray, dst: np.ndarray
             succ[s, j] = t
             cnt[s, j] = c
     return succ, cnt
+
+
+def emitted_pairs(tree_tok: np.ndarray, out_tok: np.ndarray, acc_len: np.ndarray):
+    """(src, dst) bigrams of each request's emitted tokens: root -> out[0] -> ... -> out[acc_len-1]."""
+    src, dst = [], []
+    for b in range(len(acc_len)):
+        prev = int(tree_tok[b][0])
+        for t in range(int(acc_len[b])):
+            src.append(prev)
+            dst.append(int(out_tok[b][t]))
+            prev = int(out_tok[b][t])
+    return np.array(src, dtype=np.int32), np.array(dst, dtype=np.int32)
 
 
 def empty_M(V: int, W: int):

@@ -157,3 +157,24 @@ def test_update_rejects_out_of_range():
     succ, cnt = um.empty_M(5, 2)
     with pytest.raises(ValueError):
         um.update_M(succ, cnt, np.array([5]), np.array([0]))
+
+
+def test_emitted_pairs_hand_example():
+    """Root 7 emits 3, 9 (path) and bonus 4: bigrams 7->3, 3->9, 9->4; a request that accepted only the
+    root emits its bonus: 5->6."""
+    from oracle import update_m as oupd
+    tree_tok = np.array([[7, 3, 9, 1], [5, 2, 2, 2]], np.int32)
+    out_tok = np.array([[3, 9, 4, -1], [6, -1, -1, -1]], np.int32)
+    src, dst = oupd.emitted_pairs(tree_tok, out_tok, np.array([3, 1], np.int32))
+    assert list(zip(src.tolist(), dst.tolist())) == [(7, 3), (3, 9), (9, 4), (5, 6)]
+
+
+def test_prompt_seeding_counts_bigrams():
+    """Seeding from a token stream counts each bigram: the stream 1 2 1 2 1 3 gives row 1 = {2: 2, 3: 1}
+    and row 2 = {1: 2} (closed form by counting)."""
+    from oracle import update_m as oupd
+    succ, cnt = oupd.empty_M(4, 2)
+    toks = np.array([1, 2, 1, 2, 1, 3], np.int32)
+    succ, cnt = oupd.update_M(succ, cnt, toks[:-1], toks[1:])
+    assert succ[1].tolist() == [2, 3] and cnt[1].tolist() == [2, 1]
+    assert succ[2].tolist() == [1, -1] and cnt[2].tolist() == [2, 0]

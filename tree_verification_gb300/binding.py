@@ -79,6 +79,8 @@ _SIGNATURES = {
     "graft_update_M_workspace_size": [_I64, ctypes.POINTER(_SZ)],
     "graft_update_M": [_P, _P, _I, _I, _P, _P, _I64, _P, _P, _SZ, _P],
     "graft_update_M_noalloc": [_P, _P, _I, _I, _P, _P, _I64, _P, _P],
+    "graft_update_M_emitted_workspace_size": [_I, _I, ctypes.POINTER(_SZ)],
+    "graft_update_M_emitted": [_P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P],
     "graft_status_string": [_I],
     "graft_version": [],
     "graft_launch_count": [],
@@ -352,3 +354,33 @@ def graft_version() -> int:
 
 def graft_launch_count() -> int:
     return int(lib().graft_launch_count())
+
+
+def graft_update_M_emitted_workspace_size(B: int, Kmax: int) -> int:
+    n = _SZ()
+    _check(lib().graft_update_M_emitted_workspace_size(B, Kmax, ctypes.byref(n)), "workspace size")
+    return n.value
+
+
+def graft_update_M_emitted(M_succ, M_cnt, tree_tok, out_tok, acc_len, status=None, ws=None, stream=None):
+    """Add the bigrams of the tokens a step emitted (root -> out_tok[0] -> ... -> out_tok[acc_len-1])."""
+    V, W = M_succ.shape
+    _need(M_succ, "M_succ", torch.int32)
+    _need(M_cnt, "M_cnt", torch.int32, (V, W))
+    B, Kmax = tree_tok.shape
+    _need(tree_tok, "tree_tok", torch.int32, (B, Kmax))
+    _need(out_tok, "out_tok", torch.int32, (B, Kmax))
+    _need(acc_len, "acc_len", torch.int32, (B,))
+    ws, nws = _ws(graft_update_M_emitted_workspace_size(B, Kmax), M_succ.device, ws)
+    _check(lib().graft_update_M_emitted(_ptr(M_succ), _ptr(M_cnt), V, W, B, Kmax, _ptr(tree_tok), _ptr(out_tok),
+                                        _ptr(acc_len), _ptr(status), _ptr(ws), nws, _stream(stream)),
+           "graft_update_M_emitted")
+
+
+def graft_seed_M_from_tokens(M_succ, M_cnt, tokens, status=None, ws=None, stream=None):
+    """Seed M with a prompt's bigrams (tokens[i] -> tokens[i+1]) in one order-independent update."""
+    _need(tokens, "tokens", torch.int32)
+    if tokens.numel() < 2:
+        return
+    t = tokens.reshape(-1)
+    graft_update_M(M_succ, M_cnt, t[:-1], t[1:], status=status, ws=ws, stream=stream)

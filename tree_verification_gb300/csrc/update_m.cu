@@ -72,6 +72,7 @@ __global__ void pairs_kernel(int32_t* __restrict__ succ, int32_t* __restrict__ c
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const int s = src[i], t = dst[i];
+    if (s == -1 && t == -1) return;  // no pair in this slot
     if (s < 0 || s >= V || t < 0 || t >= V) {
         flag_status(status, GRAFT_STATUS_TOKEN_RANGE);
         return;
@@ -163,6 +164,27 @@ __global__ void rerank_kernel(int32_t* __restrict__ succ, int32_t* __restrict__ 
         const int tok = (int)(uint32_t)(key & 0xffffffffull);
         rs[lane] = tok;
         rc[lane] = c;
+    }
+}
+
+// The bigrams of the tokens a verify step emitted, one slot per tree node:
+// slot t < acc_len[b] holds (previous token -> out_tok[b][t]), where the token
+// before out_tok[b][0] is the tree's root (the last token emitted before the
+// step); the remaining slots hold the (-1, -1) no-pair marker.
+__global__ void emitted_pairs_kernel(int B, int Kmax, const int32_t* __restrict__ tree_tok,
+                                     const int32_t* __restrict__ out_tok, const int32_t* __restrict__ acc_len,
+                                     int32_t* __restrict__ src, int32_t* __restrict__ dst) {
+    griddep_enter();
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= B * Kmax) return;
+    const int b = i / Kmax, t = i % Kmax;
+    const int n = acc_len[b];
+    if (t < n && n <= Kmax) {
+        src[i] = t == 0 ? tree_tok[(size_t)b * Kmax] : out_tok[i - 1];
+        dst[i] = out_tok[i];
+    } else {
+        src[i] = -1;
+        dst[i] = -1;
     }
 }
 
@@ -281,5 +303,49 @@ extern "C" int graft_update_M_noalloc(int32_t* M_succ, int32_t* M_cnt, int V, in
     launch_pdl(pairs_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, M_succ, M_cnt, V, W, src, dst, n, w, status);
     launch_pdl(rerank_kernel, dim3((unsigned)((n + 7) / 8)), dim3(256), 0, st, M_succ, M_cnt, W, w);
     count_launches(3);
+    return launch_status();
+}
+
+// ----------------------------------------------------------------------------
+// graft_update_M_emitted: prompt-evidence refresh from a step's emitted tokens
+// ----------------------------------------------------------------------------
+extern "C" int graft_update_M_emitted_workspace_size(int B, int Kmax, size_t* bytes) {
+    if (bytes == nullptr || B < 0 || Kmax < 1) return GRAFT_ERR_INVALID_ARG;
+    const int64_t n = (int64_t)B * Kmax;
+    if (n > (1LL << 28)) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    WsCarver c(nullptr);
+    c.take<int32_t>(n);
+    c.take<int32_t>(n);
+    carve_update(c, n);
+    *bytes = c.bytes();
+    return GRAFT_OK;
+}
+
+extern "C" int graft_update_M_emitted(int32_t* M_succ, int32_t* M_cnt, int V, int W, int B, int Kmax,
+                                      const int32_t* tree_tok, const int32_t* out_tok, const int32_t* acc_len,
+                                      int32_t* status, void* ws, size_t ws_bytes, graft_stream_t stream) {
+    if (V < 1 || W < 1 || B < 0 || Kmax < 1) return GRAFT_ERR_INVALID_ARG;
+    if (W > GRAFT_MAX_W || Kmax > GRAFT_MAX_KMAX) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    if (B == 0) return GRAFT_OK;
+    if (M_succ == nullptr || M_cnt == nullptr || tree_tok == nullptr || out_tok == nullptr || acc_len == nullptr)
+        return GRAFT_ERR_INVALID_ARG;
+    const int64_t n = (int64_t)B * Kmax;
+    if (n > (1LL << 28)) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    size_t need = 0;
+    graft_update_M_emitted_workspace_size(B, Kmax, &need);
+    if (!ws_ok(ws, ws_bytes, need)) return GRAFT_ERR_WORKSPACE;
+    WsCarver c(ws);
+    int32_t* src = c.take<int32_t>(n);
+    int32_t* dst = c.take<int32_t>(n);
+    UpdWs w = carve_update(c, n);
+    cudaStream_t st = (cudaStream_t)stream;
+    const int cb = (int)((w.cap + 255) / 256);
+    launch_pdl(emitted_pairs_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, B, Kmax, tree_tok, out_tok,
+               acc_len, src, dst);
+    launch_pdl(clear_kernel, dim3(cb < 1024 ? cb : 1024), dim3(256), 0, st, w);
+    launch_pdl(pairs_kernel, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, st, M_succ, M_cnt, V, W, src, dst, n,
+               w, status);
+    launch_pdl(rerank_kernel, dim3((unsigned)((n + 7) / 8)), dim3(256), 0, st, M_succ, M_cnt, W, w);
+    count_launches(4);
     return launch_status();
 }

@@ -4,8 +4,12 @@
 and runs them in the Graft article's order on one CUDA stream:
 
     graft_build_tree  ->  graft_tree_attention x n_layers  ->
-    graft_accept_compact  ->  graft_update_M (pairs = every tree node's
-    (token, target argmax))
+    graft_accept_compact  ->  M update
+
+The M update follows ``m_policy``: "tree" adds every tree node's (token,
+target argmax) pair (graft_update_M); "emitted" adds the bigrams of the
+tokens the step emitted (graft_update_M_emitted), the prompt-evidence policy
+that ``prefill_M`` seeds with the prompt's bigrams; "both" does both.
 
 Because every buffer is fixed, a whole step can be captured once in a CUDA
 graph and replayed, which removes the per-layer host launch cost.  The
@@ -25,7 +29,10 @@ from . import binding as gb
 class VerifyStep:
     def __init__(self, cfg: gb.GraftConfig, B: int, Hq: int, Hkv: int, n_layers: int, Lcap: int, device,
                  Kc: Sequence[torch.Tensor], Vc: Sequence[torch.Tensor], Kt: Sequence[torch.Tensor],
-                 Vt: Sequence[torch.Tensor]):
+                 Vt: Sequence[torch.Tensor], m_policy: str = "tree"):
+        if m_policy not in ("tree", "emitted", "both"):
+            raise ValueError("m_policy must be 'tree', 'emitted' or 'both'")
+        self.m_policy = m_policy
         self.cfg, self.B, self.Hq, self.Hkv, self.n_layers, self.Lcap = cfg, B, Hq, Hkv, n_layers, Lcap
         self.device = torch.device(device)
         K, dev = cfg.Kmax, self.device
@@ -42,6 +49,7 @@ class VerifyStep:
         self.ws_attn = torch.empty(max(1, gb.graft_tree_attention_workspace_size(B, Hq, Hkv, K, Lcap)), **u8)
         self.ws_acc = torch.empty(max(1, gb.graft_accept_compact_workspace_size(B, K, cfg.V)), **u8)
         self.ws_upd = torch.empty(max(1, gb.graft_update_M_workspace_size(B * K)), **u8)
+        self.ws_emit = torch.empty(max(1, gb.graft_update_M_emitted_workspace_size(B, K)), **u8)
         self.O = torch.empty(B, K, Hq, gb.HEAD_DIM, dtype=torch.bfloat16, device=dev)
         self.Kc, self.Vc, self.Kt, self.Vt = list(Kc), list(Vc), list(Kt), list(Vt)
         self.Kc_ptrs = gb.layer_pointers(self.Kc, dev)
@@ -62,8 +70,16 @@ class VerifyStep:
         gb.graft_accept_compact(target_logits, self.tree["tok"], self.tree["parent"], self.tree["depth"],
                                 self.Kc_ptrs, self.Vc_ptrs, self.Kt_ptrs, self.Vt_ptrs, self.n_layers, self.Hkv,
                                 self.Lcap, L, out=self.acc, status=self.status, ws=self.ws_acc)
-        gb.graft_update_M(M_succ, M_cnt, self.tree["tok"].view(-1), self.acc["argmax"].view(-1),
-                          status=self.status, ws=self.ws_upd)
+        if self.m_policy in ("tree", "both"):
+            gb.graft_update_M(M_succ, M_cnt, self.tree["tok"].view(-1), self.acc["argmax"].view(-1),
+                              status=self.status, ws=self.ws_upd)
+        if self.m_policy in ("emitted", "both"):
+            gb.graft_update_M_emitted(M_succ, M_cnt, self.tree["tok"], self.acc["out_tok"], self.acc["acc_len"],
+                                      status=self.status, ws=self.ws_emit)
+
+    def prefill_M(self, M_succ, M_cnt, prompt_tokens) -> None:
+        """Seed M with the prompt's bigrams (the prompt-evidence policy's starting table)."""
+        gb.graft_seed_M_from_tokens(M_succ, M_cnt, prompt_tokens, status=self.status)
 
     def capture(self, *args, **kw) -> torch.cuda.CUDAGraph:
         """Capture run(*args) into a CUDA graph (the arguments' storage is baked in)."""

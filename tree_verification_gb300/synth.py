@@ -56,6 +56,7 @@ class Workload:
     checkpoints: Tuple[int, ...] = (0, 1, 5)
     head_dim: int = 128
     seed: int = 0
+    d_model: int = 4096         # hidden size of the target's final layer (lm_head input)
 
     @property
     def group(self) -> int:
@@ -76,7 +77,7 @@ class Workload:
 
 WORKLOADS = {
     "tiny": Workload("tiny", B=1, Hq=8, Hkv=2, n_layers=1, L=(512, 512), Kmax=32, D=6, k=4, V=32000, W=8,
-                     plant=(5, 5), M_init="zipf"),
+                     plant=(5, 5), M_init="zipf", d_model=256),
     "llama3_8b": Workload("llama3_8b", B=1, Hq=32, Hkv=8, n_layers=32, L=(4096, 4096), Kmax=64, D=8, k=8,
                           V=128256, W=16, plant=(5, 5), M_init="empty"),
     "qwen3_8b_batch": Workload("qwen3_8b_batch", B=64, Hq=32, Hkv=8, n_layers=36, L=(512, 4096), Kmax=64, D=8,
@@ -233,3 +234,11 @@ def plant_paths(logits: torch.Tensor, tok, parent, depth, lengths: Sequence[int]
                 t += 1
             row[t] = row.max() + 1.0
     return ends
+
+
+def lm_head_inputs(wl: Workload, device, seed_offset: int = 71):
+    """Synthetic final hidden states [B*Kmax][d_model] and output embedding [V][d_model], bf16 N(0,1)."""
+    g = torch.Generator(device="cpu").manual_seed(wl.seed + seed_offset)
+    H = torch.randn(wl.B * wl.Kmax, wl.d_model, generator=g).to(torch.bfloat16).to(device)
+    W = torch.randn(wl.V, wl.d_model, generator=g).to(torch.bfloat16).to(device)
+    return H, W
