@@ -144,6 +144,32 @@ int graft_build_tree(const GraftConfig* cfg, int B, const float* draft_logits,
                      int32_t* status, void* ws, size_t ws_bytes, graft_stream_t stream);
 
 /*
+ * graft_build_tree_block — graft_build_tree for a block drafter (Graft
+ * abstract and results paragraph: grafting applied to DFlash-style block
+ * drafting).  A block drafter emits one distribution per depth in a single
+ * pass, not one per frontier node, so
+ *
+ *   block_logits [B][D][V] f32   row (b, d) is the drafter's distribution at
+ *                                depth d + 1, shared by every frontier node
+ *                                of drafter call d
+ *
+ * and the tree is assembled exactly as graft_build_tree would from drafter
+ * logits whose k slot rows of each depth all equal that row: per-position
+ * top-k, cumulative scores, pruning at the checkpoints and the retrieval
+ * graft.  Same outputs, workspace and errors as graft_build_tree.
+ *
+ * Ablations of the method need no entry point of their own: without
+ * pruning, set every tau to 0 (the confidence never drops below it, so the
+ * dense tree of stage n_checkpoints is built); without retrieval, pass an
+ * all-empty M (every retrieved slot becomes a pad: token 0 under the root).
+ */
+int graft_build_tree_block(const GraftConfig* cfg, int B, const float* block_logits,
+                           const int32_t* root_tok, const int32_t* M_succ, const int32_t* L,
+                           int32_t* tree_tok, int32_t* tree_parent, int32_t* tree_depth,
+                           int32_t* tree_pos, uint64_t* tree_mask, int32_t* stage,
+                           int32_t* status, void* ws, size_t ws_bytes, graft_stream_t stream);
+
+/*
  * graft_retrieve — the retrieval fill alone (Graft article, step summary:
  * retrieval starts from the root token through the GPU-resident adjacency
  * matrix; method paragraph, second point).

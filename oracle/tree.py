@@ -209,14 +209,24 @@ def merge(root_tok: int, draft_nodes: List[Cand], ret_tok: Sequence[int],
     return Tree(tok=tok, parent=parent, depth=depth, pos=pos, mask=mask, stage=stage, n_draft=n_draft)
 
 
-def build_tree(draft_logits_b: np.ndarray, root_tok: int, M_succ: np.ndarray, L: int, cfg: dict):
+def build_tree(draft_logits_b: np.ndarray, root_tok: int, M_succ: np.ndarray, L: int, cfg: dict,
+               block: bool = False):
     """Stages 1-3 for one request from slot-indexed drafter logits.
 
     ``draft_logits_b[d][f]`` is the drafter's logit row for the f-th frontier
     node of call d (call 0 uses slot 0, the root).  Returns (tree, draft
     result, retrieved tokens of the whole envelope).
+
+    ``block=True`` reads a block drafter's output instead (Graft abstract and
+    results paragraph: grafting applied to DFlash-style block drafting):
+    ``draft_logits_b[d]`` is the one distribution the drafter gives for depth
+    d + 1, which every frontier node of call d expands with the same top-k,
+    cumulative scores, pruning and graft.
     """
-    res = draft_tree(lambda d, f, _path: draft_logits_b[d, f], root_tok, cfg)
+    if block:
+        res = draft_tree(lambda d, f, _path: draft_logits_b[d], root_tok, cfg)
+    else:
+        res = draft_tree(lambda d, f, _path: draft_logits_b[d, f], root_tok, cfg)
     nodes = retained_draft(res, cfg)
     ret = retrieve(root_tok, M_succ, cfg["tmpl_parent"], cfg["tmpl_rank"])
     tree = merge(root_tok, nodes, ret, cfg["tmpl_parent"], res.stage, L, cfg)
@@ -224,7 +234,7 @@ def build_tree(draft_logits_b: np.ndarray, root_tok: int, M_succ: np.ndarray, L:
 
 
 def build_tree_batch(draft_logits: np.ndarray, root_tok: np.ndarray, M_succ: np.ndarray,
-                     L: np.ndarray, cfg: dict) -> dict:
+                     L: np.ndarray, cfg: dict, block: bool = False) -> dict:
     """build_tree over a batch; returns dense [B][Kmax] arrays like the library's outputs."""
     B = draft_logits.shape[0]
     Kmax = cfg["Kmax"]
@@ -234,7 +244,7 @@ def build_tree_batch(draft_logits: np.ndarray, root_tok: np.ndarray, M_succ: np.
                ret=np.full((B, len(cfg["tmpl_parent"])), -1, np.int32))
     results = []
     for b in range(B):
-        tree, res, ret = build_tree(draft_logits[b], int(root_tok[b]), M_succ, int(L[b]), cfg)
+        tree, res, ret = build_tree(draft_logits[b], int(root_tok[b]), M_succ, int(L[b]), cfg, block=block)
         out["tok"][b] = tree.tok
         out["parent"][b] = tree.parent
         out["depth"][b] = tree.depth

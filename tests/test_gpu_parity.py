@@ -439,3 +439,52 @@ def test_update_M_long_context_warmup():
     s, c = _warm_M_oracle(wl)
     assert np.array_equal(to_np(s_d), s) and np.array_equal(to_np(c_d), c)
     assert int(c.sum()) == 5 * (wl.Lmax - 1)
+
+
+@pytest.mark.parametrize("V,seed", [(4096, 4), (128256, 5)])
+def test_build_tree_block_draft_parity(V, seed):
+    """graft_build_tree_block (one drafter row per depth, shared by the frontier) against the oracle."""
+    wl = _peaked_wl(V, 12, seed)
+    boosts = [0.0, 10.0, 13.0, 14.0, 15.0, 16.0, 17.0, 18.0, 20.0, 22.0, 25.0, 30.0]
+    if V == 4096:
+        boosts = [b - math.log(128256 / 4096) for b in boosts]
+    cfg, cfg_o = lib_cfg(wl), oracle_cfg(wl)
+    block = synth.peaked_draft_logits(wl, DEV, boosts, seed)[:, :, 0, :].contiguous()
+    roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
+    s_np, _ = synth.zipf_M(wl.V, wl.W, seed)
+    status = _status()
+    gpu = gb().graft_build_tree(cfg, block, roots.to(DEV), torch.from_numpy(s_np).to(DEV), L.to(DEV), status=status,
+                                block=True)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    trees, margins = [], []
+    for b in range(wl.B):
+        rows = block[b].cpu().numpy()
+        row_fn = lambda d, f, _p, rows=rows: rows[d]
+        res = otree.draft_tree(row_fn, int(roots[b]), cfg_o)
+        ret = otree.retrieve(int(roots[b]), s_np, cfg_o["tmpl_parent"], cfg_o["tmpl_rank"])
+        trees.append(otree.merge(int(roots[b]), otree.retained_draft(res, cfg_o), ret, cfg_o["tmpl_parent"],
+                                 res.stage, int(L[b]), cfg_o))
+        margins.append(otree.draft_margins(row_fn, int(roots[b]), cfg_o))
+    ok = [b for b in range(wl.B) if margins[b] > MARGIN]
+    assert len(ok) >= wl.B - 2, f"too many near-tie requests: {margins}"
+    _compare_tree({k: v[ok] for k, v in gpu.items()}, [trees[b] for b in ok])
+
+
+def test_ablation_without_retrieval_pads_the_graft():
+    """The no-retrieval ablation (an all-empty M): pruned trees keep their draft nodes and every grafted
+    slot is a pad (token 0, in the template's shape), as the oracle builds it."""
+    wl = _peaked_wl(4096, 12, 6)
+    boosts = [b - math.log(128256 / 4096) for b in [0.0, 10.0, 13.0, 14.0, 15.0, 16.0, 17.0, 18.0, 20.0, 22.0, 25.0,
+                                                    30.0]]
+    cfg, cfg_o = lib_cfg(wl), oracle_cfg(wl)
+    dl = synth.peaked_draft_logits(wl, DEV, boosts, 6)
+    roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
+    s_np, _ = synth.empty_M(wl.V, wl.W)
+    gpu = _build(wl, cfg, dl, roots, torch.from_numpy(s_np).to(DEV), L)
+    trees, margins = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
+    ok = [b for b in range(wl.B) if margins[b] > MARGIN]
+    _compare_tree({k: v[ok] for k, v in gpu.items()}, [trees[b] for b in ok])
+    tok = to_np(gpu["tok"])
+    for b in ok:
+        assert (tok[b, trees[b].n_draft:] == 0).all()

@@ -201,3 +201,31 @@ def test_retrieve_empty_M_all_pads():
     assert res.stage == 0 and len(t.tok) == 16
     # pads are token 0 and the tree still has Kmax nodes
     assert t.tok[t.n_draft:] == [0] * (16 - t.n_draft)
+
+
+def test_block_draft_k1_is_the_top1_chain():
+    """A block drafter with k = 1: the draft is the chain of each position's top token, and the
+    confidence after call d is the product of those tokens' probabilities (closed form)."""
+    V, D = 6, 3
+    rows = np.array([[0.0, 3.0, 1.0, 0.0, 0.0, 0.0],
+                     [2.0, 0.0, 0.0, 0.0, 4.0, 0.0],
+                     [0.0, 0.0, 0.0, 5.0, 0.0, 1.0]])
+    cfg = config.make_config(Kmax=4, D=D, k=1, V=V, W=2, checkpoints=[0, 1], tau=0.0)
+    succ = np.full((V, 2), -1, np.int32)
+    t, res, _ = tr.build_tree(rows, 2, succ, 10, cfg, block=True)
+    assert t.tok == [2, 1, 4, 3] and t.parent == [-1, 0, 1, 2] and t.depth == [0, 1, 2, 3]
+    p = np.exp(rows - logsumexp(rows, axis=1, keepdims=True))
+    want = np.cumprod([p[0, 1], p[1, 4], p[2, 3]])
+    assert np.allclose([float(c) for c in res.conf], want, rtol=1e-6)
+
+
+def test_block_draft_children_come_from_the_shared_row():
+    """With a block drafter every frontier node of call d expands the same top-k of row d."""
+    rng = np.random.default_rng(3)
+    V, D, k = 40, 4, 3
+    rows = rng.normal(0, 2, (D, V))
+    cfg = config.make_config(Kmax=12, D=D, k=k, V=V, W=2, checkpoints=[], tau=0.3)
+    res = tr.draft_tree(lambda d, f, _p: rows[d], 0, cfg)
+    top = [set(np.argsort(-rows[d], kind="stable")[:k].tolist()) for d in range(D)]
+    for c in res.pool:
+        assert int(c.token) in top[c.depth - 1]

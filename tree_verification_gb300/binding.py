@@ -67,6 +67,8 @@ _SIGNATURES = {
     "graft_config_validate": [ctypes.POINTER(GraftConfig)],
     "graft_build_tree_workspace_size": [ctypes.POINTER(GraftConfig), _I, ctypes.POINTER(_SZ)],
     "graft_build_tree": [ctypes.POINTER(GraftConfig), _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
+    "graft_build_tree_block": [ctypes.POINTER(GraftConfig), _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
+                               _P],
     "graft_retrieve": [ctypes.POINTER(GraftConfig), _I, _P, _P, _P, _P, _P],
     "graft_tree_attention_workspace_size": [_I, _I, _I, _I, _I, _I64, ctypes.POINTER(_SZ)],
     "graft_tree_attention": [_I, _I, _I, _I, _I, _P, _P, _P, _I64, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P,
@@ -173,9 +175,10 @@ def graft_build_tree_workspace_size(cfg: GraftConfig, B: int) -> int:
 
 
 def graft_build_tree(cfg: GraftConfig, draft_logits, root_tok, M_succ, L, out: Optional[dict] = None,
-                     status=None, ws=None, stream=None) -> dict:
+                     status=None, ws=None, stream=None, block: bool = False) -> dict:
+    """Drafter logits [B][D][k][V]; with block=True, block-drafter logits [B][D][V] (graft_build_tree_block)."""
     B = root_tok.shape[0]
-    _need(draft_logits, "draft_logits", torch.float32, (B, cfg.D, cfg.k, cfg.V))
+    _need(draft_logits, "draft_logits", torch.float32, (B, cfg.D, cfg.V) if block else (B, cfg.D, cfg.k, cfg.V))
     _need(root_tok, "root_tok", torch.int32, (B,))
     _need(M_succ, "M_succ", torch.int32, (cfg.V, cfg.W))
     _need(L, "L", torch.int32, (B,))
@@ -189,10 +192,11 @@ def graft_build_tree(cfg: GraftConfig, draft_logits, root_tok, M_succ, L, out: O
                    mask=torch.empty(B, K, dtype=torch.int64, device=dev),
                    stage=torch.empty(B, dtype=torch.int32, device=dev))
     ws, nws = _ws(graft_build_tree_workspace_size(cfg, B), dev, ws)
-    _check(lib().graft_build_tree(ctypes.byref(cfg), B, _ptr(draft_logits), _ptr(root_tok), _ptr(M_succ), _ptr(L),
-                                  _ptr(out["tok"]), _ptr(out["parent"]), _ptr(out["depth"]), _ptr(out["pos"]),
-                                  _ptr(out["mask"]), _ptr(out["stage"]), _ptr(status), _ptr(ws), nws,
-                                  _stream(stream)), "graft_build_tree")
+    fn = lib().graft_build_tree_block if block else lib().graft_build_tree
+    _check(fn(ctypes.byref(cfg), B, _ptr(draft_logits), _ptr(root_tok), _ptr(M_succ), _ptr(L),
+              _ptr(out["tok"]), _ptr(out["parent"]), _ptr(out["depth"]), _ptr(out["pos"]),
+              _ptr(out["mask"]), _ptr(out["stage"]), _ptr(status), _ptr(ws), nws,
+              _stream(stream)), "graft_build_tree")
     return out
 
 

@@ -105,7 +105,7 @@ __device__ __forceinline__ void warp_topk(TopK<KT>& tk, float* out_v, int* out_i
 template <int KT>
 __global__ void __launch_bounds__(kRowThreads)
 draft_rows_kernel(const float* __restrict__ logits, int D, int k, int V, int d_lo, int S,
-                  int chunk, const int32_t* __restrict__ state, RowPart* __restrict__ parts) {
+                  int chunk, const int32_t* __restrict__ state, RowPart* __restrict__ parts, int block) {
     griddep_enter();
     const int s = blockIdx.x;
     const int r = blockIdx.y;
@@ -115,8 +115,11 @@ draft_rows_kernel(const float* __restrict__ logits, int D, int k, int V, int d_l
     if (d >= D || (d == 0 && f != 0)) return;
     if (state != nullptr && state[b] != -1) return;  // pruned at an earlier checkpoint
 
+    // the split's result goes to slot (b, d, f); block drafts read one row per depth, shared by
+    // every frontier node of that depth
     const size_t row_id = ((size_t)b * D + d) * k + f;
-    const float* row = logits + row_id * (size_t)V;
+    const size_t in_row = block ? (size_t)b * D + d : row_id;
+    const float* row = logits + in_row * (size_t)V;
     const int lo = s * chunk;
     const int hi = min(V, lo + chunk);
 
@@ -268,11 +271,16 @@ draft_select_kernel(SelectParams p, int d_lo, int d_hi, BuildWs w) {
         for (int c = tid; c < nc; c += kSelThreads) {
             const int f = c / k, r = c % k;
             const float ps = (d == 0) ? 0.f : front_score[f];
-            const float sc = __fadd_rn(ps, __fsub_rn(top_v[f][r], lse_s[f]));
+            float sc = __fadd_rn(ps, __fsub_rn(top_v[f][r], lse_s[f]));
+            // a non-finite row (NaN, or fewer than k finite logits) yields the lowest score and a
+            // pad token, so every ranking below stays a strict total order
+            int tok = top_id[f][r];
+            if (!(sc == sc) || tok == INT_MAX) sc = -INFINITY;
+            if (tok == INT_MAX) tok = 0;
             cand_score[c] = sc;
             const size_t o = ((size_t)b * D + d) * KK + c;
             w.pool_score[o] = sc;
-            w.pool_tok[o] = top_id[f][r];
+            w.pool_tok[o] = tok;
             w.pool_par[o] = (d == 0) ? -1 : front_idx[f];
         }
         __syncthreads();
@@ -345,6 +353,8 @@ draft_merge_kernel(MergeParams p, const int32_t* __restrict__ root_tok, const in
     __syncthreads();
     // keep the K_draft_s - 1 best entries by (score desc, depth asc, index asc):
     // entries are stored in (depth, index) order, so the tie-break is entry order
+    for (int q = tid; q < GRAFT_MAX_KMAX; q += kMergeThreads) kept_entry[q] = -1;
+    __syncthreads();
     for (int e = tid; e < P; e += kMergeThreads) {
         const float sc = sm_pool[e];
         int rank = 0;
@@ -355,6 +365,17 @@ draft_merge_kernel(MergeParams p, const int32_t* __restrict__ root_tok, const in
         if (rank < keep) kept_entry[rank] = e;
     }
     __syncthreads();
+    // scores are never NaN here, so the ranks are a permutation; a hole would mean a broken input
+    if (tid < keep && (kept_entry[tid] < 0 || kept_entry[tid] >= P)) {
+        flag_status(status, GRAFT_STATUS_TREE);
+        kept_entry[tid] = 0;
+    }
+    __syncthreads();
+    // every slot starts as a pad under the root, so the ancestor walk below ends even on a broken input
+    if (tid < GRAFT_MAX_KMAX) {
+        s_tok[tid] = 0;
+        s_par[tid] = tid == 0 ? -1 : 0;
+    }
     // tree order among the kept: (depth asc, score desc, index asc)
     if (tid < keep) {
         const int e = kept_entry[tid];
@@ -382,7 +403,8 @@ draft_merge_kernel(MergeParams p, const int32_t* __restrict__ root_tok, const in
             parent = -1;
             for (int q = 0; q < keep; ++q)
                 if (kept_entry[q] == pe) parent = node_of_kept[q];
-            if (parent < 0) { flag_status(status, GRAFT_STATUS_TREE); parent = 0; }
+            // a parent precedes its child, which also keeps the ancestor walk below finite
+            if (parent < 0 || parent >= node) { flag_status(status, GRAFT_STATUS_TREE); parent = 0; }
         }
         s_par[node] = parent;
     }
@@ -478,9 +500,10 @@ TmplParams make_tmpl(const GraftConfig* cfg) {
 
 template <int KT>
 void launch_rows(const float* logits, const GraftConfig* cfg, int B, int d_lo, int d_hi, int S, int chunk,
-                 const int32_t* state, RowPart* parts, cudaStream_t st) {
+                 const int32_t* state, RowPart* parts, cudaStream_t st, int block) {
     dim3 grid(S, (d_hi - d_lo + 1) * cfg->k, B);
-    launch_pdl(draft_rows_kernel<KT>, dim3(grid), dim3(kRowThreads), 0, st, logits, cfg->D, cfg->k, cfg->V, d_lo, S, chunk, state, parts);
+    launch_pdl(draft_rows_kernel<KT>, dim3(grid), dim3(kRowThreads), 0, st, logits, cfg->D, cfg->k, cfg->V, d_lo, S,
+               chunk, state, parts, block);
     count_launches(1);
 }
 
@@ -513,11 +536,12 @@ extern "C" int graft_retrieve(const GraftConfig* cfg, int B, const int32_t* root
     return launch_status();
 }
 
-extern "C" int graft_build_tree(const GraftConfig* cfg, int B, const float* draft_logits,
-                                const int32_t* root_tok, const int32_t* M_succ, const int32_t* L,
-                                int32_t* tree_tok, int32_t* tree_parent, int32_t* tree_depth,
-                                int32_t* tree_pos, uint64_t* tree_mask, int32_t* stage,
-                                int32_t* status, void* ws, size_t ws_bytes, graft_stream_t stream) {
+namespace {
+
+int build_tree_impl(const GraftConfig* cfg, int B, const float* draft_logits, int block, const int32_t* root_tok,
+                    const int32_t* M_succ, const int32_t* L, int32_t* tree_tok, int32_t* tree_parent,
+                    int32_t* tree_depth, int32_t* tree_pos, uint64_t* tree_mask, int32_t* stage, int32_t* status,
+                    void* ws, size_t ws_bytes, graft_stream_t stream) {
     const int rc = graft_config_validate(cfg);
     if (rc != GRAFT_OK) return rc;
     if (B < 0) return GRAFT_ERR_INVALID_ARG;
@@ -560,9 +584,9 @@ extern "C" int graft_build_tree(const GraftConfig* cfg, int B, const float* draf
     for (int g = 0; g <= cfg->n_checkpoints && d_lo < cfg->D; ++g) {
         const int d_hi = (g < cfg->n_checkpoints) ? cfg->checkpoint[g] : cfg->D - 1;
         const int32_t* gate = (d_lo == 0) ? nullptr : w.state;
-        if (cfg->k <= 4) launch_rows<4>(draft_logits, cfg, B, d_lo, d_hi, S, chunk, gate, w.parts, st);
-        else if (cfg->k <= 8) launch_rows<8>(draft_logits, cfg, B, d_lo, d_hi, S, chunk, gate, w.parts, st);
-        else launch_rows<16>(draft_logits, cfg, B, d_lo, d_hi, S, chunk, gate, w.parts, st);
+        if (cfg->k <= 4) launch_rows<4>(draft_logits, cfg, B, d_lo, d_hi, S, chunk, gate, w.parts, st, block);
+        else if (cfg->k <= 8) launch_rows<8>(draft_logits, cfg, B, d_lo, d_hi, S, chunk, gate, w.parts, st, block);
+        else launch_rows<16>(draft_logits, cfg, B, d_lo, d_hi, S, chunk, gate, w.parts, st, block);
         launch_pdl(draft_select_kernel, dim3(B), dim3(kSelThreads), 0, st, sp, d_lo, d_hi, w);
         count_launches(1);
         d_lo = d_hi + 1;
@@ -586,4 +610,24 @@ extern "C" int graft_build_tree(const GraftConfig* cfg, int B, const float* draf
                                                       tree_pos, tree_mask, stage, status);
     count_launches(1);
     return launch_status();
+}
+
+}  // namespace
+
+extern "C" int graft_build_tree(const GraftConfig* cfg, int B, const float* draft_logits,
+                                const int32_t* root_tok, const int32_t* M_succ, const int32_t* L,
+                                int32_t* tree_tok, int32_t* tree_parent, int32_t* tree_depth,
+                                int32_t* tree_pos, uint64_t* tree_mask, int32_t* stage,
+                                int32_t* status, void* ws, size_t ws_bytes, graft_stream_t stream) {
+    return build_tree_impl(cfg, B, draft_logits, 0, root_tok, M_succ, L, tree_tok, tree_parent, tree_depth, tree_pos,
+                           tree_mask, stage, status, ws, ws_bytes, stream);
+}
+
+extern "C" int graft_build_tree_block(const GraftConfig* cfg, int B, const float* block_logits,
+                                      const int32_t* root_tok, const int32_t* M_succ, const int32_t* L,
+                                      int32_t* tree_tok, int32_t* tree_parent, int32_t* tree_depth,
+                                      int32_t* tree_pos, uint64_t* tree_mask, int32_t* stage,
+                                      int32_t* status, void* ws, size_t ws_bytes, graft_stream_t stream) {
+    return build_tree_impl(cfg, B, block_logits, 1, root_tok, M_succ, L, tree_tok, tree_parent, tree_depth, tree_pos,
+                           tree_mask, stage, status, ws, ws_bytes, stream);
 }
