@@ -19,6 +19,7 @@ from typing import List
 import numpy as np
 
 from . import accept as acc
+from . import sampling as smp
 from . import attention as att
 from . import tree as tr
 from . import update_m as um
@@ -156,3 +157,76 @@ def greedy_hybrid(lm: TinyLM, prompt: List[int], n_new: int, Lcap: int, cfg: dic
         steps.append(dict(stage=res.stage, acc_len=n,
                           retrieved_accepted=sum(1 for p in path if p >= tree.n_draft)))
     return out[:n_new], cache, L, steps
+
+
+def sample_ar(lm: TinyLM, prompt: List[int], n_new: int, Lcap: int, T: float, seed: int):
+    """Autoregressive sampling at temperature T with the position-keyed Gumbel noise of
+    oracle.sampling; returns (tokens, cache, L, perturbed-score gaps)."""
+    cache = lm.new_cache(Lcap)
+    L = 0
+    logits = None
+    out: List[int] = []
+    gaps: List[float] = []
+
+    def push(tok):
+        nonlocal L, logits
+        lg, kv = lm.forward([tok], [L], [1], cache, L)
+        for c, (k, v) in zip(cache, kv):
+            c["K"][L] = k[0]
+            c["V"][L] = v[0]
+        L += 1
+        logits = lg[0]
+
+    for t in prompt:
+        push(t)
+    while len(out) < n_new:
+        y, gap = smp.sample_row(logits, T, seed, 0, L)  # the token sampled here goes to position L
+        gaps.append(gap)
+        out.append(y)
+        push(y)
+    return out, cache, L, gaps
+
+
+def sample_hybrid(lm: TinyLM, prompt: List[int], n_new: int, Lcap: int, cfg: dict, T: float, seed: int,
+                  sharpen: float = 8.0, noise: float = 1.0):
+    """Hybrid-tree decoding with sampling acceptance: the target's sample at every node, then the
+    greedy rule on the samples.  Returns (tokens, cache, L, per-step records, perturbed-score gaps)."""
+    rng = np.random.default_rng(seed + 7)
+    cache = lm.new_cache(Lcap)
+    L = 0
+    for t in prompt[:-1]:
+        _, kv = lm.forward([t], [L], [1], cache, L)
+        for c, (k, v) in zip(cache, kv):
+            c["K"][L] = k[0]
+            c["V"][L] = v[0]
+        L += 1
+    root = prompt[-1]
+    M_succ, M_cnt = um.empty_M(lm.V, cfg["W"])
+    out: List[int] = []
+    steps, gaps = [], []
+    while len(out) < n_new:
+        def row_fn(d, f, path, L=L):
+            chain = [(1 << (i + 1)) - 1 for i in range(len(path))]
+            lg, _ = lm.forward(path, [L + i for i in range(len(path))], chain, cache, L)
+            return (sharpen * lg[-1] + rng.normal(0.0, noise, lm.V)).astype(np.float32)
+
+        res = tr.draft_tree(row_fn, root, cfg)
+        nodes = tr.retained_draft(res, cfg)
+        ret = tr.retrieve(root, M_succ, cfg["tmpl_parent"], cfg["tmpl_rank"])
+        tree = tr.merge(root, nodes, ret, cfg["tmpl_parent"], res.stage, L, cfg)
+        logits, kv = lm.forward(tree.tok, tree.pos, tree.mask, cache, L)
+        y, gap = smp.sample_tree(logits[None], np.array(tree.pos)[None], T, seed)
+        g, n, path, out_tok, bonus = acc.accept_from_argmax(y[0], tree.tok, tree.parent, tree.depth)
+        gaps.extend(gap[0][p] for p in path)
+        for c, (k, v) in zip(cache, kv):
+            for t, p in enumerate(path):
+                c["K"][L + t] = k[p]
+                c["V"][L + t] = v[p]
+        L += n
+        out.extend(out_tok)
+        root = bonus
+        M_succ, M_cnt = um.update_M(M_succ, M_cnt, np.array(tree.tok), np.array(g))
+        steps.append(dict(stage=res.stage, acc_len=n,
+                          retrieved_accepted=sum(1 for p in path if p >= tree.n_draft)))
+    return out[:n_new], cache, L, steps, gaps
+
