@@ -265,6 +265,42 @@ int graft_lm_head_argmax(int N, int d_model, int V, const void* H, const void* W
                          graft_stream_t stream);
 
 /*
+ * graft_sample_tokens — the target's sample at every tree node, for lossless
+ * sampling acceptance at temperature > 0 (Graft article, architecture
+ * paragraph, and Graft abstract: verification is lossless).  Every proposal
+ * in a Graft tree is deterministic (the drafter's top-k, retrieved tokens);
+ * for such proposals the speculative-sampling rule over a node's children
+ * (accept child i with its residual probability, renormalise on rejection)
+ * has the law of drawing one sample y ~ softmax(logits / T) per node and
+ * accepting the first child whose token is y.  Feed the samples to
+ * graft_accept_compact as its argmax input (target_logits NULL).
+ *
+ *   target_logits [B][Kmax][V] f32, tree_pos [B][Kmax] i32 (graft_build_tree)
+ *   temperature > 0; seed: 64-bit stream key
+ * Output: sampled [B][Kmax] = argmax_v(logits[v] / T + G_v), G Gumbel noise
+ *   from Philox-4x32-10 (Salmon et al., SC 2011) with counter (v / 4,
+ *   tree_pos + 1, b, 0) and key (seed low, seed high) words, draw x = word
+ *   v % 4, u = ((x >> 9) + 1/2) / 2^23, G = -log(-log u).  Nodes at the same
+ *   position see the same noise, so tree decoding emits exactly what
+ *   autoregressive sampling with this noise emits.
+ * Workspace: graft_sample_tokens_workspace_size.
+ */
+int graft_sample_tokens_workspace_size(int B, int Kmax, int V, size_t* bytes);
+int graft_sample_tokens(int B, int Kmax, int V, const float* target_logits, const int32_t* tree_pos,
+                        float temperature, uint64_t seed, int32_t* sampled, void* ws, size_t ws_bytes,
+                        graft_stream_t stream);
+
+/*
+ * graft_lm_head_sample — graft_sample_tokens fused into the lm_head product
+ * of graft_lm_head_argmax: rows n = b * Kmax + i of H are the nodes of the
+ * B trees, tree_pos [N] their positions; the logits are never written.
+ * N must be a multiple of Kmax.  Workspace: graft_lm_head_argmax_workspace_size.
+ */
+int graft_lm_head_sample(int N, int d_model, int V, const void* H, const void* W_lm, int Kmax,
+                         const int32_t* tree_pos, float temperature, uint64_t seed, int32_t* sampled,
+                         int32_t* status, void* ws, size_t ws_bytes, graft_stream_t stream);
+
+/*
  * graft_update_M — online update of the adjacency table from verified
  * pairs (Graft article, method paragraph, fourth point: M is updated
  * continuously from the verified tree's logits).

@@ -77,6 +77,9 @@ _SIGNATURES = {
     "graft_accept_compact": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I64, _P, _P, _P, _P, _P, _P,
                              _P, _P, _SZ, _P],
     "graft_lm_head_argmax_workspace_size": [_I, ctypes.POINTER(_SZ)],
+    "graft_lm_head_sample": [_I, _I, _I, _P, _P, _I, _P, ctypes.c_float, ctypes.c_uint64, _P, _P, _P, _SZ, _P],
+    "graft_sample_tokens_workspace_size": [_I, _I, _I, ctypes.POINTER(_SZ)],
+    "graft_sample_tokens": [_I, _I, _I, _P, _P, ctypes.c_float, ctypes.c_uint64, _P, _P, _SZ, _P],
     "graft_lm_head_argmax": [_I, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P],
     "graft_update_M_workspace_size": [_I64, ctypes.POINTER(_SZ)],
     "graft_update_M": [_P, _P, _I, _I, _P, _P, _I64, _P, _P, _SZ, _P],
@@ -304,6 +307,46 @@ def graft_lm_head_argmax(H, W_lm, argmax=None, max_logit=None, status=None, ws=N
     _check(lib().graft_lm_head_argmax(N, d, V, _ptr(H), _ptr(W_lm), _ptr(argmax), _ptr(max_logit), _ptr(status),
                                       _ptr(ws), nws, _stream(stream)), "graft_lm_head_argmax")
     return argmax, max_logit
+
+
+def graft_sample_tokens_workspace_size(B: int, Kmax: int, V: int) -> int:
+    n = _SZ()
+    _check(lib().graft_sample_tokens_workspace_size(B, Kmax, V, ctypes.byref(n)), "workspace size")
+    return n.value
+
+
+def graft_sample_tokens(target_logits, tree_pos, temperature: float, seed: int, sampled=None, ws=None, stream=None):
+    """The target's sample per tree node (Gumbel-max with position-keyed Philox noise); [B][Kmax] int32."""
+    B, Kmax, V = target_logits.shape
+    _need(target_logits, "target_logits", torch.float32)
+    _need(tree_pos, "tree_pos", torch.int32, (B, Kmax))
+    if sampled is None:
+        sampled = torch.empty(B, Kmax, dtype=torch.int32, device=target_logits.device)
+    ws, nws = _ws(graft_sample_tokens_workspace_size(B, Kmax, V), target_logits.device, ws)
+    _check(lib().graft_sample_tokens(B, Kmax, V, _ptr(target_logits), _ptr(tree_pos), float(temperature),
+                                     int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(sampled), _ptr(ws), nws, _stream(stream)),
+           "graft_sample_tokens")
+    return sampled
+
+
+def graft_lm_head_sample(H, W_lm, tree_pos, temperature: float, seed: int, sampled=None, status=None, ws=None,
+                         stream=None):
+    """graft_sample_tokens fused into the lm_head product; H [B*Kmax][d], tree_pos [B][Kmax]; returns [B*Kmax]."""
+    N, d = H.shape
+    V = W_lm.shape[0]
+    _need(H, "H", torch.bfloat16, (N, d))
+    _need(W_lm, "W_lm", torch.bfloat16, (V, d))
+    B, Kmax = tree_pos.shape
+    _need(tree_pos, "tree_pos", torch.int32, (B, Kmax))
+    if B * Kmax != N:
+        raise ValueError("H must have one row per tree node")
+    if sampled is None:
+        sampled = torch.empty(N, dtype=torch.int32, device=H.device)
+    ws, nws = _ws(graft_lm_head_argmax_workspace_size(N), H.device, ws)
+    _check(lib().graft_lm_head_sample(N, d, V, _ptr(H), _ptr(W_lm), Kmax, _ptr(tree_pos), float(temperature),
+                                      int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(sampled), _ptr(status), _ptr(ws), nws,
+                                      _stream(stream)), "graft_lm_head_sample")
+    return sampled
 
 
 def graft_update_M_workspace_size(n: int) -> int:

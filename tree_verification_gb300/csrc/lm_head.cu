@@ -19,12 +19,18 @@
 // ties go to the lower id.  Consecutive CTAs take the row tiles of one
 // token tile, so each W tile is read from HBM once while H stays in L2.
 //
+// The sampling variant (graft_lm_head_sample) adds Gumbel noise keyed by
+// (request, position, token) to every logit / T before the maximum
+// (philox.cuh), which draws the target's sample at every node for lossless
+// sampling acceptance, again without writing the logits.
+//
 // Every mbarrier wait is bounded; on timeout the CTA raises
 // GRAFT_STATUS_TIMEOUT, drains its loads and releases TMEM.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include "common.cuh"
+#include "philox.cuh"
 #include "tc_ptx.cuh"
 
 namespace graft {
@@ -85,9 +91,17 @@ __device__ __forceinline__ void raise_abort(volatile uint32_t* flag, int32_t* st
     flag_status(status, GRAFT_STATUS_TIMEOUT);
 }
 
+struct SampleArgs {
+    const int32_t* tree_pos;  // [N]: node n samples the token at tree_pos[n] + 1
+    int Kmax;                 // request of row n = n / Kmax
+    float inv_T;
+    unsigned long long seed;
+};
+
+template <bool SAMPLE>
 __global__ void __launch_bounds__(NTHREADS, 1)
 lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, unsigned long long* __restrict__ keys,
-                      int32_t* status) {
+                      int32_t* status, SampleArgs sa) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -173,10 +187,25 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
             tc_fence_after();
             float best = -INFINITY;
             int bi = -1;
+            uint32_t nb = 0, npos = 0;
+            if (SAMPLE && n < N) {
+                nb = (uint32_t)(n / sa.Kmax);
+                npos = (uint32_t)(sa.tree_pos[n] + 1);
+            }
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 float x[32];
                 tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + c0, x);
                 tmem_wait_ld();
+                if (SAMPLE) {
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const uint4 r4 = noise_draws(sa.seed, nb, npos, (uint32_t)((v0 + c0 + i) >> 2));
+                        x[i] = x[i] * sa.inv_T + gumbel_of(r4.x);
+                        x[i + 1] = x[i + 1] * sa.inv_T + gumbel_of(r4.y);
+                        x[i + 2] = x[i + 2] * sa.inv_T + gumbel_of(r4.z);
+                        x[i + 3] = x[i + 3] * sa.inv_T + gumbel_of(r4.w);
+                    }
+                }
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
                     const int v = v0 + c0 + i;
@@ -247,9 +276,10 @@ extern "C" int graft_lm_head_argmax_workspace_size(int N, size_t* bytes) {
     return GRAFT_OK;
 }
 
-extern "C" int graft_lm_head_argmax(int N, int d_model, int V, const void* H, const void* W_lm, int32_t* argmax,
-                                    float* max_logit, int32_t* status, void* ws, size_t ws_bytes,
-                                    graft_stream_t stream) {
+namespace {
+
+int lm_head_impl(int N, int d_model, int V, const void* H, const void* W_lm, int32_t* argmax, float* max_logit,
+                 const lmh::SampleArgs* sa, int32_t* status, void* ws, size_t ws_bytes, graft_stream_t stream) {
     using namespace lmh;
     if (N < 0 || d_model < 1 || V < 1) return GRAFT_ERR_INVALID_ARG;
     if (N == 0) return GRAFT_OK;
@@ -265,21 +295,47 @@ extern "C" int graft_lm_head_argmax(int N, int d_model, int V, const void* H, co
     unsigned long long* keys = c.take<unsigned long long>((size_t)N);
     Maps m;
     if (!encode_rows(&m.h, H, N, d_model, BM) || !encode_rows(&m.w, W_lm, V, d_model, BN)) return GRAFT_ERR_CUDA;
-    static bool attr_set[64] = {false};
+    static bool attr_set[2][64] = {{false}};
+    const int smp = sa != nullptr;
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (!cuda_ok(cudaFuncSetAttribute(lm_head_argmax_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          (int)SMEM_BYTES)))
-            return GRAFT_ERR_CUDA;
-        attr_set[dev] = true;
+    if (dev >= 0 && dev < 64 && !attr_set[smp][dev]) {
+        const cudaError_t e =
+            smp ? cudaFuncSetAttribute(lm_head_argmax_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES)
+                : cudaFuncSetAttribute(lm_head_argmax_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)SMEM_BYTES);
+        if (!cuda_ok(e)) return GRAFT_ERR_CUDA;
+        attr_set[smp][dev] = true;
     }
     cudaStream_t st = (cudaStream_t)stream;
     const unsigned small = (unsigned)((N + 255) / 256 < 1024 ? (N + 255) / 256 : 1024);
+    const dim3 grid((unsigned)row_tiles, (unsigned)tok_tiles);
     launch_pdl(key_init_kernel, dim3(small), dim3(256), 0, st, keys, N);
-    launch_pdl(lm_head_argmax_kernel, dim3((unsigned)row_tiles, (unsigned)tok_tiles), dim3(NTHREADS), SMEM_BYTES, st,
-               m, N, d_model, V, keys, status);
+    if (smp)
+        launch_pdl(lm_head_argmax_kernel<true>, grid, dim3(NTHREADS), SMEM_BYTES, st, m, N, d_model, V, keys, status,
+                   *sa);
+    else
+        launch_pdl(lm_head_argmax_kernel<false>, grid, dim3(NTHREADS), SMEM_BYTES, st, m, N, d_model, V, keys, status,
+                   SampleArgs{nullptr, 1, 1.f, 0ull});
     launch_pdl(key_final_kernel, dim3(small), dim3(256), 0, st, keys, N, argmax, max_logit);
     count_launches(3);
     return launch_status();
+}
+
+}  // namespace
+
+extern "C" int graft_lm_head_argmax(int N, int d_model, int V, const void* H, const void* W_lm, int32_t* argmax,
+                                    float* max_logit, int32_t* status, void* ws, size_t ws_bytes,
+                                    graft_stream_t stream) {
+    return lm_head_impl(N, d_model, V, H, W_lm, argmax, max_logit, nullptr, status, ws, ws_bytes, stream);
+}
+
+extern "C" int graft_lm_head_sample(int N, int d_model, int V, const void* H, const void* W_lm, int Kmax,
+                                    const int32_t* tree_pos, float temperature, uint64_t seed, int32_t* sampled,
+                                    int32_t* status, void* ws, size_t ws_bytes, graft_stream_t stream) {
+    if (Kmax < 1 || tree_pos == nullptr || !(temperature > 0.f) || (N > 0 && N % Kmax != 0))
+        return GRAFT_ERR_INVALID_ARG;
+    const lmh::SampleArgs sa{tree_pos, Kmax, 1.0f / temperature, (unsigned long long)seed};
+    return lm_head_impl(N, d_model, V, H, W_lm, sampled, nullptr, &sa, status, ws, ws_bytes, stream);
 }
