@@ -418,7 +418,7 @@ def run_graft(args):
         t_e2e = float(t.item())
 
     # the fused lm_head argmax (greedy tokens straight from final hidden states) on this workload's rows
-    lmh = None
+    lmh = sample_from_logits = None
     if args.secondary_reps > 0:
         H, W_lm = synth.lm_head_inputs(wl, dev)
         g_out = torch.empty(H.shape[0], dtype=torch.int32, device=dev)
@@ -436,6 +436,28 @@ def run_graft(args):
         nbytes = (H.numel() + W_lm.numel()) * 2 + H.shape[0] * 8
         lmh = {"rows": H.shape[0], "d_model": wl.d_model, "vocab": wl.V, "us": t_lmh * 1e6,
                "tflops": flops / t_lmh / 1e12, "gbs": nbytes / t_lmh / 1e9}
+        # sampling acceptance: the target's sample per node, fused into the lm_head and from given logits
+        pos = step.tree["pos"]
+        smp_graph = torch.cuda.CUDAGraph()
+        gb.graft_lm_head_sample(H, W_lm, pos, 1.0, 1234, sampled=g_out, status=step.status, ws=lws)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(smp_graph):
+            gb.graft_lm_head_sample(H, W_lm, pos, 1.0, 1234, sampled=g_out, status=step.status, ws=lws)
+        for _ in range(3):
+            smp_graph.replay()
+        t_smp = timed(smp_graph, args.secondary_reps) / args.secondary_reps
+        lmh["sample_us"] = t_smp * 1e6
+        sws = torch.empty(max(1, gb.graft_sample_tokens_workspace_size(wl.B, wl.Kmax, wl.V)), dtype=torch.uint8,
+                          device=dev)
+        st_graph = torch.cuda.CUDAGraph()
+        gb.graft_sample_tokens(tl, pos, 1.0, 1234, sampled=step.acc["argmax"], ws=sws)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(st_graph):
+            gb.graft_sample_tokens(tl, pos, 1.0, 1234, sampled=step.acc["argmax"], ws=sws)
+        for _ in range(3):
+            st_graph.replay()
+        t_st = timed(st_graph, args.secondary_reps) / args.secondary_reps
+        sample_from_logits = {"us": t_st * 1e6, "gbs": tl.numel() * 4 / t_st / 1e9}
         del H, W_lm
 
     bytes_call = attention_bytes_per_call(wl, L0.cpu())
@@ -463,7 +485,7 @@ def run_graft(args):
         "secondary": {"tree_attention_gbs": achieved, "tree_attention_frac_of_peak": achieved / peak,
                       "retrieval_fill_us": t_ret * 1e6, "build_tree_us": t_tree * 1e6,
                       "launches_per_step": launches_per_step, "device_status": status,
-                      "lm_head_argmax": lmh},
+                      "lm_head_argmax": lmh, "sample_tokens_from_logits": sample_from_logits},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inputs = (dl, tl, roots, L0, M_succ, M_cnt, layers[0])

@@ -52,3 +52,46 @@ def test_lm_head_sample_parity():
     logits = olm.logits(H.float().numpy(), W.float().numpy()).reshape(B, K, V)
     n_cert = _check(logits, pos, T, seed, to_np(got).reshape(B, K))
     assert n_cert >= 0.9 * B * K
+
+
+def test_verify_step_with_sampling_and_emitted_policy():
+    """A whole step at temperature 0.7 with M refreshed from the tree pairs and the emitted bigrams,
+    against the oracle run on the same inputs."""
+    from oracle import accept as oacc
+    from oracle import config as oconfig
+    from oracle import tree as otree
+    from oracle import update_m as oupd
+    from tree_verification_gb300 import synth
+    from tree_verification_gb300.step import VerifyStep
+
+    wl = synth.WORKLOADS["tiny"]
+    cfg = gb().graft_config_init(wl.Kmax, wl.D, wl.k, wl.V, wl.W, list(wl.checkpoints), wl.tau)
+    cfg_o = oconfig.make_config(Kmax=wl.Kmax, D=wl.D, k=wl.k, V=wl.V, W=wl.W)
+    Lcap = wl.lcap()
+    dl = synth.draft_logits(wl, DEV)
+    roots, L0 = synth.root_tokens(wl), synth.prefix_lengths(wl)
+    s_np, c_np = synth.zipf_M(wl.V, wl.W, wl.seed + 5)
+    Q, Kc, Vc, Kt, Vt = synth.layer_tensors(wl, 0, DEV, Lcap=Lcap)
+    res = otree.draft_tree(lambda d, f, _p: dl[0, d, f].cpu().numpy(), int(roots[0]), cfg_o)
+    tree = otree.merge(int(roots[0]), otree.retained_draft(res, cfg_o),
+                       otree.retrieve(int(roots[0]), s_np, cfg_o["tmpl_parent"], cfg_o["tmpl_rank"]),
+                       cfg_o["tmpl_parent"], res.stage, int(L0[0]), cfg_o)
+    tl = synth.target_logits(wl, DEV) * 4.0  # peaked enough that sampling accepts a few nodes
+    T, seed = 0.7, 5
+    y, gap = osmp.sample_tree(tl.cpu().numpy(), np.array(tree.pos)[None], T, seed)
+    assert gap.min() >= CERT
+    g, n, path, out_tok, bonus = oacc.accept_from_argmax(y[0], tree.tok, tree.parent, tree.depth)
+    succ, cnt = oupd.update_M(s_np, c_np, np.array(tree.tok), y[0])
+    succ, cnt = oupd.update_M(succ, cnt, *oupd.emitted_pairs(np.array([tree.tok]), np.array([out_tok + [-1]]),
+                                                            np.array([n])))
+    M_succ, M_cnt = torch.from_numpy(s_np).to(DEV), torch.from_numpy(c_np).to(DEV)
+    L = L0.to(DEV)
+    step = VerifyStep(cfg, wl.B, wl.Hq, wl.Hkv, 1, Lcap, DEV, [Kc], [Vc], [Kt], [Vt], m_policy="both",
+                      temperature=T, seed=seed)
+    step.run(dl, roots.to(DEV), M_succ, M_cnt, L, [Q], tl)
+    torch.cuda.synchronize()
+    assert int(step.status.item()) == 0
+    assert int(step.acc["acc_len"][0]) == n
+    assert to_np(step.acc["out_tok"][0])[:n].tolist() == out_tok
+    assert int(step.acc["bonus"][0]) == bonus
+    assert np.array_equal(to_np(M_succ), succ) and np.array_equal(to_np(M_cnt), cnt)

@@ -6,6 +6,10 @@ and runs them in the Graft article's order on one CUDA stream:
     graft_build_tree  ->  graft_tree_attention x n_layers  ->
     graft_accept_compact  ->  M update
 
+With ``temperature`` > 0 the step verifies by sampling: graft_sample_tokens
+draws the target's sample at every node (keyed by ``seed`` and position)
+and graft_accept_compact accepts on those samples; otherwise it is greedy.
+
 The M update follows ``m_policy``: "tree" adds every tree node's (token,
 target argmax) pair (graft_update_M); "emitted" adds the bigrams of the
 tokens the step emitted (graft_update_M_emitted), the prompt-evidence policy
@@ -29,10 +33,11 @@ from . import binding as gb
 class VerifyStep:
     def __init__(self, cfg: gb.GraftConfig, B: int, Hq: int, Hkv: int, n_layers: int, Lcap: int, device,
                  Kc: Sequence[torch.Tensor], Vc: Sequence[torch.Tensor], Kt: Sequence[torch.Tensor],
-                 Vt: Sequence[torch.Tensor], m_policy: str = "tree"):
+                 Vt: Sequence[torch.Tensor], m_policy: str = "tree", temperature: float = 0.0, seed: int = 0):
         if m_policy not in ("tree", "emitted", "both"):
             raise ValueError("m_policy must be 'tree', 'emitted' or 'both'")
         self.m_policy = m_policy
+        self.temperature, self.seed = float(temperature), int(seed)
         self.cfg, self.B, self.Hq, self.Hkv, self.n_layers, self.Lcap = cfg, B, Hq, Hkv, n_layers, Lcap
         self.device = torch.device(device)
         K, dev = cfg.Kmax, self.device
@@ -50,6 +55,7 @@ class VerifyStep:
         self.ws_acc = torch.empty(max(1, gb.graft_accept_compact_workspace_size(B, K, cfg.V)), **u8)
         self.ws_upd = torch.empty(max(1, gb.graft_update_M_workspace_size(B * K)), **u8)
         self.ws_emit = torch.empty(max(1, gb.graft_update_M_emitted_workspace_size(B, K)), **u8)
+        self.ws_smp = torch.empty(max(1, gb.graft_sample_tokens_workspace_size(B, K, cfg.V)), **u8)
         self.O = torch.empty(B, K, Hq, gb.HEAD_DIM, dtype=torch.bfloat16, device=dev)
         self.Kc, self.Vc, self.Kt, self.Vt = list(Kc), list(Vc), list(Kt), list(Vt)
         self.Kc_ptrs = gb.layer_pointers(self.Kc, dev)
@@ -67,9 +73,17 @@ class VerifyStep:
         for l in (range(self.n_layers) if attn_layers is None else attn_layers):
             gb.graft_tree_attention(Q[l], self.Kc[l], self.Vc[l], self.Kt[l], self.Vt[l], L, self.tree["mask"],
                                     self.scale, O=self.O, status=self.status, ws=self.ws_attn)
-        gb.graft_accept_compact(target_logits, self.tree["tok"], self.tree["parent"], self.tree["depth"],
-                                self.Kc_ptrs, self.Vc_ptrs, self.Kt_ptrs, self.Vt_ptrs, self.n_layers, self.Hkv,
-                                self.Lcap, L, out=self.acc, status=self.status, ws=self.ws_acc)
+        if self.temperature > 0.0:
+            gb.graft_sample_tokens(target_logits, self.tree["pos"], self.temperature, self.seed,
+                                   sampled=self.acc["argmax"], ws=self.ws_smp)
+            gb.graft_accept_compact(None, self.tree["tok"], self.tree["parent"], self.tree["depth"],
+                                    self.Kc_ptrs, self.Vc_ptrs, self.Kt_ptrs, self.Vt_ptrs, self.n_layers, self.Hkv,
+                                    self.Lcap, L, out=self.acc, status=self.status, ws=self.ws_acc,
+                                    argmax=self.acc["argmax"], V=self.cfg.V)
+        else:
+            gb.graft_accept_compact(target_logits, self.tree["tok"], self.tree["parent"], self.tree["depth"],
+                                    self.Kc_ptrs, self.Vc_ptrs, self.Kt_ptrs, self.Vt_ptrs, self.n_layers, self.Hkv,
+                                    self.Lcap, L, out=self.acc, status=self.status, ws=self.ws_acc)
         if self.m_policy in ("tree", "both"):
             gb.graft_update_M(M_succ, M_cnt, self.tree["tok"].view(-1), self.acc["argmax"].view(-1),
                               status=self.status, ws=self.ws_upd)
