@@ -31,6 +31,16 @@ struct AttnArgs {
     int32_t* status;
 };
 
+// Marks the log2-sum-exp slots of one 128-row tile's partial for chunk c:
+// -inf for a chunk past the request's keys (it contributes nothing), +inf
+// for chunk 0 of a request that fits one chunk (its output was written
+// directly, so the merge leaves the rows alone).  No-op without partials.
+static __device__ __noinline__ void mark_partial(const AttnArgs& a, int b, int kvh, int tile, int c, float value) {
+    if (a.nchunk <= 1 || a.part_lse == nullptr || a.cluster > 0 || tile >= a.nRB) return;
+    const size_t base = ((((size_t)b * a.Hkv + kvh) * a.nRB + tile) * a.nchunk + c) * 128;
+    for (int r = threadIdx.x; r < 128; r += blockDim.x) a.part_lse[base + r] = value;
+}
+
 // Warp-level mma.sync path: any group size; 128-row CTAs.
 int attn_mma_launch(const AttnArgs& a, cudaStream_t st);
 // tcgen05 path: group sizes dividing 128; CTAs of two 128-row tiles

@@ -85,10 +85,15 @@ attn_partial_kernel(AttnArgs a) {
     const int Lb = a.L[b];
     if (Lb < 0 || Lb > a.Lcap) {
         if (c == 0 && tid == 0 && rb == 0 && kvh == 0) flag_status(a.status, GRAFT_STATUS_LENGTH);
+        mark_partial(a, b, kvh, rb, c, -INFINITY);
         return;
     }
     const int nck = Lb > 0 ? (Lb + a.C - 1) / a.C : 1;
-    if (c >= nck) return;
+    if (c >= nck) {
+        mark_partial(a, b, kvh, rb, c, -INFINITY);
+        return;
+    }
+    if (nck == 1) mark_partial(a, b, kvh, rb, 0, INFINITY);
     const int k0 = c * a.C;
     const int k1 = min(Lb, k0 + a.C);
     const int nb_prefix = (k1 - k0 + BN - 1) / BN;
@@ -301,9 +306,12 @@ attn_partial_kernel(AttnArgs a) {
 
 }  // namespace attn_mma
 
-// Merges the per-chunk partial outputs of every (request, KV head, row) whose
-// request spans more than one key chunk: O = sum_c 2^(lse_c - lse) O_c with
-// lse = log2 sum_c 2^lse_c.  One warp per output row, four dims per lane.
+// Merges the per-chunk partial outputs of every (request, KV head, row) in
+// one pass: O = sum_c 2^(lse_c - lse) O_c with lse = log2 sum_c 2^lse_c,
+// kept as a running maximum.  The attention kernels mark chunks past a
+// request's keys with lse = -inf and rows already written directly with
+// lse_0 = +inf, so the merge needs no request length and issues the loads of
+// four chunks at once.  One warp per output row, four dims per lane.
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(AttnArgs a) {
     griddep_enter();
@@ -317,28 +325,43 @@ attn_combine_kernel(AttnArgs a) {
     const int b = (int)(row / (128LL * a.nRB * a.Hkv));
     const int gr = tile * 128 + r;
     if (gr >= a.R) return;
-    const int Lb = a.L[b];
-    if (Lb < 0 || Lb > a.Lcap) return;
-    const int nck = Lb > 0 ? (Lb + a.C - 1) / a.C : 1;
-    if (nck == 1) return;
     const size_t base = (((size_t)b * a.Hkv + kvh) * a.nRB + tile) * a.nchunk;
-    float mx = -INFINITY;
-    for (int c = lane; c < nck; c += 32) mx = fmaxf(mx, a.part_lse[(base + c) * 128 + r]);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    const float* lse = a.part_lse + base * 128 + r;
+    const float* po = a.part_o + (base * 128 + r) * GRAFT_HEAD_DIM + lane * 4;
+    float m = -INFINITY, l = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float wsum = 0.f;
-    for (int c = 0; c < nck; ++c) {
-        const size_t pi = (base + c) * 128 + r;
-        const float w = exp2f(a.part_lse[pi] - mx);
-        const float4 v = *reinterpret_cast<const float4*>(a.part_o + pi * GRAFT_HEAD_DIM + lane * 4);
-        acc.x += w * v.x;
-        acc.y += w * v.y;
-        acc.z += w * v.z;
-        acc.w += w * v.w;
-        wsum += w;
+    for (int c0 = 0; c0 < a.nchunk; c0 += 4) {
+        float lc[4];
+        float4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int c = c0 + u;
+            lc[u] = c < a.nchunk ? lse[(size_t)c * 128] : -INFINITY;
+            v[u] = c < a.nchunk ? *reinterpret_cast<const float4*>(po + (size_t)c * 128 * GRAFT_HEAD_DIM)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (c0 == 0 && lc[0] == INFINITY) return;  // written directly by the attention kernel
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (lc[u] == -INFINITY) continue;  // nothing from this chunk (uniform over the warp)
+            if (lc[u] > m) {
+                const float s = (m == -INFINITY) ? 0.f : exp2f(m - lc[u]);
+                acc.x *= s;
+                acc.y *= s;
+                acc.z *= s;
+                acc.w *= s;
+                l *= s;
+                m = lc[u];
+            }
+            const float w = exp2f(lc[u] - m);
+            acc.x += w * v[u].x;
+            acc.y += w * v[u].y;
+            acc.z += w * v[u].z;
+            acc.w += w * v[u].w;
+            l += w;
+        }
     }
-    const float inv = 1.f / wsum;
+    const float inv = l > 0.f ? 1.f / l : 0.f;
     const int node = gr / a.G, h = kvh * a.G + gr % a.G;
     __nv_bfloat16* dst =
         reinterpret_cast<__nv_bfloat16*>(a.O) + (((size_t)b * a.Kmax + node) * a.Hq + h) * GRAFT_HEAD_DIM + lane * 4;

@@ -172,9 +172,12 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     const int nck = (Lb > 0 && !bad_len) ? (Lb + a.C - 1) / a.C : 1;
     if (bad_len || c >= nck) {  // uniform over the CTA
         if (bad_len && tid == 0 && c == 0 && rb == 0 && kvh == 0) flag_status(a.status, GRAFT_STATUS_LENGTH);
+        for (int t = 0; t < ntile; ++t) mark_partial(a, b, kvh, rb * 2 + t, c, -INFINITY);
         if (warp == 1) tmem_dealloc(tmem, 512);
         return;
     }
+    if (nck == 1)
+        for (int t = 0; t < ntile; ++t) mark_partial(a, b, kvh, rb * 2 + t, 0, INFINITY);
     const int k0 = c * a.C;
     const int k1 = min(Lb, k0 + a.C);
     const int nb_prefix = (k1 - k0 + BN - 1) / BN;

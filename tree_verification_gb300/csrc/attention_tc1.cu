@@ -177,9 +177,11 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     const int nck = (Lb > 0 && !bad_len) ? (Lb + a.C - 1) / a.C : 1;
     if (bad_len || (c >= nck && ncl == 0)) {  // uniform over the CTA (and over a cluster: same b)
         if (bad_len && tid == 0 && c == 0 && rb == 0 && kvh == 0) flag_status(a.status, GRAFT_STATUS_LENGTH);
+        mark_partial(a, b, kvh, rb, c, -INFINITY);
         if (warp == 2) tmem_dealloc(tmem, 512);
         return;
     }
+    if (nck == 1) mark_partial(a, b, kvh, rb, 0, INFINITY);
     // in a cluster a chunk past the request's keys stays for the merge and contributes nothing
     const bool empty = c >= nck;
     const int k0 = c * a.C;
