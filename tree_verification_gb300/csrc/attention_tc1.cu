@@ -141,7 +141,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     const int rb = blockIdx.x % a.nRB;  // 128-row tile within (request, KV head)
     const int kvh = blockIdx.x / a.nRB;
     const int c = blockIdx.y;
-    const int b = blockIdx.z;
+    int b = blockIdx.z;  // remapped below to the request this CTA serves
     const int ncl = a.cluster;  // > 0: the chunks of this row tile form one cluster (rank = c)
 
     // Prologue that touches no global memory: it overlaps the previous kernel's tail.
@@ -172,6 +172,22 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Longest-first dispatch: CTAs launch in blockIdx.z order, so z maps to the z-th longest
+    // request (ties to the lower index) and short requests fill the last wave.
+    if (a.B > 1 && a.B <= NTHREADS) {
+        __shared__ int s_req;
+        if (tid < a.B) {
+            const int li = a.L[tid];
+            int rank = 0;
+            for (int j = 0; j < a.B; ++j) {
+                const int lj = a.L[j];
+                rank += (lj > li) || (lj == li && j < tid);
+            }
+            if (rank == (int)blockIdx.z) s_req = tid;
+        }
+        __syncthreads();
+        b = s_req;
+    }
     const int Lb = a.L[b];
     const bool bad_len = Lb < 0 || Lb > a.Lcap;
     const int nck = (Lb > 0 && !bad_len) ? (Lb + a.C - 1) / a.C : 1;
