@@ -186,7 +186,10 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     const int Lb = a.L[b];
     const bool bad_len = Lb < 0 || Lb > a.Lcap;
     const int nck = (Lb > 0 && !bad_len) ? (Lb + a.C - 1) / a.C : 1;
-    if (bad_len || c >= nck) {  // uniform over the CTA
+    // A split request whose prefix leaves a chunk CTA idle gives it the tree block, so the last
+    // prefix chunk does not carry one block more than the others.
+    const int tree_chunk = (nck > 1 && nck < a.nchunk) ? nck : nck - 1;
+    if (bad_len || c > tree_chunk) {  // uniform over the CTA
         if (bad_len && tid == 0 && c == 0 && rb == 0 && kvh == 0) flag_status(a.status, GRAFT_STATUS_LENGTH);
         for (int t = 0; t < ntile; ++t) mark_partial(a, b, kvh, rb * 2 + t, c, -INFINITY);
         if (warp == 1) tmem_dealloc(tmem, 512);
@@ -195,9 +198,9 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     if (nck == 1)
         for (int t = 0; t < ntile; ++t) mark_partial(a, b, kvh, rb * 2 + t, 0, INFINITY);
     const int k0 = c * a.C;
-    const int k1 = min(Lb, k0 + a.C);
+    const int k1 = max(k0, min(Lb, k0 + a.C));
     const int nb_prefix = (k1 - k0 + BN - 1) / BN;
-    const bool has_tree = (c == nck - 1);
+    const bool has_tree = (c == tree_chunk);
     const int nb = nb_prefix + (has_tree ? 1 : 0);
     const int ragged_block = ((k1 - k0) % BN) != 0 ? nb_prefix - 1 : -1;
     const int ragged_valid = (k1 - k0) % BN;

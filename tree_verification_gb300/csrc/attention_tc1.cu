@@ -191,7 +191,10 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     const int Lb = a.L[b];
     const bool bad_len = Lb < 0 || Lb > a.Lcap;
     const int nck = (Lb > 0 && !bad_len) ? (Lb + a.C - 1) / a.C : 1;
-    if (bad_len || (c >= nck && ncl == 0)) {  // uniform over the CTA (and over a cluster: same b)
+    // A split request whose prefix leaves a chunk CTA idle gives it the tree block, so the last
+    // prefix chunk does not carry one block more than the others (not in cluster mode).
+    const int tree_chunk = (ncl == 0 && nck > 1 && nck < a.nchunk) ? nck : nck - 1;
+    if (bad_len || (c > tree_chunk && ncl == 0)) {  // uniform over the CTA (and over a cluster: same b)
         if (bad_len && tid == 0 && c == 0 && rb == 0 && kvh == 0) flag_status(a.status, GRAFT_STATUS_LENGTH);
         mark_partial(a, b, kvh, rb, c, -INFINITY);
         if (warp == 2) tmem_dealloc(tmem, 512);
@@ -199,11 +202,11 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     }
     if (nck == 1) mark_partial(a, b, kvh, rb, 0, INFINITY);
     // in a cluster a chunk past the request's keys stays for the merge and contributes nothing
-    const bool empty = c >= nck;
+    const bool empty = c > tree_chunk;
     const int k0 = c * a.C;
-    const int k1 = empty ? k0 : min(Lb, k0 + a.C);
+    const int k1 = empty ? k0 : max(k0, min(Lb, k0 + a.C));
     const int nb_prefix = (k1 - k0 + BN - 1) / BN;
-    const bool has_tree = !empty && (c == nck - 1);
+    const bool has_tree = !empty && (c == tree_chunk);
     const int nb = nb_prefix + (has_tree ? 1 : 0);
     const int ragged_block = ((k1 - k0) % BN) != 0 ? nb_prefix - 1 : -1;
     const int ragged_valid = (k1 - k0) % BN;
