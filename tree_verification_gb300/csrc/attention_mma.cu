@@ -310,8 +310,11 @@ attn_partial_kernel(AttnArgs a) {
 // one pass: O = sum_c 2^(lse_c - lse) O_c with lse = log2 sum_c 2^lse_c,
 // kept as a running maximum.  The attention kernels mark chunks past a
 // request's keys with lse = -inf and rows already written directly with
-// lse_0 = +inf, so the merge needs no request length and issues the loads of
-// four chunks at once.  One warp per output row, four dims per lane.
+// lse_0 = +inf, so the merge needs no request length.  One warp per output
+// row, four dims per lane; the loads of up to 16 chunks are issued together,
+// so a row costs one memory round trip per 16 chunks.
+constexpr int kMergeBatch = 16;
+
 __global__ void __launch_bounds__(256)
 attn_combine_kernel(AttnArgs a) {
     griddep_enter();
@@ -330,29 +333,33 @@ attn_combine_kernel(AttnArgs a) {
     const float* po = a.part_o + (base * 128 + r) * GRAFT_HEAD_DIM + lane * 4;
     float m = -INFINITY, l = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int c0 = 0; c0 < a.nchunk; c0 += 4) {
-        float lc[4];
-        float4 v[4];
+    for (int c0 = 0; c0 < a.nchunk; c0 += kMergeBatch) {
+        float lc[kMergeBatch];
+        float4 v[kMergeBatch];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
+        for (int u = 0; u < kMergeBatch; ++u) {
             const int c = c0 + u;
             lc[u] = c < a.nchunk ? lse[(size_t)c * 128] : -INFINITY;
             v[u] = c < a.nchunk ? *reinterpret_cast<const float4*>(po + (size_t)c * 128 * GRAFT_HEAD_DIM)
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
         }
         if (c0 == 0 && lc[0] == INFINITY) return;  // written directly by the attention kernel
+        float mb = m;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            if (lc[u] == -INFINITY) continue;  // nothing from this chunk (uniform over the warp)
-            if (lc[u] > m) {
-                const float s = (m == -INFINITY) ? 0.f : exp2f(m - lc[u]);
-                acc.x *= s;
-                acc.y *= s;
-                acc.z *= s;
-                acc.w *= s;
-                l *= s;
-                m = lc[u];
-            }
+        for (int u = 0; u < kMergeBatch; ++u) mb = fmaxf(mb, lc[u]);
+        if (mb == -INFINITY) continue;  // nothing from this batch (uniform over the warp)
+        if (mb > m) {
+            const float s = (m == -INFINITY) ? 0.f : exp2f(m - mb);
+            acc.x *= s;
+            acc.y *= s;
+            acc.z *= s;
+            acc.w *= s;
+            l *= s;
+            m = mb;
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            if (lc[u] == -INFINITY) continue;  // chunk past the request's keys: its loaded partial is garbage
             const float w = exp2f(lc[u] - m);
             acc.x += w * v[u].x;
             acc.y += w * v[u].y;

@@ -9,9 +9,9 @@
 // One-tile variant: one CTA computes one 128-row tile of query rows (all
 // query heads of one KV head for 128 / group tree nodes) against one key
 // chunk, in 128-key blocks.  It suits short chunks (small batches, short
-// prefixes: many CTAs with few blocks each), where its shorter prologue and
-// TMEM-resident Q beat the two-tile kernel of attention_tc.cu, whose CTAs
-// share each K/V block between two tiles.
+// prefixes: many CTAs with few blocks each), where its shorter prologue
+// beats the two-tile kernel of attention_tc.cu, whose CTAs share each K/V
+// block between two tiles.
 //
 // Warp roles (8 warps):
 //   warp 0      TMA producer: the Q tile once, then K blocks into a 3-stage
@@ -19,17 +19,17 @@
 //               stage is released as soon as its S product has run
 //   warp 3      TMA producer: V blocks into their own 3-stage ring, a stage
 //               released once its PV product has run
-//   warp 1      MMA issuer (one lane): S = Q K^T with Q read from TMEM, then
-//               O += P V with P read from TMEM; shared-memory descriptors
-//               are built once and offset per MMA
+//   warp 1      MMA issuer (one lane): S = Q K^T with both operands in
+//               shared memory, then O += P V with P read from TMEM;
+//               shared-memory descriptors are built once and offset per MMA
 //   warp 2      owns the TMEM allocation (512 columns)
-//   warps 4-7   copy Q into TMEM, then softmax + epilogue (TMEM lanes
-//               0-127, one query row per thread)
-// TMEM columns: S/P double buffer [0,128) and [128,256), O [256,384), Q as
-// packed bf16 pairs [384,448).  Keeping Q in TMEM leaves the K block as the
-// only shared-memory operand of the S product, so that product is bound by
-// the tensor pipe rather than by shared-memory bandwidth.  Softmax
-// overwrites the first 64 columns of its S buffer with P as packed bf16
+//   warps 4-7   softmax + epilogue (TMEM lanes 0-127, one query row per
+//               thread)
+// TMEM columns: S/P double buffer [0,128) and [128,256), O [256,384).  The
+// first S product issues as soon as the Q tile and the first K block have
+// landed: Q is read by the tensor core from shared memory, which measured
+// faster per MMA than a TMEM A operand at this shape and needs no copy
+// before the first product.  Softmax overwrites the first 64 columns of its S buffer with P as packed bf16
 // pairs; the PV MMA takes that as its A operand straight from TMEM, so P
 // never touches shared memory.
 //
@@ -84,8 +84,7 @@ constexpr uint32_t OFF_STAGE = OFF_K;  // epilogue staging reuses the rings once
 constexpr uint32_t OFF_LSE = OFF_STAGE + 128 * 512;  // cluster mode: the staged rows' log2-sum-exp
 // barriers
 constexpr int BAR_Q = 0;              // Q tile landed in shared memory
-constexpr int BAR_QT = 1;             // Q copied into TMEM (128 arrivals)
-constexpr int BAR_KF = 2;             // [SK] K block landed
+constexpr int BAR_KF = 1;             // [SK] K block landed
 constexpr int BAR_KE = BAR_KF + SK;   // [SK] K block consumed by its S product
 constexpr int BAR_VF = BAR_KE + SK;   // [SV] V block landed
 constexpr int BAR_VE = BAR_VF + SV;   // [SV] V block consumed by its PV product
@@ -105,7 +104,6 @@ static_assert(BN == 128, "one S/P buffer is 128 columns, P its first 64");
 
 constexpr uint32_t TM_S = 0;    // + buf * 128
 constexpr uint32_t TM_O = 256;
-constexpr uint32_t TM_Q = 384;
 constexpr float RESCALE_LOG2 = 8.f;
 constexpr uint64_t kWaitNs = 500000000ull;   // bound on any single wait (the kernel runs for microseconds)
 constexpr uint64_t kDrainNs = 100000000ull;  // bound on draining in-flight loads after an abort
@@ -148,7 +146,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     if (tid == 0) {
         for (int i = 0; i < N_BARS; ++i) {
             uint32_t cnt = 1;
-            if (i == BAR_QT || i == BAR_P || i == BAR_P + 1 || i == BAR_EPI) cnt = 128;
+            if (i == BAR_P || i == BAR_P + 1 || i == BAR_EPI) cnt = 128;
             mbar_init(bar(i), cnt);
         }
         *abort_flag = 0;
@@ -258,10 +256,11 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         // ------------------------------------------------------------ MMA issuer (lane 0 issues)
         const uint32_t idS = idesc_bf16(128, BN, false, false);
         const uint32_t idO = idesc_bf16(128, HD, false, true);
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_QT), 0, kWaitNs));
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), 0, kWaitNs));
         // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
         // start-address field, which sits in the low bits and cannot carry out of them here
         // (every shared-memory address is below 256 KB).
+        const uint64_t q_desc = sdesc_sw128(base + OFF_Q, 16, 1024);
         const uint64_t k_desc = sdesc_sw128(base + OFF_K, 16, 1024);
         const uint64_t v_desc = sdesc_sw128(base + OFF_V, BOX_BYTES, 1024);
         // S(j) into S/P buffer j % 2, then release K(j)
@@ -274,7 +273,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
-                    mma_bf16_ts(d, tmem + TM_Q + kk * 8, kd + (off >> 4), idS, kk > 0);
+                    mma_bf16_ss(d, q_desc + (off >> 4), kd + (off >> 4), idS, kk > 0);
                 }
                 mma_commit(bar(BAR_S + (j & 1)));
                 mma_commit(bar(BAR_KE + j % SK));
@@ -316,7 +315,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         if (lane == 0) mma_commit(bar(BAR_DONE));
         __syncwarp();
     } else if (warp >= 4) {
-        // ------------------------------------------------------------ Q into TMEM, softmax, epilogue
+        // ------------------------------------------------------------ softmax, epilogue
         const int quad = warp & 3;
         const int r = quad * 32 + lane;  // row within the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -326,27 +325,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         const uint64_t anc = row_ok ? a.mask[(size_t)b * a.Kmax + node] : 0ull;
         const float sl2 = a.scale * 1.4426950408889634f;
         float m_used = -INFINITY, l_sum = 0.f;  // running max (log2 units) and row sum
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), 0, kWaitNs) && !aborted(abort_flag));
-        if (ok) {
-            // this thread's Q row: 16-byte chunk q of a 128-byte swizzled row sits at q ^ (row & 7)
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                const uint8_t* qrow = gbase + OFF_Q + h * (Q_TILE_BYTES / 2) + r * 128;
-                float w[32];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint4 v = *reinterpret_cast<const uint4*>(qrow + ((q ^ (r & 7)) << 4));
-                    w[4 * q] = __uint_as_float(v.x);
-                    w[4 * q + 1] = __uint_as_float(v.y);
-                    w[4 * q + 2] = __uint_as_float(v.z);
-                    w[4 * q + 3] = __uint_as_float(v.w);
-                }
-                tmem_st32(tmem + lane_base + TM_Q + h * 32, w);
-            }
-            tmem_wait_st();
-        }
-        tc_fence_before();
-        mbar_arrive(bar(BAR_QT));
+        bool ok = true;
         for (int j = 0; j < nb && ok; ++j) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + (j & 1)), (j >> 1) & 1, kWaitNs) &&
                                              !aborted(abort_flag));
