@@ -511,42 +511,61 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         // ------------------------------------------------------------ merge across the cluster
         // every CTA's staged rows and log2-sum-exp are complete and visible cluster-wide; this
         // CTA merges rows [r0, r1): O = sum_k 2^(lse_k - lse) O_k with lse = log2 sum_k 2^lse_k,
-        // one warp per row, four dims per lane, partials read from the other CTAs' shared memory
+        // one warp per row, four dims per lane.  A warp takes two rows at a time and issues all
+        // their distributed-shared-memory loads (every CTA's log2-sum-exp and partial row) before
+        // it uses any, so a pair of rows costs one round trip.
         cluster_sync();
         const int rows_per = (128 + ncl - 1) / ncl;
         const int r0 = c * rows_per, r1 = min(128, r0 + rows_per);
         const uint32_t stage_l = base + OFF_STAGE, lse_l = base + OFF_LSE;
-        for (int row = r0 + warp; row < r1; row += NTHREADS / 32) {
-            const int g = rb * 128 + row;
-            if (g >= a.R) continue;
-            const float lk = lane < ncl ? dsmem_ld_f32(dsmem_addr(lse_l + row * 4, (uint32_t)lane)) : -INFINITY;
-            float mx = lk;
+        constexpr int RPW = 2;     // rows per warp per round
+        constexpr int MAXCL = 8;   // portable cluster size bound (the launch checks it)
+        for (int row0 = r0 + warp * RPW; row0 < r1; row0 += (NTHREADS / 32) * RPW) {
+            float lk[RPW];
+            float4 v[RPW][MAXCL];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float wk = (lk == -INFINITY) ? 0.f : ex2(lk - mx);
-            float wsum = wk;
+            for (int q = 0; q < RPW; ++q) {
+                const int row = row0 + q;
+                const bool live = row < r1;  // uniform over the warp
+                lk[q] = (live && lane < ncl) ? dsmem_ld_f32(dsmem_addr(lse_l + row * 4, (uint32_t)lane)) : -INFINITY;
+                const uint32_t src = stage_l + row * 512 + ((lane ^ (row & 31)) << 4);
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            const uint32_t src = stage_l + row * 512 + ((lane ^ (row & 31)) << 4);
-            for (int k = 0; k < ncl; ++k) {
-                const float w = __shfl_sync(0xffffffffu, wk, k);
-                if (w == 0.f) continue;  // uniform over the warp
-                const float4 v = dsmem_ld_f32x4(dsmem_addr(src, (uint32_t)k));
-                acc.x += w * v.x;
-                acc.y += w * v.y;
-                acc.z += w * v.z;
-                acc.w += w * v.w;
+                for (int k = 0; k < MAXCL; ++k)
+                    v[q][k] = (live && k < ncl) ? dsmem_ld_f32x4(dsmem_addr(src, (uint32_t)k))
+                                                : make_float4(0.f, 0.f, 0.f, 0.f);
             }
-            const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-            const int nd = g / a.G, hh = kvh * a.G + g % a.G;
-            __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-            __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-            uint2 v;
-            v.x = *reinterpret_cast<uint32_t*>(&lo);
-            v.y = *reinterpret_cast<uint32_t*>(&hi);
-            *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.O) +
-                                      (((size_t)b * a.Kmax + nd) * a.Hq + hh) * HD + lane * 4) = v;
+#pragma unroll
+            for (int q = 0; q < RPW; ++q) {
+                const int row = row0 + q;
+                const int g = rb * 128 + row;
+                if (row >= r1 || g >= a.R) continue;  // uniform over the warp
+                float mx = lk[q];
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                const float wk = (lk[q] == -INFINITY) ? 0.f : ex2(lk[q] - mx);
+                float wsum = wk;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int k = 0; k < MAXCL; ++k) {
+                    const float w = __shfl_sync(0xffffffffu, wk, k);
+                    if (w == 0.f) continue;  // empty or absent CTA: its staged row is not used
+                    acc.x += w * v[q][k].x;
+                    acc.y += w * v[q][k].y;
+                    acc.z += w * v[q][k].z;
+                    acc.w += w * v[q][k].w;
+                }
+                const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+                const int nd = g / a.G, hh = kvh * a.G + g % a.G;
+                __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+                __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+                uint2 o2;
+                o2.x = *reinterpret_cast<uint32_t*>(&lo);
+                o2.y = *reinterpret_cast<uint32_t*>(&hi);
+                *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.O) +
+                                          (((size_t)b * a.Kmax + nd) * a.Hq + hh) * HD + lane * 4) = o2;
+            }
         }
         // no CTA leaves (and frees its shared memory) while another still reads it
         cluster_sync();
