@@ -211,6 +211,8 @@ def _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed, layer=0):
     (1, 64, 4, 5, [700], 768),                 # group 16, 80 rows: one partial tile
     (2, 12, 4, 64, [1000, 3000], 3072),        # group 3: the mma.sync path
     (3, 24, 4, 40, [0, 129, 700], 768),        # group 6, 240 rows: the mma.sync path
+    (1, 32, 8, 64, [3000], 32768),             # cache far past the prefix: chunks follow the length
+    (2, 12, 4, 64, [2500, 100], 16384),        # the same on the mma.sync path
 ])
 def test_attention_parity(B, Hq, Hkv, Kmax, Ls, Lcap):
     Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed=B * 31 + Kmax)

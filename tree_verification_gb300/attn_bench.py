@@ -1,6 +1,6 @@
 """Per-call timing of graft_tree_attention on one synthetic workload.
 
-    python -m tree_verification_gb300.attn_bench WORKLOAD [--layers N] [--reps R]
+    python -m tree_verification_gb300.attn_bench WORKLOAD [--layers N] [--reps R] [--lcap C]
 
 Builds N layers of the workload's synthetic Q / KV cache / tree KV (distinct
 buffers per layer, so repeated calls are not served from L2), captures the N
@@ -8,6 +8,9 @@ layer calls in one CUDA graph, replays it R times after a warm-up and prints
 one line: microseconds per call, the call's compulsory bytes (prefix and tree
 K/V, Q in, O out) over that time, and the device status word.  The tree mask
 is a chain (every node sees its ancestors), which does not change the work.
+--lcap sizes the KV cache for C positions instead of the workload's prefix
+plus its decode steps (the prefixes stay the same), to show that the time
+follows the prefix lengths rather than the cache capacity.
 """
 from __future__ import annotations
 
@@ -26,10 +29,11 @@ def main(argv=None):
     p.add_argument("workload", choices=sorted(synth.WORKLOADS))
     p.add_argument("--layers", type=int, default=4)
     p.add_argument("--reps", type=int, default=20)
+    p.add_argument("--lcap", type=int, default=0)
     args = p.parse_args(argv)
     wl = synth.WORKLOADS[args.workload]
     dev = torch.device("cuda")
-    Lcap = wl.lcap()
+    Lcap = max(args.lcap, wl.lcap()) if args.lcap else wl.lcap()
     L = synth.prefix_lengths(wl).to(dev)
     layers = [synth.layer_tensors(wl, l, dev, Lcap=Lcap) for l in range(args.layers)]
     chain = np.array([[(1 << (i + 1)) - 1 for i in range(wl.Kmax)]] * wl.B, dtype=np.uint64)

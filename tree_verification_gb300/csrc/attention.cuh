@@ -14,8 +14,8 @@ struct AttnArgs {
     int nRB;                      // 128-row blocks per (request, KV head)
     int tiles;                    // tcgen05 path: 128-row tiles per CTA (1 or 2)
     int cluster;                  // one-tile kernel: chunks reduced in a thread-block cluster (0: off)
-    int C;                        // prefix keys per chunk (multiple of 128)
-    int nchunk;                   // chunks per (request, KV head) allowed by Lcap
+    int C;                        // minimum prefix keys per chunk (multiple of 128)
+    int nchunk;                   // chunk CTAs per (request, KV head, row tile)
     int Lcap;
     float scale;
     const void* Q;
@@ -41,6 +41,16 @@ static __device__ __noinline__ void mark_partial(const AttnArgs& a, int b, int k
     for (int r = threadIdx.x; r < 128; r += blockDim.x) a.part_lse[base + r] = value;
 }
 
+// Prefix keys per chunk for a request of Lb keys: its keys split evenly over
+// the a.nchunk chunk CTAs in whole 128-key blocks, never fewer than a.C.  The
+// split follows each request's own length, not the cache capacity, so a cache
+// sized far beyond the current prefixes still spreads them over the SMs.
+// Chunks past ceil(Lb / chunk) hold no prefix keys.
+static __device__ __forceinline__ int chunk_len(const AttnArgs& a, int Lb) {
+    const int per = (Lb + a.nchunk - 1) / a.nchunk;
+    const int blk = (per + ATTN_TC_BLOCK_KEYS - 1) / ATTN_TC_BLOCK_KEYS * ATTN_TC_BLOCK_KEYS;
+    return blk > a.C ? blk : a.C;
+}
 // Warp-level mma.sync path: any group size; 128-row CTAs.
 int attn_mma_launch(const AttnArgs& a, cudaStream_t st);
 // tcgen05 path: group sizes dividing 128; CTAs of two 128-row tiles

@@ -17,33 +17,34 @@ struct AttnPlan {
     bool tc;
 };
 
-// Key-chunk policy: split the keys of each (request, KV head, row block)
-// into as many chunks as keep one CTA per SM busy (no partial second wave),
-// but never below kMinChunk keys so partial outputs stay a modest share of
-// the KV bytes.  Chunks are whole 128-key blocks.
+// Key-chunk policy: each (request, KV head, row block) gets as many chunk
+// CTAs as keep one CTA per SM busy (no partial second wave), but no more than
+// the cache capacity can fill with chunks of at least kMinChunk keys, so the
+// partial outputs stay a modest share of the KV bytes.  Each CTA then derives
+// its request's chunk length from the request's own key count (chunk_len in
+// attention.cuh), so the split does not depend on how far the cache capacity
+// exceeds the prefixes.
 //
 // Row blocks: on the tcgen05 path a CTA takes two 128-row tiles that share
-// every K/V block, unless that plan would leave each CTA fewer than 1024
-// keys; then one tile per CTA (twice the CTAs, a shorter prologue) does
-// better.  A single row block always goes to the two-tile kernel.
+// every K/V block, unless that plan would leave each CTA of a full-capacity
+// request fewer than 1024 keys; then one tile per CTA (twice the CTAs, a
+// shorter prologue) does better.  A single row block always goes to the
+// two-tile kernel.
 //
 // GRAFT_ATTN_CLUSTER=1 makes the chunks of a row tile (one tile per CTA,
 // split keys) run as one thread-block cluster (at most 8 CTAs, so the chunk
 // count is capped at 8) that merges its partials in distributed shared
-// memory instead of the merge kernel.  It is off by default: clusters of
-// single-SM CTAs did not all fit at once on the measured shapes and ran
-// slower than the merge kernel.
+// memory instead of the merge kernel.  It is off by default: the merge moves
+// every partial row through the SM-to-SM network, which measured slower than
+// writing the partials to L2 for the merge kernel, and clusters of 7 or 8
+// single-SM CTAs do not all fit at once.
 // GRAFT_ATTN_MIN_CHUNK and GRAFT_ATTN_TILES (1 or 2) override the policy for
 // tuning and tests; the workspace size and the launch read the same values.
-long long chunk_keys(long long Lcap, long long units, int sms, long long min_chunk) {
-    constexpr long long blk = ATTN_TC_BLOCK_KEYS;
+long long chunk_count(long long Lcap, long long units, int sms, long long min_chunk) {
     long long target = sms / units;
     if (target < 1) target = 1;
-    long long C = (Lcap + target - 1) / target;
-    C = (C + blk - 1) / blk * blk;
-    if (C < min_chunk) C = min_chunk;
-    if (C > (1LL << 30)) C = 1LL << 30;
-    return C;
+    const long long fill = Lcap > 0 ? (Lcap + min_chunk - 1) / min_chunk : 1;
+    return target < fill ? target : fill;
 }
 
 AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
@@ -60,31 +61,26 @@ AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
         const long long v = atoll(env);
         if (v >= blk) min_chunk = (v + blk - 1) / blk * blk;
     }
+    if (min_chunk > (1LL << 30)) min_chunk = 1LL << 30;
     p.tiles = 1;
     if (p.tc) {
         const long long units2 = (long long)B * Hkv * ((p.nRB + 1) / 2);
+        const long long n2 = chunk_count(Lcap, units2, sms, min_chunk);
         // with a single row block both kernels run the same grid; the two-tile kernel is quicker
-        p.tiles = (p.nRB == 1 || chunk_keys(Lcap, units2, sms, min_chunk) >= 1024) ? 2 : 1;
+        p.tiles = (p.nRB == 1 || (Lcap + n2 - 1) / n2 >= 1024) ? 2 : 1;
         if (const char* env = getenv("GRAFT_ATTN_TILES")) {
             const int v = atoi(env);
             if (v == 1 || v == 2) p.tiles = v;
         }
     }
     const long long units = (long long)B * Hkv * ((p.nRB + p.tiles - 1) / p.tiles);
-    p.C = (int)chunk_keys(Lcap, units, sms, min_chunk);
-    p.nchunk = Lcap > 0 ? (int)((Lcap + p.C - 1) / p.C) : 1;
-    if (p.nchunk < 1) p.nchunk = 1;
+    p.C = (int)min_chunk;
+    p.nchunk = (int)chunk_count(Lcap, units, sms, min_chunk);
     p.cluster = 0;
     const char* cenv = getenv("GRAFT_ATTN_CLUSTER");
     if (p.tc && p.tiles == 1 && p.nchunk > 1 && cenv && atoi(cenv) == 1) {
-        if (p.nchunk > 8) {
-            long long C = (Lcap + 7) / 8;
-            C = (C + blk - 1) / blk * blk;
-            if (C < min_chunk) C = min_chunk;
-            p.C = (int)C;
-            p.nchunk = (int)((Lcap + C - 1) / C);
-        }
-        if (p.nchunk > 1) p.cluster = p.nchunk;
+        if (p.nchunk > 8) p.nchunk = 8;
+        p.cluster = p.nchunk;
     }
     return p;
 }

@@ -88,14 +88,15 @@ attn_partial_kernel(AttnArgs a) {
         mark_partial(a, b, kvh, rb, c, -INFINITY);
         return;
     }
-    const int nck = Lb > 0 ? (Lb + a.C - 1) / a.C : 1;
+    const int Cb = chunk_len(a, Lb);
+    const int nck = Lb > 0 ? (Lb + Cb - 1) / Cb : 1;
     if (c >= nck) {
         mark_partial(a, b, kvh, rb, c, -INFINITY);
         return;
     }
     if (nck == 1) mark_partial(a, b, kvh, rb, 0, INFINITY);
-    const int k0 = c * a.C;
-    const int k1 = min(Lb, k0 + a.C);
+    const int k0 = c * Cb;
+    const int k1 = min(Lb, k0 + Cb);
     const int nb_prefix = (k1 - k0 + BN - 1) / BN;
     const bool has_tree = (c == nck - 1);
     const int nb = nb_prefix + (has_tree ? 1 : 0);

@@ -185,7 +185,8 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     }
     const int Lb = a.L[b];
     const bool bad_len = Lb < 0 || Lb > a.Lcap;
-    const int nck = (Lb > 0 && !bad_len) ? (Lb + a.C - 1) / a.C : 1;
+    const int Cb = chunk_len(a, bad_len ? 0 : Lb);
+    const int nck = (Lb > 0 && !bad_len) ? (Lb + Cb - 1) / Cb : 1;
     // A split request whose prefix leaves a chunk CTA idle gives it the tree block, so the last
     // prefix chunk does not carry one block more than the others.
     const int tree_chunk = (nck > 1 && nck < a.nchunk) ? nck : nck - 1;
@@ -197,8 +198,8 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     }
     if (nck == 1)
         for (int t = 0; t < ntile; ++t) mark_partial(a, b, kvh, rb * 2 + t, 0, INFINITY);
-    const int k0 = c * a.C;
-    const int k1 = max(k0, min(Lb, k0 + a.C));
+    const int k0 = c * Cb;
+    const int k1 = max(k0, min(Lb, k0 + Cb));
     const int nb_prefix = (k1 - k0 + BN - 1) / BN;
     const bool has_tree = (c == tree_chunk);
     const int nb = nb_prefix + (has_tree ? 1 : 0);

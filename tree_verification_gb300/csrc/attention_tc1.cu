@@ -188,7 +188,8 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     }
     const int Lb = a.L[b];
     const bool bad_len = Lb < 0 || Lb > a.Lcap;
-    const int nck = (Lb > 0 && !bad_len) ? (Lb + a.C - 1) / a.C : 1;
+    const int Cb = chunk_len(a, bad_len ? 0 : Lb);
+    const int nck = (Lb > 0 && !bad_len) ? (Lb + Cb - 1) / Cb : 1;
     // A split request whose prefix leaves a chunk CTA idle gives it the tree block, so the last
     // prefix chunk does not carry one block more than the others (not in cluster mode).
     const int tree_chunk = (ncl == 0 && nck > 1 && nck < a.nchunk) ? nck : nck - 1;
@@ -201,8 +202,8 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     if (nck == 1) mark_partial(a, b, kvh, rb, 0, INFINITY);
     // in a cluster a chunk past the request's keys stays for the merge and contributes nothing
     const bool empty = c > tree_chunk;
-    const int k0 = c * a.C;
-    const int k1 = empty ? k0 : max(k0, min(Lb, k0 + a.C));
+    const int k0 = c * Cb;
+    const int k1 = empty ? k0 : max(k0, min(Lb, k0 + Cb));
     const int nb_prefix = (k1 - k0 + BN - 1) / BN;
     const bool has_tree = !empty && (c == tree_chunk);
     const int nb = nb_prefix + (has_tree ? 1 : 0);
