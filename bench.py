@@ -279,6 +279,32 @@ def make_inputs(wl, dev, gb, synth):
     return cfg, Lcap, dl, roots, L0, M_succ, M_cnt, layers, tl
 
 
+def input_arena(seg_tensors, dev):
+    """Copies the tensors of each (key, [tensors]) segment into one device buffer, 256-byte aligned,
+    segments contiguous.  Returns the buffer, each segment's byte range and the tensors' views."""
+    import torch
+    align = lambda x: (x + 255) // 256 * 256
+    off, plan = 0, []
+    for key, ts in seg_tensors:
+        s0 = off
+        offs = []
+        for t in ts:
+            offs.append(off)
+            off = align(off + t.numel() * t.element_size())
+        plan.append((key, ts, offs, s0, off))
+    arena = torch.empty(off, dtype=torch.uint8, device=dev)
+    segs, views = {}, {}
+    for key, ts, offs, s0, s1 in plan:
+        vs = []
+        for t, o in zip(ts, offs):
+            v = arena[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+            v.copy_(t)
+            vs.append(v)
+        segs[key] = (s0, s1)
+        views[key] = vs
+    return arena, segs, views
+
+
 def attention_bytes_per_call(wl, L0) -> float:
     """Compulsory bytes of one layer call: prefix K and V, tree K and V, Q in, O out (bf16)."""
     d = wl.head_dim
@@ -303,6 +329,16 @@ def run_graft(args):
     _build.build()
     wl = synth.WORKLOADS[args.workload]
     cfg, Lcap, dl, roots, L0, M_succ, M_cnt, layers, tl = make_inputs(wl, dev, gb, synth)
+    # Every per-step input lives in one device arena, segment by segment in the order the step
+    # consumes them (drafter logits, roots and lengths; then each layer's Q and tree K/V; then the
+    # target logits), mirrored by one pinned host arena: the end-to-end step streams each segment
+    # in with one copy while earlier stages run.
+    seg_tensors = [("tree", [dl, roots, L0])] + [(l, [layers[l][0], layers[l][3], layers[l][4]])
+                                                  for l in range(wl.n_layers)] + [("accept", [tl])]
+    arena, segs, views = input_arena(seg_tensors, dev)
+    dl, roots, L0 = views["tree"]
+    tl = views["accept"][0]
+    layers = [(views[l][0], layers[l][1], layers[l][2], views[l][1], views[l][2]) for l in range(wl.n_layers)]
     Q = [x[0] for x in layers]
     step = VerifyStep(cfg, wl.B, wl.Hq, wl.Hkv, wl.n_layers, Lcap, dev, [x[1] for x in layers],
                       [x[2] for x in layers], [x[3] for x in layers], [x[4] for x in layers])
@@ -385,22 +421,38 @@ def run_graft(args):
         t_ret = timed(ret_graph, args.secondary_reps) / (args.secondary_reps * n_rep)
         t_tree = timed(tree_graph, args.secondary_reps) / (args.secondary_reps * n_rep)
 
-    # end-to-end through the public step API: pinned host inputs copied in, results read back every step
-    host = {"dl": dl, "tl": tl, "roots": roots, "L0": L0}
-    for l in range(wl.n_layers):
-        host[f"Q{l}"], host[f"Kt{l}"], host[f"Vt{l}"] = Q[l], step.Kt[l], step.Vt[l]
-    pinned = {k: v.cpu().pin_memory() for k, v in host.items()}
+    # End to end through the public step API: every step copies its inputs in from pinned host
+    # memory (one copy per segment, on a copy stream, each stage waiting only for its own segment)
+    # and reads its accepted tokens and lengths back; the whole thing is one captured graph.
+    host_arena = arena.cpu().pin_memory()
     out_host = torch.empty(wl.B, wl.Kmax, dtype=torch.int32).pin_memory()
     len_host = torch.empty(wl.B, dtype=torch.int32).pin_memory()
-    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    h2d = sum(s1 - s0 for s0, s1 in segs.values())
     d2h = out_host.numel() * 4 + len_host.numel() * 4
+    copy_stream = torch.cuda.Stream(device=dev)
+    seg_ready = {k: torch.cuda.Event() for k in segs}
 
-    def e2e_step():
-        for k, v in host.items():
-            v.copy_(pinned[k], non_blocking=True)
-        graph.replay()
+    def e2e_body():
+        main = torch.cuda.current_stream()
+        copy_stream.wait_stream(main)
+        with torch.cuda.stream(copy_stream):
+            for k, (s0, s1) in segs.items():
+                arena[s0:s1].copy_(host_arena[s0:s1], non_blocking=True)
+                seg_ready[k].record()
+        main.wait_event(seg_ready["tree"])
+        L.copy_(L0)
+        step.run(dl, roots, M_succ, M_cnt, L, Q, tl, inputs_ready=lambda k: main.wait_event(seg_ready[k]))
         out_host.copy_(step.acc["out_tok"], non_blocking=True)
         len_host.copy_(step.acc["acc_len"], non_blocking=True)
+
+    e2e_body()
+    torch.cuda.synchronize()
+    e2e_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(e2e_graph):
+        e2e_body()
+
+    def e2e_step():
+        e2e_graph.replay()
         torch.cuda.current_stream().synchronize()
 
     n_e2e = min(args.e2e_steps, args.steps)

@@ -23,7 +23,7 @@ Q / tree KV / KV caches, the cache lengths and the table M.
 from __future__ import annotations
 
 import math
-from typing import List, Optional, Sequence
+from typing import Callable, List, Optional, Sequence
 
 import torch
 
@@ -66,13 +66,27 @@ class VerifyStep:
         self.graph: Optional[torch.cuda.CUDAGraph] = None
 
     def run(self, draft_logits, root_tok, M_succ, M_cnt, L, Q: Sequence[torch.Tensor], target_logits,
-            attn_layers: Optional[Sequence[int]] = None) -> None:
-        """Enqueue one step on the current stream (asynchronous)."""
+            attn_layers: Optional[Sequence[int]] = None,
+            inputs_ready: Optional[Callable[[object], None]] = None) -> None:
+        """Enqueue one step on the current stream (asynchronous).
+
+        ``inputs_ready``, if given, is called just before each stage is enqueued, with "tree"
+        (drafter logits, root tokens, lengths), then each layer index (that layer's Q and tree
+        K/V), then "accept" (target logits), so the caller can order the stream after whatever
+        produces that stage's inputs (for example a copy on another stream) instead of waiting
+        for all of them before the step starts.
+        """
+        if inputs_ready is not None:
+            inputs_ready("tree")
         gb.graft_build_tree(self.cfg, draft_logits, root_tok, M_succ, L, out=self.tree, status=self.status,
                             ws=self.ws_tree)
         for l in (range(self.n_layers) if attn_layers is None else attn_layers):
+            if inputs_ready is not None:
+                inputs_ready(l)
             gb.graft_tree_attention(Q[l], self.Kc[l], self.Vc[l], self.Kt[l], self.Vt[l], L, self.tree["mask"],
                                     self.scale, O=self.O, status=self.status, ws=self.ws_attn)
+        if inputs_ready is not None:
+            inputs_ready("accept")
         if self.temperature > 0.0:
             gb.graft_sample_tokens(target_logits, self.tree["pos"], self.temperature, self.seed,
                                    sampled=self.acc["argmax"], ws=self.ws_smp)
