@@ -35,6 +35,7 @@ if ROOT not in sys.path:
 METRIC = "tree-verify steps/s; tree-attention HBM GB/s vs GB300 peak; retrieval fill µs"
 UNIT = "steps/s"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 ATTN_SOURCES = ["attention_tc.cu", "attention_tc1.cu", "attention_mma.cu", "attention.cuh", "attention_api.cu",
                 "tc_ptx.cuh", "common.cuh"]
 
@@ -124,6 +125,49 @@ def measured_peaks():
         return float(j["hbm_gbs"]), "measured"
     except (OSError, ValueError, KeyError):
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peak():
+    """Dense bf16 TFLOP/s as a burst (the attention call is timed on its own)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["bf16_tflops"]), "measured"
+    except (OSError, ValueError, KeyError):
+        return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+# exp2 results per clock per SM of the special-function unit (four per SM sub-partition)
+EX2_PER_CLOCK_PER_SM = 16
+
+
+def attention_roofline(wl, L0, t_call, clocks, sms):
+    """The three ideal times of one attention call and the fraction of each that the call achieves:
+    HBM (compulsory bytes), tensor cores (4 Hq Kmax 128 sum L flops of the prefix part) and the
+    exponential unit (Hq Kmax sum L exp2).  The bound is whichever of HBM and tensor is longer."""
+    nbytes = attention_bytes_per_call(wl, L0)
+    sum_l = int(L0.sum())
+    flops = 4.0 * wl.Hq * wl.Kmax * wl.head_dim * sum_l
+    ex2 = float(wl.Hq * wl.Kmax * sum_l)
+    hbm, hbm_kind = measured_peaks()
+    tc, tc_kind = measured_tensor_peak()
+    mhz = (clocks or {}).get("sm_mhz") or 2070.0
+    sfu = EX2_PER_CLOCK_PER_SM * sms * mhz * 1e6
+    t_hbm, t_tc, t_sfu = nbytes / (hbm * 1e9), flops / (tc * 1e12), ex2 / sfu
+    fractions = {"hbm": t_hbm / t_call, "tensor": t_tc / t_call, "sfu": t_sfu / t_call}
+    if t_tc > t_hbm:
+        r = {"bound": "tensor", "achieved": flops / t_call / 1e12, "peak": tc, "unit": "TFLOP/s",
+             "peak_source": f"{tc_kind} bf16_tflops"}
+    else:
+        r = {"bound": "hbm", "achieved": nbytes / t_call / 1e9, "peak": hbm, "unit": "GB/s",
+             "peak_source": f"{hbm_kind} hbm_gbs"}
+    r["frac"] = r["achieved"] / r["peak"]
+    r["fractions"] = fractions
+    r["fractions_basis"] = (f"ideal time over the call's time: compulsory bytes at {hbm:.0f} GB/s, prefix flops at "
+                            f"{tc:.0f} TFLOP/s, exp2 at {EX2_PER_CLOCK_PER_SM}/clock/SM x {sms} SMs x {mhz:.0f} MHz")
+    r["bytes_per_call"], r["flops_per_call"], r["ex2_per_call"] = nbytes, flops, ex2
+    return r
 
 
 def attn_source_hash() -> str:
@@ -388,6 +432,19 @@ def run_graft(args):
         e.synchronize()
         return s.elapsed_time(e) / 1000.0
 
+    def timed_steps(g, reps):
+        """Total seconds of reps back-to-back replays, and each replay's milliseconds (an event
+        before every replay and one after the last)."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+        torch.cuda.synchronize()
+        for i in range(reps):
+            ev[i].record()
+            g.replay()
+        ev[reps].record()
+        ev[reps].synchronize()
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
+        return ev[0].elapsed_time(ev[reps]) / 1000.0, per
+
     for _ in range(max(3, args.warmup)):
         graph.replay()
     torch.cuda.synchronize()
@@ -401,7 +458,7 @@ def run_graft(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    t_main = timed(graph, args.steps)
+    t_main, per_step_ms = timed_steps(graph, args.steps)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -516,6 +573,9 @@ def run_graft(args):
     peak, peak_kind = measured_peaks()
     achieved = bytes_call / t_attn / 1e9
     traffic = recorded_traffic(args.workload)
+    roof = attention_roofline(wl, L0.cpu(), t_attn, clocks, torch.cuda.get_device_properties(dev).multi_processor_count)
+    roof.update({"traffic": traffic, "kernel": "graft_tree_attention (one layer call)", "call_us": t_attn * 1e6})
+    q = statistics.quantiles(per_step_ms, n=10) if len(per_step_ms) >= 10 else [float("nan")] * 9
     result = {
         "metric": METRIC, "value": world * args.steps / t_max, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1000.0 * t_max / args.steps, "higher_is_better": True,
@@ -527,10 +587,8 @@ def run_graft(args):
                          f"per step in distinct per-layer buffers",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "accumulate": "fp32"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": traffic, "kernel": "graft_tree_attention (one layer call)",
-                     "peak_source": f"{peak_kind} hbm_gbs", "bytes_per_call": bytes_call,
-                     "call_us": t_attn * 1e6},
+        "roofline": roof,
+        "step_ms": {"median": statistics.median(per_step_ms), "p10": q[0], "p90": q[8]},
         "e2e": {"value": world * n_e2e / t_e2e if n_e2e > 0 else None, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
