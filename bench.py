@@ -569,6 +569,20 @@ def run_graft(args):
         sample_from_logits = {"us": t_st * 1e6, "gbs": tl.numel() * 4 / t_st / 1e9}
         del H, W_lm
 
+    # attention alone on the other workloads' shapes (the long-context and batched configurations
+    # carry the HBM target), four distinct layers per replay so every call streams from DRAM
+    attn_other = {}
+    if args.secondary_reps > 0 and world == 1:
+        from tree_verification_gb300 import attn_bench
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        for name in ("llama31_8b_long", "qwen3_8b_batch", "qwen3_235b"):
+            owl = synth.WORKLOADS[name]
+            us, nb, st = attn_bench.time_calls(owl, 4, 10, dev=dev)
+            r = attention_roofline(owl, synth.prefix_lengths(owl), us * 1e-6, clocks, sms)
+            attn_other[name] = {"call_us": us, "gbs": nb / us / 1e3, "bound": r["bound"], "frac": r["frac"],
+                                "fractions": r["fractions"], "status": st}
+        torch.cuda.empty_cache()
+
     bytes_call = attention_bytes_per_call(wl, L0.cpu())
     peak, peak_kind = measured_peaks()
     achieved = bytes_call / t_attn / 1e9
@@ -595,7 +609,8 @@ def run_graft(args):
         "secondary": {"tree_attention_gbs": achieved, "tree_attention_frac_of_peak": achieved / peak,
                       "retrieval_fill_us": t_ret * 1e6, "build_tree_us": t_tree * 1e6,
                       "launches_per_step": launches_per_step, "device_status": status,
-                      "lm_head_argmax": lmh, "sample_tokens_from_logits": sample_from_logits},
+                      "lm_head_argmax": lmh, "sample_tokens_from_logits": sample_from_logits,
+                      "attention_other_workloads": attn_other},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         inputs = (dl, tl, roots, L0, M_succ, M_cnt, layers[0])
