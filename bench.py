@@ -36,7 +36,8 @@ METRIC = "tree-verify steps/s; tree-attention HBM GB/s vs GB300 peak; retrieval 
 UNIT = "steps/s"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-ATTN_SOURCES = ["attention_tc.cu", "attention_tc1.cu", "attention_mma.cu", "attention.cuh", "attention_api.cu",
+ATTN_SOURCES = ["attention_tc.cu", "attention_tcp.cu", "attention_tc1.cu", "attention_mma.cu", "attention.cuh",
+                "attention_api.cu",
                 "tc_ptx.cuh", "common.cuh"]
 
 

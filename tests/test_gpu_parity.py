@@ -250,6 +250,41 @@ def test_attention_parity_tilings_chunkings(monkeypatch, tiles, cluster, min_chu
     assert_attention_close(to_np(O), ref)
 
 
+@pytest.mark.parametrize("ctas", ["1", "3", "7"])
+@pytest.mark.parametrize("min_chunk", ["256", "1000000"])
+@pytest.mark.parametrize("B,Hq,Hkv,Kmax,Ls,Lcap", [
+    (5, 32, 8, 64, [4096, 0, 777, 1, 2300], 4160),   # empty and one-key prefixes, ragged tails
+    (3, 16, 2, 48, [1500, 300, 129], 1536),          # 384 rows: a partial second tile
+    (2, 64, 4, 64, [2000, 63], 2048),                # group 16: four tile pairs per KV head
+])
+def test_attention_parity_persistent(monkeypatch, ctas, min_chunk, B, Hq, Hkv, Kmax, Ls, Lcap):
+    """The persistent two-tile kernel with a few CTAs, so each runs many work items back to back
+    (direct rows and split-key partials, items that skip, items of a request past its keys)."""
+    monkeypatch.setenv("GRAFT_ATTN_TILES", "2")
+    monkeypatch.setenv("GRAFT_ATTN_PERSIST_CTAS", ctas)
+    monkeypatch.setenv("GRAFT_ATTN_MIN_CHUNK", min_chunk)
+    Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed=11 * B + Kmax)
+    status = _status()
+    O = gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), torch.from_numpy(masks.view(np.int64)).to(DEV),
+                                  1 / math.sqrt(128), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oatt.tree_attention(to_np(Q), to_np(Kc), to_np(Vc), to_np(Kt), to_np(Vt), L.numpy(), masks,
+                              1 / math.sqrt(128))
+    assert_attention_close(to_np(O), ref)
+
+
+def test_attention_persistent_length_past_capacity_is_flagged(monkeypatch):
+    monkeypatch.setenv("GRAFT_ATTN_TILES", "2")
+    monkeypatch.setenv("GRAFT_ATTN_PERSIST_CTAS", "2")
+    Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(2, 32, 8, 64, [700, 100], 640, seed=3)
+    status = _status()
+    gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), torch.from_numpy(masks.view(np.int64)).to(DEV), 0.1,
+                              status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & gb().STATUS_LENGTH
+
+
 def test_attention_length_past_capacity_is_flagged():
     Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(1, 8, 2, 32, [700], 640, seed=3)
     status = _status()

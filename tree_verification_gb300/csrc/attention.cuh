@@ -58,6 +58,10 @@ int attn_mma_launch(const AttnArgs& a, cudaStream_t st);
 bool attn_tc_supported(int G);
 int attn_tc_launch(const AttnArgs& a, cudaStream_t st);
 int attn_tc1_launch(const AttnArgs& a, cudaStream_t st);
+// Persistent two-tile kernel (attention_tcp.cu): the work items of the two-tile grid (nRB even)
+// dealt to `ctas` CTAs that run theirs back to back; then the merge, as attn_tc_launch.
+int attn_tcp_items(const AttnArgs& a);
+int attn_tcp_launch(const AttnArgs& a, int ctas, cudaStream_t st);
 // Merges split-key partials (no-op when every request fits one chunk or a
 // cluster reduced them).
 int attn_combine_launch(const AttnArgs& a, cudaStream_t st);

@@ -14,6 +14,7 @@ namespace {
 
 struct AttnPlan {
     int G, R, nRB, C, nchunk, tiles, cluster;
+    int persist;  // > 0: CTAs of the persistent two-tile kernel
     bool tc;
 };
 
@@ -38,6 +39,12 @@ struct AttnPlan {
 // every partial row through the SM-to-SM network, which measured slower than
 // writing the partials to L2 for the merge kernel, and clusters of 7 or 8
 // single-SM CTAs do not all fit at once.
+// Persistence: when the two-tile grid would need more than one wave (more
+// work items than SMs) and the row tiles pair up (an even tile count), one
+// CTA per SM runs the items back to back (attention_tcp.cu), which hides each
+// item's start and finish behind its neighbours and deals items of
+// decreasing length evenly.  GRAFT_ATTN_PERSIST=0 turns this off;
+// GRAFT_ATTN_PERSIST_CTAS=n forces it with n CTAs (tests).
 // GRAFT_ATTN_MIN_CHUNK and GRAFT_ATTN_TILES (1 or 2) override the policy for
 // tuning and tests; the workspace size and the launch read the same values.
 long long chunk_count(long long Lcap, long long units, int sms, long long min_chunk) {
@@ -81,6 +88,16 @@ AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
     if (p.tc && p.tiles == 1 && p.nchunk > 1 && cenv && atoi(cenv) == 1) {
         if (p.nchunk > 8) p.nchunk = 8;
         p.cluster = p.nchunk;
+    }
+    p.persist = 0;
+    if (p.tc && p.tiles == 2 && p.nRB % 2 == 0 && p.cluster == 0) {
+        const long long items = (long long)B * p.nchunk * Hkv * (p.nRB / 2);
+        const char* penv = getenv("GRAFT_ATTN_PERSIST");
+        const char* cnt = getenv("GRAFT_ATTN_PERSIST_CTAS");
+        if (cnt && atoi(cnt) > 0)
+            p.persist = (int)(items < atoi(cnt) ? items : atoi(cnt));
+        else if (items > sms && !(penv && atoi(penv) == 0))
+            p.persist = sms;
     }
     return p;
 }
@@ -165,6 +182,7 @@ extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Km
     a.status = status;
     attn_ws(p, B, Hkv, &a, ws);
     if ((long long)p.nRB * Hkv > 65535LL || p.nchunk > 65535) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    if (p.persist > 0) return attn_tcp_launch(a, p.persist, (cudaStream_t)stream);
     if (p.tc) return p.tiles == 2 ? attn_tc_launch(a, (cudaStream_t)stream) : attn_tc1_launch(a, (cudaStream_t)stream);
     return attn_mma_launch(a, (cudaStream_t)stream);
 }
