@@ -182,7 +182,9 @@ extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Km
     a.status = status;
     attn_ws(p, B, Hkv, &a, ws);
     if ((long long)p.nRB * Hkv > 65535LL || p.nchunk > 65535) return GRAFT_ERR_UNSUPPORTED_SHAPE;
-    if (p.persist > 0) return attn_tcp_launch(a, p.persist, (cudaStream_t)stream);
+    // the persistent kernel stores output rows in 32-byte pieces
+    if (p.persist > 0 && (reinterpret_cast<uintptr_t>(O) & 31) == 0)
+        return attn_tcp_launch(a, p.persist, (cudaStream_t)stream);
     if (p.tc) return p.tiles == 2 ? attn_tc_launch(a, (cudaStream_t)stream) : attn_tc1_launch(a, (cudaStream_t)stream);
     return attn_mma_launch(a, (cudaStream_t)stream);
 }

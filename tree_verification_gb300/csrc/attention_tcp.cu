@@ -98,6 +98,14 @@ __device__ __forceinline__ void raise_abort(volatile uint32_t* flag, int32_t* st
     flag_status(status, GRAFT_STATUS_TIMEOUT);
 }
 
+// 32-byte store (eight 32-bit words) to a 32-byte aligned global address: a warp's 32 rows fill
+// whole 32-byte sectors per instruction
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]), "r"(w[1]),
+                 "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
 // One work item: both tiles of row pair rb of (request b, KV head kvh) against key chunk c.
 struct Item {
     int b, kvh, rb, c;
@@ -539,23 +547,23 @@ attn_tcp_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 if (!row_ok) continue;
                 if (it.direct) {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 8) {
-                        uint4 v;
-                        __nv_bfloat162 x0 = __floats2bfloat162_rn(o[x] * inv, o[x + 1] * inv);
-                        __nv_bfloat162 x1 = __floats2bfloat162_rn(o[x + 2] * inv, o[x + 3] * inv);
-                        __nv_bfloat162 x2 = __floats2bfloat162_rn(o[x + 4] * inv, o[x + 5] * inv);
-                        __nv_bfloat162 x3 = __floats2bfloat162_rn(o[x + 6] * inv, o[x + 7] * inv);
-                        v.x = *reinterpret_cast<uint32_t*>(&x0);
-                        v.y = *reinterpret_cast<uint32_t*>(&x1);
-                        v.z = *reinterpret_cast<uint32_t*>(&x2);
-                        v.w = *reinterpret_cast<uint32_t*>(&x3);
-                        *reinterpret_cast<uint4*>(orow + c0 + x) = v;
+                    for (int x = 0; x < 32; x += 16) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int y = 0; y < 8; ++y) {
+                            __nv_bfloat162 h2 = __floats2bfloat162_rn(o[x + 2 * y] * inv, o[x + 2 * y + 1] * inv);
+                            w[y] = *reinterpret_cast<uint32_t*>(&h2);
+                        }
+                        st_global_v8(orow + c0 + x, w);  // O rows start 32-byte aligned (the launch checks O)
                     }
                 } else {
 #pragma unroll
-                    for (int x = 0; x < 32; x += 4)
-                        *reinterpret_cast<float4*>(prow + c0 + x) =
-                            make_float4(o[x] * inv, o[x + 1] * inv, o[x + 2] * inv, o[x + 3] * inv);
+                    for (int x = 0; x < 32; x += 8) {
+                        uint32_t w[8];
+#pragma unroll
+                        for (int y = 0; y < 8; ++y) w[y] = __float_as_uint(o[x + y] * inv);
+                        st_global_v8(prow + c0 + x, w);
+                    }
                 }
             }
             if (!it.direct && row_ok) a.part_lse[pbase + r] = m_used + log2f(l_sum);
