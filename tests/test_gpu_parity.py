@@ -256,6 +256,8 @@ def test_attention_parity_tilings_chunkings(monkeypatch, tiles, cluster, min_chu
     (5, 32, 8, 64, [4096, 0, 777, 1, 2300], 4160),   # empty and one-key prefixes, ragged tails
     (3, 16, 2, 48, [1500, 300, 129], 1536),          # 384 rows: a partial second tile
     (2, 64, 4, 64, [2000, 63], 2048),                # group 16: four tile pairs per KV head
+    (1, 8, 2, 64, [1000], 1024),                     # a single request: no length ranking
+    (300, 8, 2, 64, [(37 * b) % 400 for b in range(300)], 400),  # more requests than the ranking table
 ])
 def test_attention_parity_persistent(monkeypatch, ctas, min_chunk, B, Hq, Hkv, Kmax, Ls, Lcap):
     """The persistent two-tile kernel with a few CTAs, so each runs many work items back to back
