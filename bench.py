@@ -63,6 +63,17 @@ def dist_env():
     return world, rank, local
 
 
+def slowest_over_ranks(seconds: float, device, world: int) -> float:
+    """The longest of every rank's time (the job's time for weak-scaled replicas)."""
+    if world <= 1:
+        return seconds
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason samples taken while the timed region runs."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -464,11 +475,7 @@ def run_graft(args):
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
-    t_max = t_main
-    if world > 1:
-        t = torch.tensor([t_main], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_max = float(t.item())
+    t_max = slowest_over_ranks(t_main, dev, world)
     status = int(step.status.item())
 
     # secondary timings (after the main timed region)
@@ -522,10 +529,7 @@ def run_graft(args):
         for _ in range(n_e2e):
             e2e_step()
         t_e2e = time.perf_counter() - t0
-    if world > 1:
-        t = torch.tensor([t_e2e], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        t_e2e = float(t.item())
+    t_e2e = slowest_over_ranks(t_e2e, dev, world)
 
     # the fused lm_head argmax (greedy tokens straight from final hidden states) on this workload's rows
     lmh = sample_from_logits = None
