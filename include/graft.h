@@ -205,6 +205,47 @@ int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Kmax, const v
                          graft_stream_t stream);
 
 /*
+ * GraftAttnTuning — explicit overrides of graft_tree_attention's launch plan
+ * (host struct, passed by pointer; NULL or an all-zero struct keeps the
+ * default plan).  The default plan depends only on the call's shape and the
+ * current device's SM count; these fields let tests drive every kernel
+ * variant on small shapes and let tuning runs compare plans.  The result is
+ * the same attention whatever the plan (up to float32 summation order).
+ *
+ *   tiles         0 = default; 1 or 2 = 128-row query tiles per CTA on the
+ *                 tensor-core path (group sizes dividing 128)
+ *   min_chunk     0 = default (256); else the fewest prefix keys a key chunk
+ *                 may hold (rounded up to whole 128-key blocks): large values
+ *                 give one chunk per request
+ *   persist_ctas  0 = default (the persistent two-tile kernel with one CTA
+ *                 per SM when the two-tile grid exceeds one wave); -1 = never
+ *                 persistent; n > 0 = persistent with min(n, work items) CTAs
+ *                 whenever the two-tile kernel runs with an even tile count
+ *   reserved      must be zero
+ *
+ * graft_tree_attention_workspace_size_ex / graft_tree_attention_ex take the
+ * same arguments as the plain entry points plus `tuning`; a workspace must be
+ * sized with the same tuning it is used with.  Invalid fields return
+ * GRAFT_ERR_INVALID_ARG.
+ */
+typedef struct GraftAttnTuning {
+    int32_t tiles;
+    int32_t min_chunk;
+    int32_t persist_ctas;
+    int32_t reserved[5];
+} GraftAttnTuning;
+
+int graft_tree_attention_workspace_size_ex(int B, int Hq, int Hkv, int head_dim, int Kmax,
+                                           int64_t Lcap, const GraftAttnTuning* tuning,
+                                           size_t* bytes);
+int graft_tree_attention_ex(int B, int Hq, int Hkv, int head_dim, int Kmax, const void* Q,
+                            const void* Kc, const void* Vc, int64_t Lcap, const void* Kt,
+                            const void* Vt, const int32_t* L, const uint64_t* tree_mask,
+                            float scale, void* O, int32_t* status,
+                            const GraftAttnTuning* tuning, void* ws, size_t ws_bytes,
+                            graft_stream_t stream);
+
+/*
  * graft_accept_compact — greedy lossless acceptance and KV compaction
  * (Graft article, architecture paragraph: retrieved nodes are ordinary
  * proposals and the final distribution stays lossless).
@@ -356,7 +397,10 @@ int graft_update_M_emitted(int32_t* M_succ, int32_t* M_cnt, int V, int W, int B,
  * GRAFT_ERR_UNSUPPORTED_SHAPE and enqueues nothing.  The call allocates and
  * frees nothing.  Its first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  All calls on a device share the array
+ * call before any stream capture.  The address is kept for the life of the
+ * process, so resetting a device (cudaDeviceReset) after that first call is
+ * not supported.  Device ordinals 0 to 63 are supported; a current device
+ * beyond them returns GRAFT_ERR_UNSUPPORTED_SHAPE.  All calls on a device share the array
  * (each call clears the parts it reads), so calls that may run at the same
  * time on the GPU — different streams with no ordering between them — race
  * and corrupt each other's result: order them on one stream or with events.

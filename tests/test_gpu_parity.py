@@ -226,23 +226,20 @@ def test_attention_parity(B, Hq, Hkv, Kmax, Ls, Lcap):
     assert_attention_close(to_np(O), ref)
 
 
-@pytest.mark.parametrize("tiles,cluster", [("1", "0"), ("1", "1"), ("2", "1")])
-@pytest.mark.parametrize("min_chunk", ["128", "384", "1000000"])
+@pytest.mark.parametrize("tiles", [1, 2])
+@pytest.mark.parametrize("min_chunk", [128, 384, 1000000])
 @pytest.mark.parametrize("B,Hq,Hkv,Kmax,Ls,Lcap", [
     (2, 32, 8, 64, [4096, 777], 4160),
     (3, 16, 2, 48, [0, 1500, 300], 1536),      # three tiles: the last CTA pair has one
 ])
-def test_attention_parity_tilings_chunkings(monkeypatch, tiles, cluster, min_chunk, B, Hq, Hkv, Kmax, Ls, Lcap):
-    """Both tcgen05 kernels (one and two 128-row tiles per CTA; the one-tile kernel with its split-key
-    partials merged by the merge kernel or inside a cluster) with key chunks of one block, of three
-    blocks, and one chunk per request."""
-    monkeypatch.setenv("GRAFT_ATTN_TILES", tiles)
-    monkeypatch.setenv("GRAFT_ATTN_CLUSTER", cluster)
-    monkeypatch.setenv("GRAFT_ATTN_MIN_CHUNK", min_chunk)
+def test_attention_parity_tilings_chunkings(tiles, min_chunk, B, Hq, Hkv, Kmax, Ls, Lcap):
+    """Both tcgen05 kernels (one and two 128-row tiles per CTA, split-key partials merged by the merge
+    kernel) with key chunks of one block, of three blocks, and one chunk per request."""
+    tuning = dict(tiles=tiles, min_chunk=min_chunk, persist_ctas=-1)
     Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed=7 * B + Kmax)
     status = _status()
     O = gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), torch.from_numpy(masks.view(np.int64)).to(DEV),
-                                  1 / math.sqrt(128), status=status)
+                                  1 / math.sqrt(128), status=status, tuning=tuning)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     ref = oatt.tree_attention(to_np(Q), to_np(Kc), to_np(Vc), to_np(Kt), to_np(Vt), L.numpy(), masks,
@@ -250,8 +247,8 @@ def test_attention_parity_tilings_chunkings(monkeypatch, tiles, cluster, min_chu
     assert_attention_close(to_np(O), ref)
 
 
-@pytest.mark.parametrize("ctas", ["1", "3", "7"])
-@pytest.mark.parametrize("min_chunk", ["256", "1000000"])
+@pytest.mark.parametrize("ctas", [1, 3, 7])
+@pytest.mark.parametrize("min_chunk", [256, 1000000])
 @pytest.mark.parametrize("B,Hq,Hkv,Kmax,Ls,Lcap", [
     (5, 32, 8, 64, [4096, 0, 777, 1, 2300], 4160),   # empty and one-key prefixes, ragged tails
     (3, 16, 2, 48, [1500, 300, 129], 1536),          # 384 rows: a partial second tile
@@ -259,16 +256,14 @@ def test_attention_parity_tilings_chunkings(monkeypatch, tiles, cluster, min_chu
     (1, 8, 2, 64, [1000], 1024),                     # a single request: no length ranking
     (300, 8, 2, 64, [(37 * b) % 400 for b in range(300)], 400),  # more requests than the ranking table
 ])
-def test_attention_parity_persistent(monkeypatch, ctas, min_chunk, B, Hq, Hkv, Kmax, Ls, Lcap):
+def test_attention_parity_persistent(ctas, min_chunk, B, Hq, Hkv, Kmax, Ls, Lcap):
     """The persistent two-tile kernel with a few CTAs, so each runs many work items back to back
     (direct rows and split-key partials, items that skip, items of a request past its keys)."""
-    monkeypatch.setenv("GRAFT_ATTN_TILES", "2")
-    monkeypatch.setenv("GRAFT_ATTN_PERSIST_CTAS", ctas)
-    monkeypatch.setenv("GRAFT_ATTN_MIN_CHUNK", min_chunk)
+    tuning = dict(tiles=2, persist_ctas=ctas, min_chunk=min_chunk)
     Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed=11 * B + Kmax)
     status = _status()
     O = gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), torch.from_numpy(masks.view(np.int64)).to(DEV),
-                                  1 / math.sqrt(128), status=status)
+                                  1 / math.sqrt(128), status=status, tuning=tuning)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     ref = oatt.tree_attention(to_np(Q), to_np(Kc), to_np(Vc), to_np(Kt), to_np(Vt), L.numpy(), masks,
@@ -276,13 +271,11 @@ def test_attention_parity_persistent(monkeypatch, ctas, min_chunk, B, Hq, Hkv, K
     assert_attention_close(to_np(O), ref)
 
 
-def test_attention_persistent_length_past_capacity_is_flagged(monkeypatch):
-    monkeypatch.setenv("GRAFT_ATTN_TILES", "2")
-    monkeypatch.setenv("GRAFT_ATTN_PERSIST_CTAS", "2")
+def test_attention_persistent_length_past_capacity_is_flagged():
     Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(2, 32, 8, 64, [700, 100], 640, seed=3)
     status = _status()
     gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), torch.from_numpy(masks.view(np.int64)).to(DEV), 0.1,
-                              status=status)
+                              status=status, tuning=dict(tiles=2, persist_ctas=2))
     torch.cuda.synchronize()
     assert int(status.item()) & gb().STATUS_LENGTH
 

@@ -52,6 +52,13 @@ class GraftConfig(ctypes.Structure):
                     tmpl_rank=list(self.tmpl_rank[: self.n_tmpl]))
 
 
+class GraftAttnTuning(ctypes.Structure):
+    """Mirror of the C struct GraftAttnTuning (graft.h): explicit launch-plan overrides of the tree
+    attention (0 in a field keeps the default plan)."""
+    _fields_ = [("tiles", ctypes.c_int32), ("min_chunk", ctypes.c_int32), ("persist_ctas", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 5)]
+
+
 class GraftError(RuntimeError):
     pass
 
@@ -73,6 +80,10 @@ _SIGNATURES = {
     "graft_tree_attention_workspace_size": [_I, _I, _I, _I, _I, _I64, ctypes.POINTER(_SZ)],
     "graft_tree_attention": [_I, _I, _I, _I, _I, _P, _P, _P, _I64, _P, _P, _P, _P, ctypes.c_float, _P, _P, _P,
                              _SZ, _P],
+    "graft_tree_attention_workspace_size_ex": [_I, _I, _I, _I, _I, _I64, ctypes.POINTER(GraftAttnTuning),
+                                               ctypes.POINTER(_SZ)],
+    "graft_tree_attention_ex": [_I, _I, _I, _I, _I, _P, _P, _P, _I64, _P, _P, _P, _P, ctypes.c_float, _P, _P,
+                                ctypes.POINTER(GraftAttnTuning), _P, _SZ, _P],
     "graft_accept_compact_workspace_size": [_I, _I, _I, ctypes.POINTER(_SZ)],
     "graft_accept_compact": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I64, _P, _P, _P, _P, _P, _P,
                              _P, _P, _SZ, _P],
@@ -214,15 +225,33 @@ def graft_retrieve(cfg: GraftConfig, root_tok, M_succ, ret_tok=None, status=None
     return ret_tok
 
 
-def graft_tree_attention_workspace_size(B: int, Hq: int, Hkv: int, Kmax: int, Lcap: int) -> int:
+def _tuning(tuning) -> Optional["GraftAttnTuning"]:
+    if tuning is None or isinstance(tuning, GraftAttnTuning):
+        return tuning
+    t = GraftAttnTuning()
+    for k, v in dict(tuning).items():
+        setattr(t, k, int(v))
+    return t
+
+
+def graft_tree_attention_workspace_size(B: int, Hq: int, Hkv: int, Kmax: int, Lcap: int, tuning=None) -> int:
+    """Workspace bytes of graft_tree_attention; ``tuning`` (a GraftAttnTuning or a dict of its fields)
+    selects graft_tree_attention_workspace_size_ex."""
     n = _SZ()
-    _check(lib().graft_tree_attention_workspace_size(B, Hq, Hkv, HEAD_DIM, Kmax, Lcap, ctypes.byref(n)),
-           "workspace size")
+    t = _tuning(tuning)
+    if t is None:
+        rc = lib().graft_tree_attention_workspace_size(B, Hq, Hkv, HEAD_DIM, Kmax, Lcap, ctypes.byref(n))
+    else:
+        rc = lib().graft_tree_attention_workspace_size_ex(B, Hq, Hkv, HEAD_DIM, Kmax, Lcap, ctypes.byref(t),
+                                                          ctypes.byref(n))
+    _check(rc, "workspace size")
     return n.value
 
 
 def graft_tree_attention(Q, Kc, Vc, Kt, Vt, L, tree_mask, scale: float, O=None, status=None, ws=None,
-                         stream=None):
+                         stream=None, tuning=None):
+    """Tree attention of one layer; ``tuning`` (a GraftAttnTuning or a dict of its fields) selects
+    graft_tree_attention_ex with that launch plan."""
     B, Kmax, Hq, d = Q.shape
     Lcap, Hkv = Kc.shape[1], Kc.shape[2]
     _need(Q, "Q", torch.bfloat16)
@@ -235,10 +264,15 @@ def graft_tree_attention(Q, Kc, Vc, Kt, Vt, L, tree_mask, scale: float, O=None, 
     if O is None:
         O = torch.empty_like(Q)
     _need(O, "O", torch.bfloat16, Q.shape)
-    ws, nws = _ws(graft_tree_attention_workspace_size(B, Hq, Hkv, Kmax, Lcap), Q.device, ws)
-    _check(lib().graft_tree_attention(B, Hq, Hkv, d, Kmax, _ptr(Q), _ptr(Kc), _ptr(Vc), Lcap, _ptr(Kt), _ptr(Vt),
-                                      _ptr(L), _ptr(tree_mask), float(scale), _ptr(O), _ptr(status), _ptr(ws), nws,
-                                      _stream(stream)), "graft_tree_attention")
+    t = _tuning(tuning)
+    ws, nws = _ws(graft_tree_attention_workspace_size(B, Hq, Hkv, Kmax, Lcap, t), Q.device, ws)
+    args = (B, Hq, Hkv, d, Kmax, _ptr(Q), _ptr(Kc), _ptr(Vc), Lcap, _ptr(Kt), _ptr(Vt), _ptr(L), _ptr(tree_mask),
+            float(scale), _ptr(O), _ptr(status))
+    if t is None:
+        rc = lib().graft_tree_attention(*args, _ptr(ws), nws, _stream(stream))
+    else:
+        rc = lib().graft_tree_attention_ex(*args, ctypes.byref(t), _ptr(ws), nws, _stream(stream))
+    _check(rc, "graft_tree_attention")
     return O
 
 

@@ -13,7 +13,6 @@ struct AttnArgs {
     int B, Hq, Hkv, G, Kmax, R;  // R = Kmax * G query rows per (request, KV head)
     int nRB;                      // 128-row blocks per (request, KV head)
     int tiles;                    // tcgen05 path: 128-row tiles per CTA (1 or 2)
-    int cluster;                  // one-tile kernel: chunks reduced in a thread-block cluster (0: off)
     int C;                        // minimum prefix keys per chunk (multiple of 128)
     int nchunk;                   // chunk CTAs per (request, KV head, row tile)
     int Lcap;
@@ -36,7 +35,7 @@ struct AttnArgs {
 // for chunk 0 of a request that fits one chunk (its output was written
 // directly, so the merge leaves the rows alone).  No-op without partials.
 static __device__ __noinline__ void mark_partial(const AttnArgs& a, int b, int kvh, int tile, int c, float value) {
-    if (a.nchunk <= 1 || a.part_lse == nullptr || a.cluster > 0 || tile >= a.nRB) return;
+    if (a.nchunk <= 1 || a.part_lse == nullptr || tile >= a.nRB) return;
     const size_t base = ((((size_t)b * a.Hkv + kvh) * a.nRB + tile) * a.nchunk + c) * 128;
     for (int r = threadIdx.x; r < 128; r += blockDim.x) a.part_lse[base + r] = value;
 }
@@ -62,8 +61,7 @@ int attn_tc1_launch(const AttnArgs& a, cudaStream_t st);
 // dealt to `ctas` CTAs that run theirs back to back; then the merge, as attn_tc_launch.
 int attn_tcp_items(const AttnArgs& a);
 int attn_tcp_launch(const AttnArgs& a, int ctas, cudaStream_t st);
-// Merges split-key partials (no-op when every request fits one chunk or a
-// cluster reduced them).
+// Merges split-key partials (no-op when every request fits one chunk).
 int attn_combine_launch(const AttnArgs& a, cudaStream_t st);
 
 }  // namespace graft

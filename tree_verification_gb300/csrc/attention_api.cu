@@ -4,8 +4,6 @@
 // CTAs is about the device's SM count (small batches, long prefixes) while
 // each chunk stays long enough that partial outputs are a small fraction of
 // the KV bytes read.  The same policy sizes the workspace.
-#include <cstdlib>
-
 #include "attention.cuh"
 #include "common.cuh"
 
@@ -13,7 +11,7 @@ namespace graft {
 namespace {
 
 struct AttnPlan {
-    int G, R, nRB, C, nchunk, tiles, cluster;
+    int G, R, nRB, C, nchunk, tiles;
     int persist;  // > 0: CTAs of the persistent two-tile kernel
     bool tc;
 };
@@ -32,21 +30,17 @@ struct AttnPlan {
 // shorter prologue) does better.  A single row block always goes to the
 // two-tile kernel.
 //
-// GRAFT_ATTN_CLUSTER=1 makes the chunks of a row tile (one tile per CTA,
-// split keys) run as one thread-block cluster (at most 8 CTAs, so the chunk
-// count is capped at 8) that merges its partials in distributed shared
-// memory instead of the merge kernel.  It is off by default: the merge moves
-// every partial row through the SM-to-SM network, which measured slower than
-// writing the partials to L2 for the merge kernel, and clusters of 7 or 8
-// single-SM CTAs do not all fit at once.
 // Persistence: when the two-tile grid would need more than one wave (more
 // work items than SMs) and the row tiles pair up (an even tile count), one
 // CTA per SM runs the items back to back (attention_tcp.cu), which hides each
 // item's start and finish behind its neighbours and deals items of
-// decreasing length evenly.  GRAFT_ATTN_PERSIST=0 turns this off;
-// GRAFT_ATTN_PERSIST_CTAS=n forces it with n CTAs (tests).
-// GRAFT_ATTN_MIN_CHUNK and GRAFT_ATTN_TILES (1 or 2) override the policy for
-// tuning and tests; the workspace size and the launch read the same values.
+// decreasing length evenly.
+//
+// The plan depends only on the call's shape, the device's SM count and the
+// optional GraftAttnTuning overrides, never on the process environment, so a
+// workspace sized for a shape fits every call of that shape.
+constexpr long long kMinChunk = 256;
+
 long long chunk_count(long long Lcap, long long units, int sms, long long min_chunk) {
     long long target = sms / units;
     if (target < 1) target = 1;
@@ -54,7 +48,16 @@ long long chunk_count(long long Lcap, long long units, int sms, long long min_ch
     return target < fill ? target : fill;
 }
 
-AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
+int check_tuning(const GraftAttnTuning* t) {
+    if (t == nullptr) return GRAFT_OK;
+    if (t->tiles != 0 && t->tiles != 1 && t->tiles != 2) return GRAFT_ERR_INVALID_ARG;
+    if (t->min_chunk < 0 || t->persist_ctas < -1) return GRAFT_ERR_INVALID_ARG;
+    for (int i = 0; i < 5; ++i)
+        if (t->reserved[i] != 0) return GRAFT_ERR_INVALID_ARG;
+    return GRAFT_OK;
+}
+
+AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap, const GraftAttnTuning* tune) {
     AttnPlan p;
     p.G = Hq / Hkv;
     p.R = Kmax * p.G;
@@ -63,11 +66,8 @@ AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
     int sms = device_sm_count();
     if (sms <= 0) sms = 148;
     constexpr long long blk = ATTN_TC_BLOCK_KEYS;
-    long long min_chunk = 256;
-    if (const char* env = getenv("GRAFT_ATTN_MIN_CHUNK")) {
-        const long long v = atoll(env);
-        if (v >= blk) min_chunk = (v + blk - 1) / blk * blk;
-    }
+    long long min_chunk = kMinChunk;
+    if (tune != nullptr && tune->min_chunk > 0) min_chunk = (tune->min_chunk + blk - 1) / blk * blk;
     if (min_chunk > (1LL << 30)) min_chunk = 1LL << 30;
     p.tiles = 1;
     if (p.tc) {
@@ -75,28 +75,18 @@ AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
         const long long n2 = chunk_count(Lcap, units2, sms, min_chunk);
         // with a single row block both kernels run the same grid; the two-tile kernel is quicker
         p.tiles = (p.nRB == 1 || (Lcap + n2 - 1) / n2 >= 1024) ? 2 : 1;
-        if (const char* env = getenv("GRAFT_ATTN_TILES")) {
-            const int v = atoi(env);
-            if (v == 1 || v == 2) p.tiles = v;
-        }
+        if (tune != nullptr && tune->tiles != 0) p.tiles = tune->tiles;
     }
     const long long units = (long long)B * Hkv * ((p.nRB + p.tiles - 1) / p.tiles);
     p.C = (int)min_chunk;
     p.nchunk = (int)chunk_count(Lcap, units, sms, min_chunk);
-    p.cluster = 0;
-    const char* cenv = getenv("GRAFT_ATTN_CLUSTER");
-    if (p.tc && p.tiles == 1 && p.nchunk > 1 && cenv && atoi(cenv) == 1) {
-        if (p.nchunk > 8) p.nchunk = 8;
-        p.cluster = p.nchunk;
-    }
     p.persist = 0;
-    if (p.tc && p.tiles == 2 && p.nRB % 2 == 0 && p.cluster == 0) {
+    if (p.tc && p.tiles == 2 && p.nRB % 2 == 0) {
         const long long items = (long long)B * p.nchunk * Hkv * (p.nRB / 2);
-        const char* penv = getenv("GRAFT_ATTN_PERSIST");
-        const char* cnt = getenv("GRAFT_ATTN_PERSIST_CTAS");
-        if (cnt && atoi(cnt) > 0)
-            p.persist = (int)(items < atoi(cnt) ? items : atoi(cnt));
-        else if (items > sms && !(penv && atoi(penv) == 0))
+        const int force = tune != nullptr ? tune->persist_ctas : 0;
+        if (force > 0)
+            p.persist = (int)(items < force ? items : force);
+        else if (force == 0 && items > sms)
             p.persist = sms;
     }
     return p;
@@ -104,7 +94,7 @@ AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap) {
 
 size_t attn_ws(const AttnPlan& p, int B, int Hkv, AttnArgs* a, void* ws) {
     WsCarver c(ws);
-    const size_t parts = (p.nchunk > 1 && p.cluster == 0) ? (size_t)B * Hkv * p.nRB * p.nchunk * 128 : 0;
+    const size_t parts = p.nchunk > 1 ? (size_t)B * Hkv * p.nRB * p.nchunk * 128 : 0;
     float* po = c.take<float>(parts * GRAFT_HEAD_DIM);
     float* pl = c.take<float>(parts);
     if (a) {
@@ -130,21 +120,29 @@ int check_shape(int B, int Hq, int Hkv, int head_dim, int Kmax, int64_t Lcap) {
 
 using namespace graft;
 
-extern "C" int graft_tree_attention_workspace_size(int B, int Hq, int Hkv, int head_dim, int Kmax, int64_t Lcap,
-                                                   size_t* bytes) {
+extern "C" int graft_tree_attention_workspace_size_ex(int B, int Hq, int Hkv, int head_dim, int Kmax, int64_t Lcap,
+                                                      const GraftAttnTuning* tuning, size_t* bytes) {
     if (bytes == nullptr) return GRAFT_ERR_INVALID_ARG;
-    const int rc = check_shape(B, Hq, Hkv, head_dim, Kmax, Lcap);
+    int rc = check_shape(B, Hq, Hkv, head_dim, Kmax, Lcap);
+    if (rc == GRAFT_OK) rc = check_tuning(tuning);
     if (rc != GRAFT_OK) return rc;
-    const AttnPlan p = plan_attention(B, Hq, Hkv, Kmax, Lcap);
+    const AttnPlan p = plan_attention(B, Hq, Hkv, Kmax, Lcap, tuning);
     *bytes = attn_ws(p, B, Hkv, nullptr, nullptr);
     return GRAFT_OK;
 }
 
-extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Kmax, const void* Q, const void* Kc,
-                                    const void* Vc, int64_t Lcap, const void* Kt, const void* Vt, const int32_t* L,
-                                    const uint64_t* tree_mask, float scale, void* O, int32_t* status, void* ws,
-                                    size_t ws_bytes, graft_stream_t stream) {
-    const int rc = check_shape(B, Hq, Hkv, head_dim, Kmax, Lcap);
+extern "C" int graft_tree_attention_workspace_size(int B, int Hq, int Hkv, int head_dim, int Kmax, int64_t Lcap,
+                                                   size_t* bytes) {
+    return graft_tree_attention_workspace_size_ex(B, Hq, Hkv, head_dim, Kmax, Lcap, nullptr, bytes);
+}
+
+extern "C" int graft_tree_attention_ex(int B, int Hq, int Hkv, int head_dim, int Kmax, const void* Q, const void* Kc,
+                                       const void* Vc, int64_t Lcap, const void* Kt, const void* Vt, const int32_t* L,
+                                       const uint64_t* tree_mask, float scale, void* O, int32_t* status,
+                                       const GraftAttnTuning* tuning, void* ws, size_t ws_bytes,
+                                       graft_stream_t stream) {
+    int rc = check_shape(B, Hq, Hkv, head_dim, Kmax, Lcap);
+    if (rc == GRAFT_OK) rc = check_tuning(tuning);
     if (rc != GRAFT_OK) return rc;
     if (B == 0) return GRAFT_OK;
     if (Q == nullptr || Kt == nullptr || Vt == nullptr || L == nullptr || tree_mask == nullptr || O == nullptr)
@@ -154,7 +152,7 @@ extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Km
                          reinterpret_cast<uintptr_t>(Vc) | reinterpret_cast<uintptr_t>(Kt) |
                          reinterpret_cast<uintptr_t>(Vt) | reinterpret_cast<uintptr_t>(O);
     if (al & 15) return GRAFT_ERR_INVALID_ARG;  // 16-byte vector loads and stores
-    const AttnPlan p = plan_attention(B, Hq, Hkv, Kmax, Lcap);
+    const AttnPlan p = plan_attention(B, Hq, Hkv, Kmax, Lcap, tuning);
     const size_t need = attn_ws(p, B, Hkv, nullptr, nullptr);
     if (!ws_ok(ws, ws_bytes, need)) return GRAFT_ERR_WORKSPACE;
     AttnArgs a{};
@@ -166,7 +164,6 @@ extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Km
     a.R = p.R;
     a.nRB = p.nRB;
     a.tiles = p.tiles;
-    a.cluster = p.cluster;
     a.C = p.C;
     a.nchunk = p.nchunk;
     a.Lcap = (int)Lcap;
@@ -187,4 +184,12 @@ extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Km
         return attn_tcp_launch(a, p.persist, (cudaStream_t)stream);
     if (p.tc) return p.tiles == 2 ? attn_tc_launch(a, (cudaStream_t)stream) : attn_tc1_launch(a, (cudaStream_t)stream);
     return attn_mma_launch(a, (cudaStream_t)stream);
+}
+
+extern "C" int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Kmax, const void* Q, const void* Kc,
+                                    const void* Vc, int64_t Lcap, const void* Kt, const void* Vt, const int32_t* L,
+                                    const uint64_t* tree_mask, float scale, void* O, int32_t* status, void* ws,
+                                    size_t ws_bytes, graft_stream_t stream) {
+    return graft_tree_attention_ex(B, Hq, Hkv, head_dim, Kmax, Q, Kc, Vc, Lcap, Kt, Vt, L, tree_mask, scale, O,
+                                   status, nullptr, ws, ws_bytes, stream);
 }

@@ -382,7 +382,7 @@ attn_combine_kernel(AttnArgs a) {
 }
 
 int attn_combine_launch(const AttnArgs& a, cudaStream_t st) {
-    if (a.nchunk <= 1 || a.cluster > 0) return GRAFT_OK;
+    if (a.nchunk <= 1) return GRAFT_OK;
     const long long rows = (long long)a.B * a.Hkv * a.nRB * 128;
     launch_pdl(attn_combine_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, a);
     count_launches(1);

@@ -43,12 +43,7 @@
 // so stale cache rows cannot inject NaN.
 //
 // The epilogue stages the tile's rows through the freed K/V ring memory and
-// writes them out along contiguous rows.  When the key chunks of a row tile
-// run as one thread-block cluster (a.cluster > 0: the chunk count, at most
-// 8), each CTA stages its normalised partial rows and their log2-sum-exp in
-// shared memory instead, and after a cluster barrier every CTA merges a
-// slice of the rows across the cluster through distributed shared memory
-// and writes them: no partials reach global memory and no merge kernel runs.
+// writes them out along contiguous rows.
 //
 // Every mbarrier wait is bounded; on timeout the CTA raises
 // GRAFT_STATUS_TIMEOUT in the status word, stops issuing work, drains what
@@ -81,7 +76,6 @@ constexpr uint32_t OFF_K = OFF_Q + Q_TILE_BYTES;
 constexpr uint32_t OFF_V = OFF_K + SK * BLK_BYTES;
 constexpr uint32_t OFF_BAR = OFF_V + SV * BLK_BYTES;
 constexpr uint32_t OFF_STAGE = OFF_K;  // epilogue staging reuses the rings once every MMA has run
-constexpr uint32_t OFF_LSE = OFF_STAGE + 128 * 512;  // cluster mode: the staged rows' log2-sum-exp
 // barriers
 constexpr int BAR_Q = 0;              // Q tile landed in shared memory
 constexpr int BAR_KF = 1;             // [SK] K block landed
@@ -140,7 +134,6 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     const int kvh = blockIdx.x / a.nRB;
     const int c = blockIdx.y;
     int b = blockIdx.z;  // remapped below to the request this CTA serves
-    const int ncl = a.cluster;  // > 0: the chunks of this row tile form one cluster (rank = c)
 
     // Prologue that touches no global memory: it overlaps the previous kernel's tail.
     if (tid == 0) {
@@ -191,21 +184,19 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     const int Cb = chunk_len(a, bad_len ? 0 : Lb);
     const int nck = (Lb > 0 && !bad_len) ? (Lb + Cb - 1) / Cb : 1;
     // A split request whose prefix leaves a chunk CTA idle gives it the tree block, so the last
-    // prefix chunk does not carry one block more than the others (not in cluster mode).
-    const int tree_chunk = (ncl == 0 && nck > 1 && nck < a.nchunk) ? nck : nck - 1;
-    if (bad_len || (c > tree_chunk && ncl == 0)) {  // uniform over the CTA (and over a cluster: same b)
+    // prefix chunk does not carry one block more than the others.
+    const int tree_chunk = (nck > 1 && nck < a.nchunk) ? nck : nck - 1;
+    if (bad_len || c > tree_chunk) {  // uniform over the CTA
         if (bad_len && tid == 0 && c == 0 && rb == 0 && kvh == 0) flag_status(a.status, GRAFT_STATUS_LENGTH);
         mark_partial(a, b, kvh, rb, c, -INFINITY);
         if (warp == 2) tmem_dealloc(tmem, 512);
         return;
     }
     if (nck == 1) mark_partial(a, b, kvh, rb, 0, INFINITY);
-    // in a cluster a chunk past the request's keys stays for the merge and contributes nothing
-    const bool empty = c > tree_chunk;
     const int k0 = c * Cb;
-    const int k1 = empty ? k0 : max(k0, min(Lb, k0 + Cb));
+    const int k1 = max(k0, min(Lb, k0 + Cb));
     const int nb_prefix = (k1 - k0 + BN - 1) / BN;
-    const bool has_tree = !empty && (c == tree_chunk);
+    const bool has_tree = c == tree_chunk;
     const int nb = nb_prefix + (has_tree ? 1 : 0);
     const int ragged_block = ((k1 - k0) % BN) != 0 ? nb_prefix - 1 : -1;
     const int ragged_valid = (k1 - k0) % BN;
@@ -407,7 +398,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_DONE), 0, kWaitNs));
             if (!ok) raise_abort(abort_flag, a.status);
         }
-        const bool direct = (nck == 1) && ncl == 0;
+        const bool direct = nck == 1;
         const float inv = (row_ok && l_sum > 0.f) ? 1.f / l_sum : 0.f;
         if (ok) {
             tc_fence_after();
@@ -447,9 +438,6 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                     }
                 }
             }
-            if (ncl > 0)
-                reinterpret_cast<float*>(gbase + OFF_LSE)[r] =
-                    (row_ok && l_sum > 0.f) ? m_used + log2f(l_sum) : -INFINITY;
         }
         mbar_arrive(bar(BAR_EPI));
         const bool staged = __all_sync(0xffffffffu, mbar_wait(bar(BAR_EPI), 0, kWaitNs));
@@ -457,7 +445,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             raise_abort(abort_flag, a.status);
             ok = false;
         }
-        if (ok && ncl == 0) {
+        if (ok) {
             // write the tile out along contiguous rows; 128 threads
             const uint8_t* stile = gbase + OFF_STAGE;
             if (direct) {
@@ -508,69 +496,6 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     __syncthreads();
     tc_fence_after();
     if (warp == 2) tmem_dealloc(tmem, 512);
-    if (ncl > 0) {
-        // ------------------------------------------------------------ merge across the cluster
-        // every CTA's staged rows and log2-sum-exp are complete and visible cluster-wide; this
-        // CTA merges rows [r0, r1): O = sum_k 2^(lse_k - lse) O_k with lse = log2 sum_k 2^lse_k,
-        // one warp per row, four dims per lane.  A warp takes two rows at a time and issues all
-        // their distributed-shared-memory loads (every CTA's log2-sum-exp and partial row) before
-        // it uses any, so a pair of rows costs one round trip.
-        cluster_sync();
-        const int rows_per = (128 + ncl - 1) / ncl;
-        const int r0 = c * rows_per, r1 = min(128, r0 + rows_per);
-        const uint32_t stage_l = base + OFF_STAGE, lse_l = base + OFF_LSE;
-        constexpr int RPW = 2;     // rows per warp per round
-        constexpr int MAXCL = 8;   // portable cluster size bound (the launch checks it)
-        for (int row0 = r0 + warp * RPW; row0 < r1; row0 += (NTHREADS / 32) * RPW) {
-            float lk[RPW];
-            float4 v[RPW][MAXCL];
-#pragma unroll
-            for (int q = 0; q < RPW; ++q) {
-                const int row = row0 + q;
-                const bool live = row < r1;  // uniform over the warp
-                lk[q] = (live && lane < ncl) ? dsmem_ld_f32(dsmem_addr(lse_l + row * 4, (uint32_t)lane)) : -INFINITY;
-                const uint32_t src = stage_l + row * 512 + ((lane ^ (row & 31)) << 4);
-#pragma unroll
-                for (int k = 0; k < MAXCL; ++k)
-                    v[q][k] = (live && k < ncl) ? dsmem_ld_f32x4(dsmem_addr(src, (uint32_t)k))
-                                                : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int q = 0; q < RPW; ++q) {
-                const int row = row0 + q;
-                const int g = rb * 128 + row;
-                if (row >= r1 || g >= a.R) continue;  // uniform over the warp
-                float mx = lk[q];
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                const float wk = (lk[q] == -INFINITY) ? 0.f : ex2(lk[q] - mx);
-                float wsum = wk;
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int k = 0; k < MAXCL; ++k) {
-                    const float w = __shfl_sync(0xffffffffu, wk, k);
-                    if (w == 0.f) continue;  // empty or absent CTA: its staged row is not used
-                    acc.x += w * v[q][k].x;
-                    acc.y += w * v[q][k].y;
-                    acc.z += w * v[q][k].z;
-                    acc.w += w * v[q][k].w;
-                }
-                const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-                const int nd = g / a.G, hh = kvh * a.G + g % a.G;
-                __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
-                __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
-                uint2 o2;
-                o2.x = *reinterpret_cast<uint32_t*>(&lo);
-                o2.y = *reinterpret_cast<uint32_t*>(&hi);
-                *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(a.O) +
-                                          (((size_t)b * a.Kmax + nd) * a.Hq + hh) * HD + lane * 4) = o2;
-            }
-        }
-        // no CTA leaves (and frees its shared memory) while another still reads it
-        cluster_sync();
-    }
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -637,27 +562,7 @@ int attn_tc1_launch(const AttnArgs& a, cudaStream_t st) {
         attr_set[dev] = true;
     }
     dim3 grid(a.nRB * a.Hkv, a.nchunk, a.B);
-    if (a.cluster > 0) {
-        // the chunks of one row tile form a cluster along y; portable cluster sizes only
-        if (a.cluster > 8 || a.cluster != a.nchunk) return GRAFT_ERR_INVALID_ARG;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = grid;
-        cfg.blockDim = dim3(NTHREADS);
-        cfg.dynamicSmemBytes = SMEM_BYTES;
-        cfg.stream = st;
-        cudaLaunchAttribute attr[2];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        attr[1].id = cudaLaunchAttributeClusterDimension;
-        attr[1].val.clusterDim.x = 1;
-        attr[1].val.clusterDim.y = (unsigned)a.cluster;
-        attr[1].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 2;
-        cudaLaunchKernelEx(&cfg, attn_tc_kernel, m, a);
-    } else {
-        launch_pdl(attn_tc_kernel, grid, dim3(NTHREADS), SMEM_BYTES, st, m, a);
-    }
+    launch_pdl(attn_tc_kernel, grid, dim3(NTHREADS), SMEM_BYTES, st, m, a);
     count_launches(1);
     const int rc = launch_status();
     if (rc != GRAFT_OK) return rc;

@@ -266,12 +266,13 @@ void* g_scratch_addr[64] = {nullptr};
 // kernels must be given the address cudaGetSymbolAddress returns.
 int noalloc_scratch(void** out) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return GRAFT_ERR_CUDA;
-    if (dev < 0 || dev >= 64) return GRAFT_ERR_UNSUPPORTED_SHAPE;
+    if (!cuda_ok(cudaGetDevice(&dev))) return GRAFT_ERR_CUDA;
+    if (dev < 0 || dev >= 64) return GRAFT_ERR_UNSUPPORTED_SHAPE;  // device ordinals 0..63 (graft.h)
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
     if (g_scratch_addr[dev] == nullptr) {
         void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_update_scratch) != cudaSuccess || p == nullptr) return GRAFT_ERR_CUDA;
+        if (!cuda_ok(cudaGetSymbolAddress(&p, g_update_scratch))) return GRAFT_ERR_CUDA;
+        if (p == nullptr) return GRAFT_ERR_CUDA;
         g_scratch_addr[dev] = p;
     }
     *out = g_scratch_addr[dev];
