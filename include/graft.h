@@ -83,7 +83,10 @@ typedef struct CUstream_st* graft_stream_t;
  *   checkpoint[s]   drafter call (0-based) after which c is tested; strictly increasing, < D
  *   tau[s]          threshold: drafting stops at the first s with c_{checkpoint[s]} < tau[s]
  *   K_draft[s]      draft nodes kept (root included) when stopped at s;
- *                   K_draft[n_checkpoints] is the unpruned stage and must equal Kmax
+ *                   K_draft[n_checkpoints] is the unpruned stage and must equal Kmax.
+ *                   A value above 1 + the stage's pool (k + checkpoint[s] k^2
+ *                   candidates) keeps the whole pool and leaves the rest of
+ *                   the draft slots as empty nodes (see graft_config_no_retrieval)
  *   n_tmpl          envelope size = max_s (Kmax - K_draft[s])
  *   tmpl_parent[j]  parent of envelope node j: -1 = the root, else an index < j
  *   tmpl_rank[j]    rank (0..W-1) of node j among its parent token's successors in M
@@ -117,6 +120,21 @@ int graft_config_init(GraftConfig* cfg, int Kmax, int D, int k, int V, int W,
 int graft_config_validate(const GraftConfig* cfg);
 
 /*
+ * graft_config_no_retrieval — turn a valid *cfg (host) into the "w/o
+ * retrieval" ablation of the Graft article's results paragraph: the
+ * retrieval budget is zero at every stage (K_ret_s = 0), so the whole
+ * budget goes to the draft, K_draft[s] = Kmax, and the envelope is empty
+ * (n_tmpl = 0).  Pruning is unchanged.  A stage whose candidate pool holds
+ * fewer than Kmax - 1 nodes (a prune at d0 with k < Kmax - 1) keeps all of
+ * them; the draft slots it cannot fill are EMPTY NODES: token
+ * GRAFT_EMPTY_TOKEN (-1), parent 0 (the root), depth 1.  No target token
+ * equals -1, so graft_accept_compact never accepts an empty node, and
+ * graft_update_M adds no pair for it.  Host only; no CUDA call.
+ */
+#define GRAFT_EMPTY_TOKEN (-1)
+int graft_config_no_retrieval(GraftConfig* cfg);
+
+/*
  * graft_build_tree — stages 1 to 3 of the step for B requests
  * (Graft article, step summary and method paragraph, first three points;
  * Graft abstract: "prune-then-graft").
@@ -132,8 +150,9 @@ int graft_config_validate(const GraftConfig* cfg);
  *   tree_tok, tree_parent (root -1), tree_depth, tree_pos (= L[b] + depth) i32,
  *   tree_mask u64 (bit j of node i set iff j is i or an ancestor of i),
  *   stage [B] i32 (pruning stage; n_checkpoints = not pruned).
- * Tree order: root; kept draft nodes by (depth asc, score desc); then the
- * stage's first K_ret envelope nodes (empty M slots give pad token 0).
+ * Tree order: root; kept draft nodes by (depth asc, score desc); empty
+ * nodes if the pool ran short of K_draft (graft_config_no_retrieval); then
+ * the stage's first K_ret envelope nodes (empty M slots give pad token 0).
  * Workspace: graft_build_tree_workspace_size.
  */
 int graft_build_tree_workspace_size(const GraftConfig* cfg, int B, size_t* bytes);
@@ -160,8 +179,8 @@ int graft_build_tree(const GraftConfig* cfg, int B, const float* draft_logits,
  *
  * Ablations of the method need no entry point of their own: without
  * pruning, set every tau to 0 (the confidence never drops below it, so the
- * dense tree of stage n_checkpoints is built); without retrieval, pass an
- * all-empty M (every retrieved slot becomes a pad: token 0 under the root).
+ * dense tree of stage n_checkpoints is built); without retrieval, apply
+ * graft_config_no_retrieval to the config (K_ret_s = 0 at every stage).
  */
 int graft_build_tree_block(const GraftConfig* cfg, int B, const float* block_logits,
                            const int32_t* root_tok, const int32_t* M_succ, const int32_t* L,
@@ -352,9 +371,10 @@ int graft_lm_head_sample(int N, int d_model, int V, const void* H, const void* W
  * Each pair already in its row adds 1 to that count (an atomic increment);
  * new successors enter with their multiplicity; each touched row keeps its
  * top W by (count desc, token asc).  The result depends only on the
- * multiset, not on pair order, and is bit-exact.  Pairs with an id outside
- * [0, V) are skipped and flagged; the pair (-1, -1) marks an empty slot and
- * is skipped silently.  Workspace: graft_update_M_workspace_size.
+ * multiset, not on pair order, and is bit-exact.  A pair whose src is -1
+ * (an empty slot, or an empty tree node of graft_config_no_retrieval) is
+ * skipped silently; any other id outside [0, V) is skipped and flagged.
+ * Workspace: graft_update_M_workspace_size.
  * To seed M from a prompt's evidence, pass its bigrams: src = tokens,
  * dst = tokens + 1, n = length - 1.
  */

@@ -108,11 +108,19 @@ def retrieval_template(D: int, W: int, n: int) -> Tuple[List[int], List[int], Li
 
 
 def make_config(Kmax: int, D: int, k: int, V: int, W: int,
-                checkpoints: Sequence[int] = (0, 1, 5), tau: float | Sequence[float] = 0.3) -> dict:
+                checkpoints: Sequence[int] = (0, 1, 5), tau: float | Sequence[float] = 0.3,
+                no_retrieval: bool = False) -> dict:
     """Collect the method's parameters into one dict (the oracle's view of a config).
 
     Checkpoints beyond the draft depth are dropped, so a shallow draft
     (D <= 5) keeps only the checkpoints it can reach.
+
+    ``no_retrieval`` is the Graft article's "w/o retrieval" ablation (results
+    paragraph).  Reading: the retrieval budget is zero at every stage,
+    K_ret_s = 0, so Kmax = K_draft_s + K_ret_s hands the whole budget to the
+    draft, K_draft_s = Kmax; a stage whose candidate pool holds fewer than
+    Kmax - 1 nodes keeps all of them and leaves the remaining slots empty
+    (see ``tree.merge``).  Pruning itself is unchanged.
     """
     cps = [d for d in checkpoints if d < D]
     if isinstance(tau, (int, float)):
@@ -120,6 +128,8 @@ def make_config(Kmax: int, D: int, k: int, V: int, W: int,
     else:
         taus = [float(t) for t in tau][: len(cps)]
     K_draft = draft_budget(Kmax, D, k, cps)
+    if no_retrieval:
+        K_draft = [Kmax] * len(K_draft)
     K_ret = [Kmax - kd for kd in K_draft]
     n_tmpl = max(K_ret)
     tp, tr, paths = retrieval_template(D, W, n_tmpl)

@@ -144,7 +144,8 @@ def greedy_hybrid(lm: TinyLM, prompt: List[int], n_new: int, Lcap: int, cfg: dic
         nodes = tr.retained_draft(res, cfg)
         ret = tr.retrieve(root, M_succ, cfg["tmpl_parent"], cfg["tmpl_rank"])
         tree = tr.merge(root, nodes, ret, cfg["tmpl_parent"], res.stage, L, cfg)
-        logits, kv = lm.forward(tree.tok, tree.pos, tree.mask, cache, L)
+        # an empty node (token -1) runs through the model as token 0; it is never accepted
+        logits, kv = lm.forward([max(t, 0) for t in tree.tok], tree.pos, tree.mask, cache, L)
         g, n, path, out_tok, bonus = acc.accept(logits, tree.tok, tree.parent, tree.depth)
         for c, (k, v) in zip(cache, kv):
             for t, p in enumerate(path):
@@ -155,7 +156,8 @@ def greedy_hybrid(lm: TinyLM, prompt: List[int], n_new: int, Lcap: int, cfg: dic
         root = bonus
         M_succ, M_cnt = um.update_M(M_succ, M_cnt, np.array(tree.tok), np.array(g))
         steps.append(dict(stage=res.stage, acc_len=n,
-                          retrieved_accepted=sum(1 for p in path if p >= tree.n_draft)))
+                          retrieved_accepted=sum(1 for p in path if p >= tree.n_draft),
+                          empty_nodes=sum(1 for t in tree.tok if t == tr.EMPTY)))
     return out[:n_new], cache, L, steps
 
 
@@ -214,7 +216,7 @@ def sample_hybrid(lm: TinyLM, prompt: List[int], n_new: int, Lcap: int, cfg: dic
         nodes = tr.retained_draft(res, cfg)
         ret = tr.retrieve(root, M_succ, cfg["tmpl_parent"], cfg["tmpl_rank"])
         tree = tr.merge(root, nodes, ret, cfg["tmpl_parent"], res.stage, L, cfg)
-        logits, kv = lm.forward(tree.tok, tree.pos, tree.mask, cache, L)
+        logits, kv = lm.forward([max(t, 0) for t in tree.tok], tree.pos, tree.mask, cache, L)
         y, gap = smp.sample_tree(logits[None], np.array(tree.pos)[None], T, seed)
         g, n, path, out_tok, bonus = acc.accept_from_argmax(y[0], tree.tok, tree.parent, tree.depth)
         gaps.extend(gap[0][p] for p in path)

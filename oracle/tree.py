@@ -33,6 +33,7 @@ from typing import Callable, List, Optional, Sequence
 import numpy as np
 
 F32 = np.float32
+EMPTY = -1  # token of an empty tree slot (a draft slot no candidate fills)
 
 
 def row_lse_topk(row: np.ndarray, k: int):
@@ -133,7 +134,8 @@ def retained_draft(res: DraftResult, cfg: dict) -> List[Cand]:
     candidates by (score desc, depth asc, candidate index asc); a child never
     scores above its parent, so the kept set is ancestor-closed.  Tree order
     is (depth asc, score desc, candidate index asc), so a parent always
-    precedes its children.
+    precedes its children.  A pool smaller than K_draft_s - 1 (possible only
+    without retrieval, where K_draft_s = Kmax) is kept whole.
     """
     keep = cfg["K_draft"][res.stage] - 1
     best = sorted(res.pool, key=lambda c: (-float(c.score), c.depth, c.idx))[:keep]
@@ -182,6 +184,12 @@ def merge(root_tok: int, draft_nodes: List[Cand], ret_tok: Sequence[int],
     top-level nodes hang off the root.  Duplicate paths are kept (no dedup),
     so the tree always has Kmax nodes.  position = L + depth, and the
     ancestor mask is mask[i] = mask[parent[i]] | (1 << i).
+
+    Reading for the "w/o retrieval" ablation (Graft article, results
+    paragraph), where K_draft_s = Kmax may exceed what a pruned draft holds:
+    the draft slots the pool cannot fill are empty nodes, token EMPTY (-1)
+    under the root at depth 1.  No target token equals -1, so an empty node
+    is never accepted, and it adds no pair to M.
     """
     Kmax = cfg["Kmax"]
     n_draft = cfg["K_draft"][stage]
@@ -195,7 +203,11 @@ def merge(root_tok: int, draft_nodes: List[Cand], ret_tok: Sequence[int],
         tok.append(c.token)
         parent.append(0 if c.parent is None else where[id(c.parent)])
         depth.append(c.depth)
-    assert len(tok) == n_draft
+    assert len(tok) <= n_draft
+    while len(tok) < n_draft:
+        tok.append(EMPTY)
+        parent.append(0)
+        depth.append(1)
     for j in range(n_ret):
         p = tmpl_parent[j]
         pi = 0 if p < 0 else n_draft + p

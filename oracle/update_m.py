@@ -15,7 +15,8 @@ M's layout and the update rule open; they are fixed here as:
 
 Reading for which pairs feed the update: every node i of every verified
 tree contributes (tree_tok[i], argmax_i), the target's greedy successor of
-that node's token in that context.
+that node's token in that context; an empty node (token -1, which only the
+"w/o retrieval" ablation produces) contributes nothing.
 
 Prompt-evidence policy (Graft article, method paragraph: retrieval uses the
 context's own evidence, which is what carries long contexts): M is seeded
@@ -38,6 +39,9 @@ def update_M(succ: np.ndarray, cnt: np.ndarray, src: np.ndarray, dst: np.ndarray
     cnt = cnt.copy()
     src = np.asarray(src).reshape(-1)
     dst = np.asarray(dst).reshape(-1)
+    # an empty tree node (token -1, see tree.merge) contributes no pair
+    keep = src != -1
+    src, dst = src[keep], dst[keep]
     if np.any((src < 0) | (src >= V) | (dst < 0) | (dst >= V)):
         raise ValueError("token id out of range")
     rows: Dict[int, Counter] = {}

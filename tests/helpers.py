@@ -27,10 +27,10 @@ def gb():
     return binding
 
 
-def oracle_cfg(wl, tau=None, checkpoints=None):
+def oracle_cfg(wl, tau=None, checkpoints=None, no_retrieval=False):
     return oconfig.make_config(Kmax=wl.Kmax, D=wl.D, k=wl.k, V=wl.V, W=wl.W,
                                checkpoints=wl.checkpoints if checkpoints is None else checkpoints,
-                               tau=wl.tau if tau is None else tau)
+                               tau=wl.tau if tau is None else tau, no_retrieval=no_retrieval)
 
 
 def lib_cfg(wl, tau=None, checkpoints=None):
@@ -54,3 +54,31 @@ def to_np(t: torch.Tensor) -> np.ndarray:
 
 def mask_to_u64(t: torch.Tensor) -> np.ndarray:
     return t.cpu().numpy().view(np.uint64)
+
+
+_WARM = {}
+
+
+def warm_M(wl):
+    """The oracle's table after the long-context warm-up: five multiset updates, each with every adjacent
+    pair of the workload's seeded 65536-token stream.  Cached per workload name."""
+    from oracle import update_m as oupd
+    from tree_verification_gb300 import synth
+    if wl.name not in _WARM:
+        src, dst = synth.stream_pairs(synth.token_stream(wl.Lmax, wl.V, wl.seed + 41))
+        s, c = synth.empty_M(wl.V, wl.W)
+        for _ in range(5):
+            s, c = oupd.update_M(s, c, src, dst)
+        _WARM[wl.name] = (s, c)
+    return _WARM[wl.name]
+
+
+def initial_M(wl):
+    """A workload's starting table as host arrays: Zipf counts, the warm-up table, or empty."""
+    from tree_verification_gb300 import synth
+    if wl.M_init == "zipf":
+        return synth.zipf_M(wl.V, wl.W, wl.seed + 5)
+    if wl.M_init == "warm":
+        s, c = warm_M(wl)
+        return s.copy(), c.copy()
+    return synth.empty_M(wl.V, wl.W)

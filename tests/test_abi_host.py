@@ -51,6 +51,33 @@ def test_config_matches_oracle(Kmax, D, k, V, W):
     assert cfg["n_tmpl"] == len(ref["tmpl_parent"])
 
 
+@pytest.mark.parametrize("Kmax,D,k,V,W", [(32, 6, 4, 32000, 8), (64, 8, 8, 128256, 16), (6, 3, 2, 8, 2)])
+def test_config_without_retrieval_matches_oracle(Kmax, D, k, V, W):
+    b = gb()
+    cfg = b.graft_config_no_retrieval(b.graft_config_init(Kmax, D, k, V, W, [0, 1, 5], 0.3)).as_dict()
+    ref = oconfig.make_config(Kmax=Kmax, D=D, k=k, V=V, W=W, no_retrieval=True)
+    assert cfg["K_draft"] == ref["K_draft"] == [Kmax] * len(ref["K_draft"])
+    assert cfg["n_tmpl"] == 0 and ref["tmpl_parent"] == []
+    assert b.graft_config_validate(b.graft_config_no_retrieval(b.graft_config_init(Kmax, D, k, V, W))) == 0
+
+
+def test_tuning_fields_are_checked():
+    lib = gb().lib()
+    b = gb()
+    sz = ctypes.c_size_t()
+    for bad in (dict(tiles=3), dict(min_chunk=-1), dict(persist_ctas=-2), dict(reserved=(ctypes.c_int32 * 5)(0, 1))):
+        t = b.GraftAttnTuning()
+        for k, v in bad.items():
+            setattr(t, k, v)
+        assert lib.graft_tree_attention_workspace_size_ex(1, 8, 2, 128, 32, 512, ctypes.byref(t), ctypes.byref(sz)) == -1
+    # no tuning (NULL) and an all-zero tuning plan the same workspace
+    assert lib.graft_tree_attention_workspace_size_ex(2, 32, 8, 128, 64, 4160, None, ctypes.byref(sz)) == 0
+    n0 = sz.value
+    t = b.GraftAttnTuning()
+    assert lib.graft_tree_attention_workspace_size_ex(2, 32, 8, 128, 64, 4160, ctypes.byref(t), ctypes.byref(sz)) == 0
+    assert sz.value == n0
+
+
 def test_config_rejects_bad():
     b = gb()
     with pytest.raises(b.GraftError):

@@ -15,7 +15,9 @@ from oracle import accept as oacc
 from oracle import attention as oatt
 from oracle import tree as otree
 from oracle import update_m as oupd
-from tests.helpers import MARGIN, assert_attention_close, gb, lib_cfg, mask_to_u64, oracle_cfg, to_np
+from tests.helpers import MARGIN, assert_attention_close, gb, initial_M, lib_cfg, mask_to_u64, oracle_cfg, to_np, \
+    warm_M
+from tests.tree_alternatives import same_tree, valid_trees
 from tree_verification_gb300 import synth
 
 pytestmark = pytest.mark.gpu
@@ -41,25 +43,60 @@ def _M(wl, device=DEV):
     return torch.from_numpy(s).to(device), torch.from_numpy(c).to(device)
 
 
-def _oracle_tree(wl, cfg_o, dl_gpu, roots, succ_np, L):
-    """Oracle tree per request, reading drafter rows from the device lazily."""
-    out, margins = [], []
+def _row_fns(wl, dl_gpu, block=False):
+    """Per request, the drafter row of (call d, frontier slot f), read from the device lazily (a block
+    drafter's row of depth d serves every slot)."""
+    fns = []
     for b in range(wl.B):
         rows = {}
 
-        def row_fn(d, f, _path, b=b):
-            key = (d, f)
+        def row_fn(d, f, _path, b=b, rows=rows):
+            key = (d, 0 if block else f)
             if key not in rows:
-                rows[key] = dl_gpu[b, d, f].cpu().numpy()
+                rows[key] = (dl_gpu[b, d] if block else dl_gpu[b, d, f]).cpu().numpy()
             return rows[key]
 
+        fns.append(row_fn)
+    return fns
+
+
+def _oracle_tree(wl, cfg_o, dl_gpu, roots, succ_np, L, block=False):
+    """Oracle tree per request, its decision margin and its drafter-row function."""
+    out, margins = [], []
+    fns = _row_fns(wl, dl_gpu, block)
+    for b in range(wl.B):
+        row_fn = fns[b]
         res = otree.draft_tree(row_fn, int(roots[b]), cfg_o)
         nodes = otree.retained_draft(res, cfg_o)
         ret = otree.retrieve(int(roots[b]), succ_np, cfg_o["tmpl_parent"], cfg_o["tmpl_rank"])
         t = otree.merge(int(roots[b]), nodes, ret, cfg_o["tmpl_parent"], res.stage, int(L[b]), cfg_o)
         out.append(t)
         margins.append(otree.draft_margins(row_fn, int(roots[b]), cfg_o))
-    return out, margins
+    return out, margins, fns
+
+
+def _gpu_tree(gpu, b, n_draft):
+    tok, par, dep, pos = (to_np(gpu[k])[b].tolist() for k in ("tok", "parent", "depth", "pos"))
+    mask = [int(x) for x in mask_to_u64(gpu["mask"])[b]]
+    st = int(to_np(gpu["stage"])[b])
+    return otree.Tree(tok=tok, parent=par, depth=dep, pos=pos, mask=mask, stage=st, n_draft=n_draft)
+
+
+def _check_trees(gpu, trees, margins, fns, roots, succ_np, L, cfg_o):
+    """Every request checked: bit-exact where every decision clears MARGIN; otherwise the GPU's tree
+    must be one of the trees the oracle builds when any decision within MARGIN goes the other way.
+    Returns the number of requests compared exactly."""
+    exact = 0
+    for b, t in enumerate(trees):
+        g = _gpu_tree(gpu, b, t.n_draft)
+        if margins[b] > MARGIN:
+            assert same_tree(g, t), f"request {b}: tree differs from the oracle's"
+            exact += 1
+        else:
+            alts = valid_trees(fns[b], int(roots[b]), succ_np, int(L[b]), cfg_o, eps=MARGIN)
+            assert any(same_tree(g, a) for a in alts), \
+                f"request {b}: tree is none of the {len(alts)} trees near-tied decisions allow"
+    return exact
 
 
 def _compare_tree(gpu, trees):
@@ -93,7 +130,7 @@ def test_build_tree_parity(name):
         succ, _ = _M(wl)
         succ_np = succ.cpu().numpy()
     gpu = _build(wl, cfg, dl, roots, succ, L)
-    trees, margins = _oracle_tree(wl, cfg_o, dl, roots, succ_np, L)
+    trees, margins, _ = _oracle_tree(wl, cfg_o, dl, roots, succ_np, L)
     assert min(margins) > MARGIN
     _compare_tree(gpu, trees)
 
@@ -115,12 +152,11 @@ def test_build_tree_all_stages(V, seed):
     s_np, _ = synth.zipf_M(wl.V, wl.W, seed)
     succ = torch.from_numpy(s_np).to(DEV)
     gpu = _build(wl, cfg, dl, roots, succ, L)
-    trees, margins = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
-    ok = [b for b in range(wl.B) if margins[b] > MARGIN]
-    assert len(ok) >= wl.B - 2, f"too many near-tie requests: {margins}"
+    trees, margins, fns = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
+    exact = _check_trees(gpu, trees, margins, fns, roots, s_np, L, cfg_o)
+    assert exact >= wl.B - 2, f"too many near-tie requests: {margins}"
     stages = to_np(gpu["stage"])
-    _compare_tree({k: v[ok] for k, v in gpu.items()}, [trees[b] for b in ok])
-    assert {0, 1, 2, 3} <= {int(stages[b]) for b in ok}
+    assert {0, 1, 2, 3} <= {int(stages[b]) for b in range(wl.B) if margins[b] > MARGIN}
 
 
 @pytest.mark.parametrize("tau", [0.0, 1.5])
@@ -132,10 +168,10 @@ def test_build_tree_tau_extremes(tau):
     s_np, _ = synth.zipf_M(wl.V, wl.W, 3)
     succ = torch.from_numpy(s_np).to(DEV)
     gpu = _build(wl, cfg, dl, roots, succ, L)
-    trees, margins = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
+    trees, margins, fns = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
     if tau == 0.0:
         assert min(margins) > MARGIN
-    _compare_tree(gpu, trees)
+    _check_trees(gpu, trees, margins, fns, roots, s_np, L, cfg_o)
     assert set(to_np(gpu["stage"]).tolist()) == ({3} if tau == 0.0 else {0})
 
 
@@ -146,13 +182,13 @@ def test_build_tree_single_node_and_empty_M():
     roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
     s_np, _ = synth.empty_M(wl.V, wl.W)
     gpu = _build(wl, cfg, dl, roots, torch.from_numpy(s_np).to(DEV), L)
-    trees, _ = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
+    trees, _, _ = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
     _compare_tree(gpu, trees)
     wl2 = synth.WORKLOADS["tiny"].scaled(B=2, V=1000)
     cfg2, cfg2_o = lib_cfg(wl2), oracle_cfg(wl2)
     dl2 = synth.draft_logits(wl2, DEV)
     gpu2 = _build(wl2, cfg2, dl2, roots, torch.from_numpy(s_np).to(DEV), L)
-    trees2, _ = _oracle_tree(wl2, cfg2_o, dl2, roots, s_np, L)
+    trees2, _, _ = _oracle_tree(wl2, cfg2_o, dl2, roots, s_np, L)
     _compare_tree(gpu2, trees2)
     assert all(t.tok[t.n_draft:] == [0] * (wl2.Kmax - t.n_draft) for t in trees2)
 
@@ -320,22 +356,24 @@ def test_attention_full_size_sampled(name, layers, reqs):
 
 def _tree_from_oracle(wl, dl, roots, succ_np, L):
     cfg_o = oracle_cfg(wl)
-    trees, _ = _oracle_tree(wl, cfg_o, dl, roots, succ_np, L)
+    trees, _, _ = _oracle_tree(wl, cfg_o, dl, roots, succ_np, L)
     tok = np.array([t.tok for t in trees], np.int32)
     par = np.array([t.parent for t in trees], np.int32)
     dep = np.array([t.depth for t in trees], np.int32)
     return tok, par, dep
 
 
-@pytest.mark.parametrize("name", ["tiny", "llama3_8b", "qwen3_8b_batch", "qwen3_235b"])
+@pytest.mark.parametrize("name", ["tiny", "llama3_8b", "qwen3_8b_batch", "llama31_8b_long", "qwen3_235b"])
 def test_accept_compact_parity(name):
+    """Acceptance and compaction on every workload; the long-context one writes past row 65536 of its
+    cache (64-bit destination offsets)."""
     wl = synth.WORKLOADS[name]
     n_layers = 2
     Lcap = wl.lcap()
     dl = synth.draft_logits(wl, DEV)
     roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
-    succ, _ = _M(wl)
-    tok, par, dep = _tree_from_oracle(wl, dl, roots, succ.cpu().numpy(), L)
+    succ_np, _ = initial_M(wl)
+    tok, par, dep = _tree_from_oracle(wl, dl, roots, succ_np, L)
     tl = synth.target_logits(wl, DEV)
     synth.plant_paths(tl, tok, par, dep, synth.planted_lengths(wl))
     layers = [synth.layer_tensors(wl.scaled(L=(8, 8)), l, DEV, Lcap=Lcap) for l in range(n_layers)]
@@ -444,18 +482,9 @@ def _warm_pairs(wl):
     return synth.stream_pairs(stream)
 
 
-_WARM = {}
-
-
 def _warm_M_oracle(wl):
     """The oracle's table after five warm-up rounds (input for the tree parity)."""
-    if wl.name not in _WARM:
-        src, dst = _warm_pairs(wl)
-        s, c = synth.empty_M(wl.V, wl.W)
-        for _ in range(5):
-            s, c = oupd.update_M(s, c, src, dst)
-        _WARM[wl.name] = (s, c)
-    return _WARM[wl.name]
+    return warm_M(wl)
 
 
 def test_update_M_long_context_warmup():
@@ -489,23 +518,14 @@ def test_build_tree_block_draft_parity(V, seed):
                                 block=True)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    trees, margins = [], []
-    for b in range(wl.B):
-        rows = block[b].cpu().numpy()
-        row_fn = lambda d, f, _p, rows=rows: rows[d]
-        res = otree.draft_tree(row_fn, int(roots[b]), cfg_o)
-        ret = otree.retrieve(int(roots[b]), s_np, cfg_o["tmpl_parent"], cfg_o["tmpl_rank"])
-        trees.append(otree.merge(int(roots[b]), otree.retained_draft(res, cfg_o), ret, cfg_o["tmpl_parent"],
-                                 res.stage, int(L[b]), cfg_o))
-        margins.append(otree.draft_margins(row_fn, int(roots[b]), cfg_o))
-    ok = [b for b in range(wl.B) if margins[b] > MARGIN]
-    assert len(ok) >= wl.B - 2, f"too many near-tie requests: {margins}"
-    _compare_tree({k: v[ok] for k, v in gpu.items()}, [trees[b] for b in ok])
+    trees, margins, fns = _oracle_tree(wl, cfg_o, block, roots, s_np, L, block=True)
+    exact = _check_trees(gpu, trees, margins, fns, roots, s_np, L, cfg_o)
+    assert exact >= wl.B - 2, f"too many near-tie requests: {margins}"
 
 
-def test_ablation_without_retrieval_pads_the_graft():
-    """The no-retrieval ablation (an all-empty M): pruned trees keep their draft nodes and every grafted
-    slot is a pad (token 0, in the template's shape), as the oracle builds it."""
+def test_build_tree_empty_M_pads_the_graft():
+    """An all-empty M: pruned trees keep their draft nodes and every grafted slot is a pad (token 0, in
+    the template's shape), as the oracle builds it."""
     wl = _peaked_wl(4096, 12, 6)
     boosts = [b - math.log(128256 / 4096) for b in [0.0, 10.0, 13.0, 14.0, 15.0, 16.0, 17.0, 18.0, 20.0, 22.0, 25.0,
                                                     30.0]]
@@ -514,9 +534,77 @@ def test_ablation_without_retrieval_pads_the_graft():
     roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
     s_np, _ = synth.empty_M(wl.V, wl.W)
     gpu = _build(wl, cfg, dl, roots, torch.from_numpy(s_np).to(DEV), L)
-    trees, margins = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
-    ok = [b for b in range(wl.B) if margins[b] > MARGIN]
-    _compare_tree({k: v[ok] for k, v in gpu.items()}, [trees[b] for b in ok])
+    trees, margins, fns = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
+    exact = _check_trees(gpu, trees, margins, fns, roots, s_np, L, cfg_o)
+    assert exact >= wl.B - 2
     tok = to_np(gpu["tok"])
-    for b in ok:
+    for b in range(wl.B):
         assert (tok[b, trees[b].n_draft:] == 0).all()
+
+
+@pytest.mark.parametrize("V,seed", [(4096, 6), (128256, 8)])
+def test_build_tree_without_retrieval(V, seed):
+    """The 'w/o retrieval' ablation (graft_config_no_retrieval: K_ret = 0 at every stage): at every
+    pruning stage the draft takes the whole budget, slots a short pool cannot fill are empty nodes
+    (token -1 under the root), and the trees equal the oracle's."""
+    wl = _peaked_wl(V, 12, seed)
+    boosts = [0.0, 10.0, 13.0, 14.0, 15.0, 16.0, 17.0, 18.0, 20.0, 22.0, 25.0, 30.0]
+    if V == 4096:
+        boosts = [b - math.log(128256 / 4096) for b in boosts]
+    cfg = gb().graft_config_no_retrieval(lib_cfg(wl))
+    cfg_o = oracle_cfg(wl, no_retrieval=True)
+    assert cfg.as_dict()["K_draft"] == cfg_o["K_draft"] and cfg.n_tmpl == 0
+    dl = synth.peaked_draft_logits(wl, DEV, boosts, seed)
+    roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
+    s_np, _ = synth.zipf_M(wl.V, wl.W, seed)  # a full M that must not be read
+    gpu = _build(wl, cfg, dl, roots, torch.from_numpy(s_np).to(DEV), L)
+    trees, margins, fns = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
+    exact = _check_trees(gpu, trees, margins, fns, roots, s_np, L, cfg_o)
+    assert exact >= wl.B - 2, f"too many near-tie requests: {margins}"
+    tok, stages = to_np(gpu["tok"]), to_np(gpu["stage"])
+    assert {0, 1, 2, 3} <= set(stages.tolist())
+    for b in range(wl.B):
+        n_pool = wl.k + ([0, 1, 5, wl.D - 1][int(stages[b])]) * wl.k ** 2
+        n_real = min(wl.Kmax - 1, n_pool)
+        assert (tok[b, 1:1 + n_real] >= 0).all() and (tok[b, 1 + n_real:] == gb().EMPTY_TOKEN).all()
+    assert (tok == gb().EMPTY_TOKEN).any()  # a d0 prune left empty slots
+
+
+def test_empty_nodes_are_never_accepted_and_add_no_pair():
+    """Empty nodes of the no-retrieval ablation: even when the target's argmax at the root is token 0 (the
+    pad token a retrieval miss would carry), an empty node is not accepted, and the M update adds pairs only
+    for real nodes."""
+    wl = synth.WORKLOADS["tiny"].scaled(V=500)
+    cfg = gb().graft_config_no_retrieval(lib_cfg(wl, tau=1.5))  # c_0 <= 1 < 1.5: always pruned at d0
+    cfg_o = oracle_cfg(wl, tau=1.5, no_retrieval=True)
+    dl = synth.draft_logits(wl, DEV)
+    roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
+    s_np, c_np = synth.empty_M(wl.V, wl.W)
+    gpu = _build(wl, cfg, dl, roots, torch.from_numpy(s_np).to(DEV), L)
+    trees, _, _ = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
+    _compare_tree(gpu, trees)
+    tok, par, dep = (to_np(gpu[k]) for k in ("tok", "parent", "depth"))
+    assert int(to_np(gpu["stage"])[0]) == 0 and (tok[0] == -1).sum() == wl.Kmax - 1 - wl.k
+    tl = synth.target_logits(wl, DEV)
+    t0 = 0 if 0 not in tok[0, 1:].tolist() else min(set(range(wl.V)) - set(tok[0].tolist()))
+    tl[0, 0, t0] = tl[0, 0].max() + 5.0  # the root's argmax: token 0 unless a draft child carries it
+    Lcap = wl.lcap()
+    Q, Kc, Vc, Kt, Vt = synth.layer_tensors(wl, 0, DEV, Lcap=Lcap)
+    ptr = lambda ts: gb().layer_pointers(ts, DEV)
+    status = _status()
+    out = gb().graft_accept_compact(tl, gpu["tok"], gpu["parent"], gpu["depth"], ptr([Kc]), ptr([Vc]), ptr([Kt]),
+                                    ptr([Vt]), 1, wl.Hkv, Lcap, L.to(DEV), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oacc.accept_batch(to_np(tl), dict(tok=tok, parent=par, depth=dep))
+    for k in ("argmax", "acc_len", "path", "out_tok", "bonus"):
+        assert np.array_equal(to_np(out[k]), ref[k]), k
+    assert int(ref["argmax"][0, 0]) == t0 and int(ref["acc_len"][0]) == 1  # no empty node accepted
+    Ms, Mc = torch.from_numpy(s_np).to(DEV), torch.from_numpy(c_np).to(DEV)
+    status = _status()
+    gb().graft_update_M(Ms, Mc, gpu["tok"].view(-1), out["argmax"].view(-1), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0  # empty nodes are skipped silently
+    want_s, want_c = oupd.update_M(s_np, c_np, tok.reshape(-1), ref["argmax"].reshape(-1))
+    assert np.array_equal(to_np(Ms), want_s) and np.array_equal(to_np(Mc), want_c)
+    assert int(want_c.sum()) == 1 + wl.k

@@ -50,3 +50,19 @@ def test_stages_and_retrieval_are_exercised(lm):
         retrieved += sum(s["retrieved_accepted"] for s in steps)
     assert seen_stages == {0, 1, 2}
     assert retrieved > 0
+
+
+def test_without_retrieval_is_lossless(lm):
+    """The 'w/o retrieval' ablation (K_ret = 0, empty slots where a pruned pool runs short) emits the
+    autoregressive greedy tokens too, and its pruned steps really carry empty nodes."""
+    cfg = config.make_config(Kmax=16, D=4, k=3, V=lm.V, W=4, tau=0.3, no_retrieval=True)
+    empties, stages = 0, set()
+    for seed, sharpen in ((1, 0.3), (4, 1.0)):
+        prompt = np.random.default_rng(seed).integers(0, lm.V, 12).tolist()
+        ar, *_ = tiny_lm.greedy_ar(lm, prompt, 30, 200)
+        hy, _, _, steps = tiny_lm.greedy_hybrid(lm, prompt, 30, 200, cfg, sharpen=sharpen, seed=seed)
+        assert hy == ar
+        assert all(s["retrieved_accepted"] == 0 for s in steps)
+        empties += sum(s["empty_nodes"] for s in steps)
+        stages |= {s["stage"] for s in steps}
+    assert empties > 0 and 0 in stages

@@ -74,6 +74,69 @@ def test_hand_worked_tree(case):
     assert t.pos == [g["L"] + d for d in c["depth"]]
 
 
+@pytest.mark.parametrize("case", [0, 1, 2])
+def test_hand_worked_tree_without_retrieval(case):
+    """The 'w/o retrieval' ablation: K_ret = 0 at every stage, the draft takes the whole budget and
+    slots its pool cannot fill stay empty (hand-derived trees)."""
+    g, logits, succ = _load_hand()
+    c = g["no_retrieval_cases"][case]
+    cfg = config.make_config(Kmax=g["Kmax"], D=g["D"], k=g["k"], V=g["V"], W=g["W"],
+                             checkpoints=g["checkpoints"], tau=c["tau"], no_retrieval=True)
+    assert cfg["K_draft"] == g["no_retrieval_K_draft"] and cfg["tmpl_parent"] == [] and cfg["K_ret"] == [0, 0, 0]
+    t, res, ret = tr.build_tree(logits[0], g["root_tok"], succ, g["L"], cfg)
+    assert res.stage == c["stage"] and ret == []
+    assert t.tok == c["tok"] and t.parent == c["parent"] and t.depth == c["depth"] and t.mask == c["mask"]
+
+
+@pytest.mark.parametrize("seed,tau", [(0, 0.9), (1, 0.3), (2, 0.6), (3, 0.0)])  # stages 0, 2, 1, 2
+def test_without_retrieval_keeps_the_best_of_the_pool(seed, tau):
+    """Without retrieval a stage's draft is the top-min(Kmax - 1, |pool|) of the pool, by path scores
+    recomputed from scratch (sum of full log-softmax values along each root path), and every other
+    slot is an empty node under the root."""
+    _, logits, _ = _random_cfg_logits(seed)
+    cfg_nr = config.make_config(Kmax=40, D=5, k=3, V=64, W=4, tau=tau, no_retrieval=True)
+    rows = {}
+
+    def row_fn(d, f, path):
+        rows[tuple(path)] = (d, f)
+        return logits[0, d, f]
+
+    res = tr.draft_tree(row_fn, 5, cfg_nr)
+    t = tr.merge(5, tr.retained_draft(res, cfg_nr), [], [], res.stage, 0, cfg_nr)
+    lsm = {key: log_softmax(logits[0, d, f].astype(np.float64)) for key, (d, f) in rows.items()}
+    # every candidate the drafter produced before stopping, scored independently
+    cands = []
+    for key in rows:
+        for tok in np.argsort(-lsm[key], kind="stable")[: cfg_nr["k"]]:
+            path = list(key) + [int(tok)]
+            cands.append((sum(lsm[tuple(path[:i])][path[i]] for i in range(1, len(path))), tuple(path)))
+    n_kept = min(39, len(cands))
+    want = {p for _, p in sorted(cands, key=lambda x: -x[0])[:n_kept]}
+    # the tree's draft nodes as root paths
+    paths = []
+    for i in range(1, 1 + n_kept):
+        path, j = [], i
+        while j >= 0:
+            path.append(t.tok[j])
+            j = t.parent[j]
+        paths.append(tuple(reversed(path)))
+    assert set(paths) == want
+    assert t.tok[1 + n_kept:] == [tr.EMPTY] * (39 - n_kept)
+    assert t.parent[1 + n_kept:] == [0] * (39 - n_kept) and t.depth[1 + n_kept:] == [1] * (39 - n_kept)
+    if res.stage == 0:
+        assert n_kept == cfg_nr["k"] < 39  # a d0 prune leaves empty slots
+
+
+def test_update_skips_empty_nodes():
+    """An empty tree node (token -1) adds no pair to M; any other id outside [0, V) is an error."""
+    from oracle import update_m as um
+    s, c = um.empty_M(10, 2)
+    s2, c2 = um.update_M(s, c, np.array([3, -1, 3, -1]), np.array([4, 7, 4, 9]))
+    assert s2[3].tolist() == [4, -1] and c2[3].tolist() == [2, 0] and int(c2.sum()) == 2
+    with pytest.raises(ValueError):
+        um.update_M(s, c, np.array([3, -2]), np.array([4, 1]))
+
+
 def _random_cfg_logits(seed, B=1, Kmax=24, D=5, k=3, V=64, W=4, sharp=3.0, tau=0.3):
     rng = np.random.default_rng(seed)
     cfg = config.make_config(Kmax=Kmax, D=D, k=k, V=V, W=W, tau=tau)
@@ -229,3 +292,52 @@ def test_block_draft_children_come_from_the_shared_row():
     top = [set(np.argsort(-rows[d], kind="stable")[:k].tolist()) for d in range(D)]
     for c in res.pool:
         assert int(c.token) in top[c.depth - 1]
+
+
+def test_alternatives_reduce_to_the_oracle_without_near_ties():
+    """The near-tie enumerator used by the GPU parity tests returns exactly the oracle's tree when no
+    decision is near a tie (each hand case, and random drafts)."""
+    from tests.tree_alternatives import same_tree, valid_trees
+    g, logits, succ = _load_hand()
+    for c in g["cases"]:
+        cfg = config.make_config(Kmax=g["Kmax"], D=g["D"], k=g["k"], V=g["V"], W=g["W"],
+                                 checkpoints=g["checkpoints"], tau=c["tau"])
+        alts = valid_trees(lambda d, f, _p: logits[0, d, f], g["root_tok"], succ, g["L"], cfg, eps=1e-6)
+        t, _, _ = tr.build_tree(logits[0], g["root_tok"], succ, g["L"], cfg)
+        assert len(alts) == 1 and same_tree(alts[0], t)
+    for seed in range(3):
+        cfg, lg, _ = _random_cfg_logits(seed)
+        row_fn = lambda d, f, _p: lg[0, d, f]
+        m = tr.draft_margins(row_fn, 5, cfg)
+        alts = valid_trees(row_fn, 5, np.full((64, 4), -1, np.int32), 0, cfg, eps=m / 2)
+        t, _, _ = tr.build_tree(lg[0], 5, np.full((64, 4), -1, np.int32), 0, cfg)
+        assert len(alts) == 1 and same_tree(alts[0], t)
+
+
+def test_alternatives_cover_a_planted_cross_row_tie():
+    """Two depth-2 candidates from different drafter rows with equal probability (0.45 x 0.5): the
+    enumerator yields the oracle's tree and the one with their frontier slots swapped, whose depth-3
+    children then come from the other rows."""
+    from tests.tree_alternatives import same_tree, valid_trees
+    V, D, k = 8, 3, 2
+    rows = {(0, 0): [(3, 0.45), (5, 0.45)], (1, 0): [(1, 0.5), (2, 0.2)], (1, 1): [(4, 0.5), (6, 0.2)],
+            (2, 0): [(7, 0.6), (0, 0.2)], (2, 1): [(2, 0.7), (3, 0.1)]}
+    logits = np.zeros((D, k, V), np.float32)
+    for (d, f), pairs in rows.items():
+        logits[d, f] = _rows_from_probs(V, pairs)
+    cfg = config.make_config(Kmax=6, D=D, k=k, V=V, W=2, checkpoints=[0, 1], tau=0.0)
+    succ = np.full((V, 2), -1, np.int32)
+    row_fn = lambda d, f, _p: logits[d, f]
+    assert tr.draft_margins(row_fn, 2, cfg) < 1e-6
+    alts = valid_trees(row_fn, 2, succ, 0, cfg, eps=1e-4)
+    t, _, _ = tr.build_tree(logits, 2, succ, 0, cfg)
+    assert same_tree(alts[0], t)
+    distinct = []
+    for a in alts:
+        if not any(same_tree(a, b) for b in distinct):
+            distinct.append(a)
+    assert len(distinct) >= 2
+    # in every alternative the depth-3 nodes are children of the two tied depth-2 nodes
+    for a in distinct:
+        d2 = {i for i in range(6) if a.depth[i] == 2}
+        assert all(a.parent[i] in d2 for i in range(6) if a.depth[i] == 3)

@@ -23,6 +23,8 @@ STATUS_TOKEN_RANGE = 1
 STATUS_CACHE_OVERFLOW = 2
 STATUS_LENGTH = 4
 STATUS_TREE = 8
+STATUS_TIMEOUT = 16
+EMPTY_TOKEN = -1
 
 MAX_KMAX = 64
 MAX_CHECKPOINTS = 4
@@ -72,6 +74,7 @@ _SZ = ctypes.c_size_t
 _SIGNATURES = {
     "graft_config_init": [ctypes.POINTER(GraftConfig), _I, _I, _I, _I, _I, _I, _P, _P],
     "graft_config_validate": [ctypes.POINTER(GraftConfig)],
+    "graft_config_no_retrieval": [ctypes.POINTER(GraftConfig)],
     "graft_build_tree_workspace_size": [ctypes.POINTER(GraftConfig), _I, ctypes.POINTER(_SZ)],
     "graft_build_tree": [ctypes.POINTER(GraftConfig), _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P],
     "graft_build_tree_block": [ctypes.POINTER(GraftConfig), _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ,
@@ -175,6 +178,12 @@ def graft_config_init(Kmax: int, D: int, k: int, V: int, W: int, checkpoints: Se
     ta = (ctypes.c_float * max(1, len(taus)))(*taus)
     _check(lib().graft_config_init(ctypes.byref(cfg), Kmax, D, k, V, W, len(cps),
                                    ctypes.cast(ca, _P), ctypes.cast(ta, _P)), "graft_config_init")
+    return cfg
+
+
+def graft_config_no_retrieval(cfg: GraftConfig) -> GraftConfig:
+    """The "w/o retrieval" ablation of cfg (K_ret = 0 at every stage), edited in place and returned."""
+    _check(lib().graft_config_no_retrieval(ctypes.byref(cfg)), "graft_config_no_retrieval")
     return cfg
 
 

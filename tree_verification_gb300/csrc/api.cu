@@ -124,14 +124,12 @@ extern "C" int graft_config_validate(const GraftConfig* c) {
     if (c->K_draft[c->n_checkpoints] != c->Kmax) return GRAFT_ERR_INVALID_ARG;
     const long long full_pool = c->k + (long long)(c->D - 1) * c->k * c->k;
     if (full_pool < c->Kmax - 1) return GRAFT_ERR_INVALID_ARG;
+    // K_draft[s] - 1 may exceed the stage's pool (k + d_s k^2 candidates): the pool is then kept
+    // whole and the remaining draft slots are empty nodes (graft_config_no_retrieval)
     int need_tmpl = 0;
     for (int s = 0; s <= c->n_checkpoints; ++s) {
         const int kd = c->K_draft[s];
         if (kd < 1 || kd > c->Kmax) return GRAFT_ERR_INVALID_ARG;
-        if (s < c->n_checkpoints) {
-            const long long pool = c->k + (long long)c->checkpoint[s] * c->k * c->k;
-            if (kd - 1 > pool) return GRAFT_ERR_INVALID_ARG;
-        }
         need_tmpl = std::max(need_tmpl, c->Kmax - kd);
     }
     if (c->n_tmpl < need_tmpl || c->n_tmpl > GRAFT_MAX_KMAX) return GRAFT_ERR_INVALID_ARG;
@@ -188,6 +186,15 @@ extern "C" int graft_config_init(GraftConfig* cfg, int Kmax, int D, int k, int V
     cfg->n_tmpl = n_tmpl;
     int rc = graft::build_envelope(D, W, n_tmpl, cfg->tmpl_parent, cfg->tmpl_rank);
     if (rc != GRAFT_OK) return rc;
+    return graft_config_validate(cfg);
+}
+
+extern "C" int graft_config_no_retrieval(GraftConfig* cfg) {
+    if (cfg == nullptr) return GRAFT_ERR_INVALID_ARG;
+    const int rc = graft_config_validate(cfg);
+    if (rc != GRAFT_OK) return rc;
+    for (int s = 0; s <= cfg->n_checkpoints; ++s) cfg->K_draft[s] = cfg->Kmax;
+    cfg->n_tmpl = 0;
     return graft_config_validate(cfg);
 }
 

@@ -344,7 +344,9 @@ draft_merge_kernel(MergeParams p, const int32_t* __restrict__ root_tok, const in
     const int n_draft = p.K_draft[st];
     const int dmax = (st < p.n_cp) ? p.checkpoint[st] : p.D - 1;
     const int P = k + dmax * KK;
-    const int keep = n_draft - 1;
+    // without retrieval K_draft_s = Kmax can exceed the pool: the whole pool is kept and the
+    // remaining draft slots stay empty (token -1 under the root)
+    const int keep = min(n_draft - 1, P);
     // pool entry e: call 0 holds entries [0, k); call d >= 1 holds [k + (d-1)k^2, k + d k^2)
     auto call_of = [&](int e) { return e < k ? 0 : 1 + (e - k) / KK; };
     auto idx_of = [&](int e) { return e < k ? e : (e - k) % KK; };
@@ -371,9 +373,10 @@ draft_merge_kernel(MergeParams p, const int32_t* __restrict__ root_tok, const in
         kept_entry[tid] = 0;
     }
     __syncthreads();
-    // every slot starts as a pad under the root, so the ancestor walk below ends even on a broken input
+    // every slot starts as a pad under the root, so the ancestor walk below ends even on a broken input;
+    // draft slots past the kept pool are empty nodes
     if (tid < GRAFT_MAX_KMAX) {
-        s_tok[tid] = 0;
+        s_tok[tid] = (tid > keep && tid < n_draft) ? -1 : 0;
         s_par[tid] = tid == 0 ? -1 : 0;
     }
     // tree order among the kept: (depth asc, score desc, index asc)

@@ -72,7 +72,7 @@ __global__ void pairs_kernel(int32_t* __restrict__ succ, int32_t* __restrict__ c
     const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
     const int s = src[i], t = dst[i];
-    if (s == -1 && t == -1) return;  // no pair in this slot
+    if (s == -1) return;  // an empty slot or an empty tree node: no pair
     if (s < 0 || s >= V || t < 0 || t >= V) {
         flag_status(status, GRAFT_STATUS_TOKEN_RANGE);
         return;
