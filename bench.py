@@ -1,19 +1,43 @@
 #!/usr/bin/env python3
 """Benchmark of the hybrid-tree verify step on one or more GPUs.
 
+    python bench.py [--gpus N] [--steps K] [--warmup W]
+
 One step = graft_build_tree (prune, retrieve, merge) + graft_tree_attention
 for every layer + graft_accept_compact + graft_update_M, on synthetic inputs
-resident in HBM, replayed from one CUDA graph.  Default workload: the
-LLaMA-3-8B-shaped verify step (batch 1, 32 layers, 32/8 heads, prefix 4096,
-Kmax 64, vocab 128256, M 128256x16).
+resident in HBM, replayed from one CUDA graph.  The headline line times K
+steps of the largest single-GPU workload, the Qwen3-235B-shaped step (batch
+16, 64/4 heads, 94 layer calls over 8192-token prefixes, Kmax 64, vocab
+151936, M 151936x32; 25 GB of KV per step).  The line's ``configs`` object
+times the whole step of the four other workloads the same way (tiny,
+llama3_8b, qwen3_8b_batch, llama31_8b_long), each with its steps/s, its
+attention call against the roofline, tree attention plus KV compaction
+against the HBM roofline, the tree build, the retrieval fill and an
+end-to-end step.
 
-Prints one JSON line (rank 0).  Under torchrun every rank runs an
-independent replica of the step on its own GPU (no collective on the data
-path); ``value`` is the steps all ranks completed divided by the slowest
-rank's time.
+Every measured workload also runs end to end through the public step API
+(``e2e``): each step copies its inputs in from pinned host memory and reads
+the accepted tokens and lengths back, all inside the timed region.
+
+Under torchrun every rank runs an independent replica of the step on its own
+GPU (no collective on the data path); ``value`` is the steps all ranks
+completed divided by the slowest rank's time.
 
 ``--impl reference`` times the CPU oracle (a plain NumPy restatement of the
-method) on the host cores, on a bounded sample of the same workload.
+method) on the host cores, on bounded samples of the same workload; it never
+loads the CUDA library.  ``cpu_baseline`` in the GPU arm's line is the same
+oracle on a sample of the headline workload, and ``cpu_full_steps`` times
+whole oracle steps of the tiny and LLaMA-3-8B workloads on one host thread
+and on all of them.
+
+Other modes:
+    --mode attention --workload W [--layers N --reps R --lcap C]
+        microseconds per graft_tree_attention call of a workload
+    --mode lm_head [--rows N --d-model D --vocab V --reps R]
+        the fused lm_head argmax and sampling kernels
+    --mode cpu_step --workload W
+        one whole oracle step on the host (run by the default mode in a
+        subprocess, to fix the BLAS thread count)
 """
 from __future__ import annotations
 
@@ -34,26 +58,39 @@ if ROOT not in sys.path:
 
 METRIC = "tree-verify steps/s; tree-attention HBM GB/s vs GB300 peak; retrieval fill µs"
 UNIT = "steps/s"
+HEADLINE = "qwen3_235b"
+OTHER_CONFIGS = ["tiny", "llama3_8b", "qwen3_8b_batch", "llama31_8b_long"]
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 ATTN_SOURCES = ["attention_tc.cu", "attention_tcp.cu", "attention_tc1.cu", "attention_mma.cu", "attention.cuh",
-                "attention_api.cu",
-                "tc_ptx.cuh", "common.cuh"]
+                "attention_api.cu", "tc_ptx.cuh", "common.cuh"]
+BLAS_ENV = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
 
 
-def parse_args():
-    p = argparse.ArgumentParser(description=__doc__)
+def parse_args(argv=None):
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=3000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=50)
+    p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["graft", "reference"], default="graft")
-    p.add_argument("--workload", default="llama3_8b")
-    p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--mode", choices=["step", "attention", "lm_head", "cpu_step"], default="step")
+    p.add_argument("--workload", default=HEADLINE)
+    p.add_argument("--configs", default=",".join(OTHER_CONFIGS),
+                   help="comma-separated workloads timed beside the headline ('none' for none)")
+    p.add_argument("--e2e-steps", type=int, default=0, help="end-to-end steps (0: the same as --steps)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=20.0)
-    p.add_argument("--secondary-reps", type=int, default=20,
-                   help="replays of the attention / retrieval / tree-build graphs (0 skips them)")
-    return p.parse_args()
+    p.add_argument("--reference-budget-s", type=float, default=150.0)
+    p.add_argument("--secondary-reps", type=int, default=10,
+                   help="replays of the attention / compaction / tree-build graphs (0 skips them)")
+    # --mode attention / lm_head
+    p.add_argument("--layers", type=int, default=4)
+    p.add_argument("--reps", type=int, default=20)
+    p.add_argument("--lcap", type=int, default=0)
+    p.add_argument("--rows", type=int, default=64)
+    p.add_argument("--d-model", type=int, default=4096)
+    p.add_argument("--vocab", type=int, default=128256)
+    return p.parse_args(argv)
 
 
 def dist_env():
@@ -129,29 +166,48 @@ class ClockSampler:
                 "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
 def measured_peaks():
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    try:
-        with open(path) as f:
-            j = json.load(f)
+    j = _peaks()
+    if "hbm_gbs" in j:
         return float(j["hbm_gbs"]), "measured"
-    except (OSError, ValueError, KeyError):
-        return FALLBACK_HBM_GBS, "fallback"
+    return FALLBACK_HBM_GBS, "fallback"
 
 
-def measured_tensor_peak():
-    """Dense bf16 TFLOP/s as a burst (the attention call is timed on its own)."""
-    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    try:
-        with open(path) as f:
-            j = json.load(f)
-        return float(j["bf16_tflops"]), "measured"
-    except (OSError, ValueError, KeyError):
-        return FALLBACK_BF16_TFLOPS, "fallback"
+def measured_tensor_peak(sustained: bool = False):
+    """Dense bf16 TFLOP/s: the burst figure (a kernel timed on its own) or the sustained one."""
+    j = _peaks()
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    if key in j:
+        return float(j[key]), "measured"
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 # exp2 results per clock per SM of the special-function unit (four per SM sub-partition)
 EX2_PER_CLOCK_PER_SM = 16
+
+
+def attention_bytes_per_call(wl, L0) -> float:
+    """Compulsory bytes of one layer call: prefix K and V, tree K and V, Q in, O out (bf16)."""
+    d = wl.head_dim
+    prefix = 2 * int(L0.sum()) * wl.Hkv * d * 2
+    tree_kv = 2 * wl.B * wl.Kmax * wl.Hkv * d * 2
+    q_o = 2 * wl.B * wl.Kmax * wl.Hq * d * 2
+    return float(prefix + tree_kv + q_o)
+
+
+def compaction_bytes_per_step(wl, acc_len) -> float:
+    """Bytes one step's KV compaction must move: every accepted node's K and V row (Hkv x 128 bf16) read
+    from the tree KV and written into the cache, in every layer."""
+    rows = int(sum(int(x) for x in acc_len))
+    return float(rows * 2 * 2 * wl.Hkv * wl.head_dim * 2 * wl.n_layers)
 
 
 def attention_roofline(wl, L0, t_call, clocks, sms):
@@ -170,7 +226,9 @@ def attention_roofline(wl, L0, t_call, clocks, sms):
     fractions = {"hbm": t_hbm / t_call, "tensor": t_tc / t_call, "sfu": t_sfu / t_call}
     if t_tc > t_hbm:
         r = {"bound": "tensor", "achieved": flops / t_call / 1e12, "peak": tc, "unit": "TFLOP/s",
-             "peak_source": f"{tc_kind} bf16_tflops"}
+             "peak_source": f"{tc_kind} bf16_tflops (burst)"}
+        tcs, _ = measured_tensor_peak(sustained=True)
+        r["frac_of_sustained"] = r["achieved"] / tcs
     else:
         r = {"bound": "hbm", "achieved": nbytes / t_call / 1e9, "peak": hbm, "unit": "GB/s",
              "peak_source": f"{hbm_kind} hbm_gbs"}
@@ -205,6 +263,10 @@ def recorded_traffic(workload: str):
 
 
 def blas_threads() -> int:
+    for k in BLAS_ENV:
+        v = os.environ.get(k)
+        if v and v.isdigit():
+            return int(v)
     try:
         from threadpoolctl import threadpool_info
         n = [d.get("num_threads", 0) for d in threadpool_info() if d.get("user_api") == "blas"]
@@ -216,100 +278,193 @@ def blas_threads() -> int:
 
 
 # ----------------------------------------------------------------------------------------------
-# CPU oracle timing (the reference arm and the cpu_baseline leg)
+# CPU oracle (the reference arm, cpu_baseline and cpu_full_steps).  Nothing here loads the CUDA
+# library: inputs come from the seeded generators and the oracle's own tree.
 # ----------------------------------------------------------------------------------------------
 
-class OracleSample:
-    """The oracle's step on host copies of a workload's inputs, timed piecewise.
-
-    A sample runs the whole tree build, acceptance and M update for the
-    sampled requests, the attention of one layer on ``attn_kv_heads`` KV
-    heads, and the compaction of one layer; the step time is extrapolated to
-    every request, KV head and layer.
-    """
-
-    def __init__(self, wl, inputs, max_requests=4):
-        import numpy as np
-        from oracle import config as oconfig
-        self.np = np
-        self.wl = wl
-        self.cfg = oconfig.make_config(Kmax=wl.Kmax, D=wl.D, k=wl.k, V=wl.V, W=wl.W, checkpoints=wl.checkpoints,
-                                       tau=wl.tau)
-        self.reqs = list(range(min(wl.B, max_requests)))
-        dl, tl, roots, L, succ, cnt, layer0 = inputs
-        self.dl = dl[self.reqs].float().cpu().numpy()
-        self.tl = tl[self.reqs].cpu().numpy()
-        self.roots = roots[self.reqs].cpu().numpy()
-        self.L = L[self.reqs].cpu().numpy()
-        self.succ = succ.cpu().numpy()
-        self.cnt = cnt.cpu().numpy()
-        Q, Kc, Vc, Kt, Vt = layer0
-        r = self.reqs
-        self.Q = Q[r].float().cpu().numpy()
-        self.Kc = Kc[r].float().cpu().numpy()
-        self.Vc = Vc[r].float().cpu().numpy()
-        self.Kt = Kt[r].float().cpu().numpy()
-        self.Vt = Vt[r].float().cpu().numpy()
-
-    def step(self, attn_kv_heads: int):
-        """Run one sampled step; returns (extrapolated seconds, seconds actually spent)."""
-        np = self.np
-        from oracle import accept as oacc
-        from oracle import attention as oatt
-        from oracle import tree as otree
-        from oracle import update_m as oupd
-        wl, cfg = self.wl, self.cfg
-        t0 = time.perf_counter()
-        tree = otree.build_tree_batch(self.dl, self.roots, self.succ, self.L, cfg)
-        t1 = time.perf_counter()
-        group = wl.Hq // wl.Hkv
-        heads = list(range(attn_kv_heads * group))
-        for b in range(len(self.reqs)):
-            lb = int(self.L[b])
-            oatt.tree_attention_one(self.Q[b], self.Kc[b, :lb], self.Vc[b, :lb], self.Kt[b], self.Vt[b], lb,
-                                    tree["mask"][b], 1 / math.sqrt(wl.head_dim), heads=heads)
-        t2 = time.perf_counter()
-        a = oacc.accept_batch(self.tl, tree)
-        Kc, Vc = self.Kc.copy(), self.Vc.copy()
-        oacc.compact(Kc, Vc, self.Kt, self.Vt, self.L.astype(np.int64), a["path"], a["acc_len"])
-        t3 = time.perf_counter()
-        oupd.update_M(self.succ, self.cnt, tree["tok"].reshape(-1), a["argmax"].reshape(-1))
-        t4 = time.perf_counter()
-        scale_req = wl.B / len(self.reqs)
-        attn = (t2 - t1) * (wl.Hkv / attn_kv_heads) * wl.n_layers
-        est = (t1 - t0) * scale_req + attn * scale_req + (t3 - t2) * scale_req + (t4 - t3) * scale_req
-        return est, t4 - t0
-
-    def describe(self, attn_kv_heads, n_steps):
-        return (f"oracle (NumPy, float64 attention) on {len(self.reqs)} of {self.wl.B} requests: full tree build, "
-                f"acceptance, compaction of one layer and M update; attention of layer 0 on {attn_kv_heads} of "
-                f"{self.wl.Hkv} KV heads; extrapolated to all requests, heads and {self.wl.n_layers} layers; "
-                f"{n_steps} sampled steps")
+def oracle_inputs(wl, dev, layers):
+    """Host copies of one step's inputs for the oracle: drafter and target logits (the target's planted
+    on the oracle's tree), roots, lengths, M and the listed layers' Q / caches / tree KV (float32)."""
+    import numpy as np
+    from oracle import config as oconfig
+    from oracle import tree as otree
+    from oracle import update_m as oupd
+    from tree_verification_gb300 import synth
+    cfg = oconfig.make_config(Kmax=wl.Kmax, D=wl.D, k=wl.k, V=wl.V, W=wl.W, checkpoints=wl.checkpoints, tau=wl.tau)
+    dl = synth.draft_logits(wl, dev).cpu().numpy()
+    roots = synth.root_tokens(wl).numpy()
+    L = synth.prefix_lengths(wl).numpy()
+    if wl.M_init == "zipf":
+        succ, cnt = synth.zipf_M(wl.V, wl.W, wl.seed + 5)
+    else:
+        succ, cnt = synth.empty_M(wl.V, wl.W)
+        if wl.M_init == "warm":
+            src, dst = synth.stream_pairs(synth.token_stream(wl.Lmax, wl.V, wl.seed + 41))
+            for _ in range(5):
+                succ, cnt = oupd.update_M(succ, cnt, src, dst)
+    tree = otree.build_tree_batch(dl, roots, succ, L, cfg)
+    tl_t = synth.target_logits(wl, dev)
+    synth.plant_paths(tl_t, tree["tok"], tree["parent"], tree["depth"], synth.planted_lengths(wl))
+    tl = tl_t.cpu().numpy()
+    del tl_t
+    Lcap = wl.lcap(1)
+    lay = {}
+    for l in layers:
+        lay[l] = [x.float().cpu().numpy() for x in synth.layer_tensors(wl, l, dev, Lcap=Lcap)]
+    return dict(cfg=cfg, dl=dl, roots=roots, L=L.astype(np.int64), succ=succ, cnt=cnt, tl=tl, layers=lay)
 
 
-def oracle_timing(wl, inputs, budget_s: float, n_steps: int):
-    samp = OracleSample(wl, inputs)
-    est, spent = samp.step(1)  # one untimed pass sizes the sample
-    kvh = wl.Hkv
-    per = spent * max(1, wl.Hkv)  # rough cost of a step with every KV head
-    if per * n_steps > budget_s:
-        kvh = 1
-    ests = []
-    t_start = time.perf_counter()
-    for _ in range(n_steps):
-        e, _ = samp.step(kvh)
+def oracle_step_sample(wl, inp, attn_requests, compact_layers):
+    """One sampled oracle step: the whole tree build, acceptance and M update for every request, the
+    attention of one layer call for ``attn_requests`` requests (all heads), and the compaction of
+    ``compact_layers`` layers.  Returns (estimated seconds of a whole step, seconds spent, seconds of the
+    sampled attention): attention scales by requests and layers, compaction by layers."""
+    from oracle import accept as oacc
+    from oracle import attention as oatt
+    from oracle import tree as otree
+    from oracle import update_m as oupd
+    l0 = min(inp["layers"])
+    Q, Kc, Vc, Kt, Vt = inp["layers"][l0]
+    scale = 1 / math.sqrt(wl.head_dim)
+    t0 = time.perf_counter()
+    tree = otree.build_tree_batch(inp["dl"], inp["roots"], inp["succ"], inp["L"], inp["cfg"])
+    t1 = time.perf_counter()
+    for b in attn_requests:
+        lb = int(inp["L"][b])
+        oatt.tree_attention_one(Q[b], Kc[b, :lb], Vc[b, :lb], Kt[b], Vt[b], lb, tree["mask"][b], scale)
+    t2 = time.perf_counter()
+    a = oacc.accept_batch(inp["tl"], tree)
+    t3 = time.perf_counter()
+    for l in sorted(inp["layers"])[:compact_layers]:
+        _, Kc_l, Vc_l, Kt_l, Vt_l = inp["layers"][l]
+        oacc.compact(Kc_l.copy(), Vc_l.copy(), Kt_l, Vt_l, inp["L"], a["path"], a["acc_len"])
+    t4 = time.perf_counter()
+    oupd.update_M(inp["succ"], inp["cnt"], tree["tok"].reshape(-1), a["argmax"].reshape(-1))
+    t5 = time.perf_counter()
+    attn = (t2 - t1) * (wl.B / max(1, len(attn_requests))) * wl.n_layers
+    compact = (t4 - t3) * (wl.n_layers / max(1, compact_layers))
+    est = (t1 - t0) + attn + (t3 - t2) + compact + (t5 - t4)
+    return est, t5 - t0, t2 - t1
+
+
+def oracle_whole_step(wl, inp):
+    """One whole oracle step (every request, every layer's attention and compaction); seconds."""
+    from oracle import step as ostep
+    n = wl.n_layers
+    lay = [inp["layers"][l] for l in range(n)]
+    Kc = [x[1].copy() for x in lay]
+    Vc = [x[2].copy() for x in lay]
+    t0 = time.perf_counter()
+    ostep.verify_step(inp["cfg"], inp["dl"], inp["roots"], inp["succ"], inp["cnt"], inp["L"], [x[0] for x in lay],
+                      Kc, Vc, [x[3] for x in lay], [x[4] for x in lay], inp["tl"], 1 / math.sqrt(wl.head_dim))
+    return time.perf_counter() - t0
+
+
+def calibrated_requests(wl, inp, seconds: float):
+    """How many requests' attention (of one layer call) a sample may include to take about `seconds`
+    (one calibration sample with one request; the stages other than attention always run whole)."""
+    _, spent, t_attn = oracle_step_sample(wl, inp, [0], 1)
+    per_req = max(t_attn, 1e-4)
+    n = int(max(1, min(wl.B, (seconds - (spent - t_attn)) / per_req)))
+    return n, spent
+
+
+def run_cpu_step(args):
+    """--mode cpu_step: whole oracle steps of one workload on this process's BLAS threads (one JSON line)."""
+    import torch
+    from tree_verification_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    dev = torch.device("cpu")
+    inp = oracle_inputs(wl, dev, range(wl.n_layers))
+    n = max(1, args.steps)
+    secs = [oracle_whole_step(wl, inp) for _ in range(n)]
+    t = statistics.median(secs)
+    print(json.dumps({"workload": wl.name, "steps_per_s": 1.0 / t, "seconds_per_step": t, "steps": n,
+                      "threads": blas_threads(), "kind": "oracle", "sample": "whole steps"}), flush=True)
+
+
+def cpu_full_steps(budget_s: float):
+    """Whole oracle steps of the tiny and LLaMA-3-8B workloads on one host thread and on every host thread,
+    each in a subprocess whose BLAS thread count is fixed before NumPy loads."""
+    out = {}
+    for name, steps in (("tiny", 5), ("llama3_8b", 1)):
+        for label, threads in (("one_thread", 1), ("all_threads", os.cpu_count() or 1)):
+            env = dict(os.environ)
+            for k in BLAS_ENV:
+                env[k] = str(threads)
+            cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--mode", "cpu_step", "--workload", name,
+                   "--steps", str(steps)]
+            try:
+                r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=budget_s)
+                line = [x for x in r.stdout.splitlines() if x.startswith("{")]
+                out.setdefault(name, {})[label] = json.loads(line[-1]) if line else {"error": r.stderr[-300:]}
+            except subprocess.TimeoutExpired:
+                out.setdefault(name, {})[label] = {"error": f"over {budget_s:.0f} s"}
+    return out
+
+
+def run_reference(args):
+    """The reference arm: the CPU oracle on the host cores (rank 0 only), never the CUDA library."""
+    world, rank, local = dist_env()
+    if rank != 0:
+        return  # the reference arm runs once, on rank 0
+    import torch
+    from tree_verification_gb300 import synth
+    wl = synth.WORKLOADS[args.workload]
+    # the same seeded inputs as the GPU arm: drawn with torch's generator on the GPU when there is one
+    # (torch plumbing only), then copied to the host
+    dev = torch.device(f"cuda:{local}") if torch.cuda.is_available() else torch.device("cpu")
+    inp = oracle_inputs(wl, dev, [0])
+    if dev.type == "cuda":
+        torch.cuda.empty_cache()
+    # each step is a bounded sample: the whole tree build, acceptance and M update, the compaction of one
+    # layer, and one layer call's attention for as many requests as fit this run's time budget
+    per_step = args.reference_budget_s / max(1, args.steps + min(args.warmup, 1))
+    n_req, _ = calibrated_requests(wl, inp, per_step)
+    reqs = list(range(n_req))
+    for _ in range(min(args.warmup, 1)):
+        oracle_step_sample(wl, inp, reqs, 1)
+    ests, spent = [], []
+    for _ in range(args.steps):
+        e, s, _ = oracle_step_sample(wl, inp, reqs, 1)
         ests.append(e)
-        if time.perf_counter() - t_start > budget_s:
-            break
+        spent.append(s)
     value = len(ests) / sum(ests)
-    return value, samp.describe(kvh, len(ests))
+    ms_sample = 1000.0 * sum(spent) / len(spent)
+    desc = (f"oracle (NumPy, float64 attention) on {os.cpu_count()} host cores; each timed step is one sample: the "
+            f"whole tree build, acceptance and M update for all {wl.B} requests, the compaction of 1 of "
+            f"{wl.n_layers} layers, and one layer call's attention for {n_req} of {wl.B} requests (all heads)")
+    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_sample, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": workload_config(wl, world),
+           "extrapolated": {"value_is": "whole-step throughput estimated from the samples",
+                            "ms_per_step_is": "measured wall time of one timed sample",
+                            "attention_scale": wl.B / n_req * wl.n_layers, "compaction_scale": wl.n_layers,
+                            "estimated_ms_per_whole_step": 1000.0 / value},
+           "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc},
+           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
 
 
 # ----------------------------------------------------------------------------------------------
 # GPU arm
 # ----------------------------------------------------------------------------------------------
 
+def workload_config(wl, world=1):
+    """The workload's sizes as the JSON line's config (the same object in both arms)."""
+    from tree_verification_gb300 import synth
+    gb_step = attention_bytes_per_call(wl, synth.prefix_lengths(wl)) * wl.n_layers / 1e9
+    return {"workload": wl.name, "batch": wl.B, "layers": wl.n_layers, "heads_q_kv": [wl.Hq, wl.Hkv],
+            "head_dim": wl.head_dim, "prefix": list(wl.L), "Kmax": wl.Kmax, "draft_depth_topk": [wl.D, wl.k],
+            "vocab": wl.V, "M_width": wl.W, "tau": wl.tau, "checkpoints": list(wl.checkpoints),
+            "parallelism": "replicas" if world > 1 else "single GPU", "accumulate": "fp32",
+            "l2": f"inputs larger than L2: {gb_step:.2f} GB of attention operands per step in distinct per-layer "
+                  f"buffers"}
+
+
 def make_inputs(wl, dev, gb, synth):
+    """A workload's device inputs; the target logits get their planted paths on the GPU's own tree."""
     import torch
     cfg = gb.graft_config_init(wl.Kmax, wl.D, wl.k, wl.V, wl.W, list(wl.checkpoints), wl.tau)
     Lcap = wl.lcap(1)
@@ -361,21 +516,235 @@ def input_arena(seg_tensors, dev):
     return arena, segs, views
 
 
-def attention_bytes_per_call(wl, L0) -> float:
-    """Compulsory bytes of one layer call: prefix K and V, tree K and V, Q in, O out (bf16)."""
-    d = wl.head_dim
-    prefix = 2 * int(L0.sum()) * wl.Hkv * d * 2
-    tree_kv = 2 * wl.B * wl.Kmax * wl.Hkv * d * 2
-    q_o = 2 * wl.B * wl.Kmax * wl.Hq * d * 2
-    return float(prefix + tree_kv + q_o)
+def _timed(g, reps):
+    """Seconds of reps back-to-back replays of graph g (CUDA events on the current stream)."""
+    import torch
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    s.record()
+    for _ in range(reps):
+        g.replay()
+    e.record()
+    e.synchronize()
+    return s.elapsed_time(e) / 1000.0
+
+
+def _timed_steps(g, reps):
+    """Total seconds of reps back-to-back replays, and each replay's milliseconds (an event before every
+    replay and one after the last, on the current stream)."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
+    torch.cuda.synchronize()
+    for i in range(reps):
+        ev[i].record()
+        g.replay()
+    ev[reps].record()
+    ev[reps].synchronize()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
+    return ev[0].elapsed_time(ev[reps]) / 1000.0, per
+
+
+def _capture(fn):
+    import torch
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        fn()  # warm the launch path outside capture
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+class WorkloadBench:
+    """One workload's whole step on the GPU: inputs resident in HBM (one device arena for every per-step
+    input, mirrored by a pinned host arena for the end-to-end step), the step and its parts captured in
+    CUDA graphs."""
+
+    def __init__(self, wl, dev):
+        import torch
+        from tree_verification_gb300 import binding as gb
+        from tree_verification_gb300 import synth
+        from tree_verification_gb300.step import VerifyStep
+        self.wl, self.dev, self.gb = wl, dev, gb
+        cfg, Lcap, dl, roots, L0, M_succ, M_cnt, layers, tl = make_inputs(wl, dev, gb, synth)
+        self.cfg, self.Lcap, self.M_succ, self.M_cnt = cfg, Lcap, M_succ, M_cnt
+        # every per-step input in one arena, segment by segment in the order the step consumes them
+        # (drafter logits, roots and lengths; then each layer's Q and tree K/V; then the target logits)
+        seg_tensors = [("tree", [dl, roots, L0])] + [(l, [layers[l][0], layers[l][3], layers[l][4]])
+                                                      for l in range(wl.n_layers)] + [("accept", [tl])]
+        self.arena, self.segs, views = input_arena(seg_tensors, dev)
+        del dl, tl
+        self.dl, self.roots, self.L0 = views["tree"]
+        self.tl = views["accept"][0]
+        self.Q = [views[l][0] for l in range(wl.n_layers)]
+        Kc = [layers[l][1] for l in range(wl.n_layers)]
+        Vc = [layers[l][2] for l in range(wl.n_layers)]
+        Kt = [views[l][1] for l in range(wl.n_layers)]
+        Vt = [views[l][2] for l in range(wl.n_layers)]
+        del layers
+        torch.cuda.empty_cache()
+        self.step = VerifyStep(cfg, wl.B, wl.Hq, wl.Hkv, wl.n_layers, Lcap, dev, Kc, Vc, Kt, Vt)
+        self.L = self.L0.clone()
+        n0 = gb.graft_launch_count()
+        self.graph = _capture(self._body)
+        self.launches_per_step = gb.graft_launch_count() - n0
+
+    def _body(self):
+        self.L.copy_(self.L0)
+        self.step.run(self.dl, self.roots, self.M_succ, self.M_cnt, self.L, self.Q, self.tl)
+
+    def time_steps(self, reps, warmup):
+        for _ in range(max(3, warmup)):
+            self.graph.replay()
+        return _timed_steps(self.graph, reps)
+
+    def parts(self, reps):
+        """Seconds per attention call, per acceptance + compaction call (the argmax given), per tree build
+        and per retrieval fill, each from its own captured graph."""
+        import torch
+        gb, st, wl = self.gb, self.step, self.wl
+
+        def attn():
+            for l in range(wl.n_layers):
+                gb.graft_tree_attention(self.Q[l], st.Kc[l], st.Vc[l], st.Kt[l], st.Vt[l], self.L0, st.tree["mask"],
+                                        st.scale, O=st.O, status=st.status, ws=st.ws_attn)
+
+        def compact():
+            self.L.copy_(self.L0)
+            gb.graft_accept_compact(None, st.tree["tok"], st.tree["parent"], st.tree["depth"], st.Kc_ptrs,
+                                    st.Vc_ptrs, st.Kt_ptrs, st.Vt_ptrs, wl.n_layers, wl.Hkv, self.Lcap, self.L,
+                                    out=st.acc, status=st.status, ws=st.ws_acc, argmax=st.acc["argmax"], V=wl.V)
+
+        n_rep = 20
+        ret_out = torch.empty(wl.B, max(1, self.cfg.n_tmpl), dtype=torch.int32, device=self.dev)
+
+        def retrieve():
+            for _ in range(n_rep):
+                gb.graft_retrieve(self.cfg, self.roots, self.M_succ, ret_tok=ret_out)
+
+        def tree():
+            for _ in range(n_rep):
+                gb.graft_build_tree(self.cfg, self.dl, self.roots, self.M_succ, self.L0, out=st.tree, ws=st.ws_tree)
+
+        self.graph.replay()  # one step fills the tree, argmax and lengths the parts read
+        torch.cuda.synchronize()
+        out = {}
+        for name, fn, per in (("attention", attn, wl.n_layers), ("compaction", compact, 1),
+                              ("retrieval", retrieve, n_rep), ("tree", tree, n_rep)):
+            g = _capture(fn)
+            g.replay()
+            out[name] = _timed(g, reps) / (reps * per)
+            del g
+        # the compaction graph advanced L and rewrote the accept outputs; one more step restores them
+        self.graph.replay()
+        torch.cuda.synchronize()
+        return out
+
+    def e2e(self, steps):
+        """Seconds for `steps` end-to-end steps through VerifyStep.run: every step copies its inputs from
+        pinned host memory (one copy per stage segment on a copy stream, each stage waiting only for its
+        own segment) and reads the accepted tokens and lengths back; one captured graph per step."""
+        import torch
+        wl, st = self.wl, self.step
+        host_arena = self.arena.cpu().pin_memory()
+        out_host = torch.empty(wl.B, wl.Kmax, dtype=torch.int32).pin_memory()
+        len_host = torch.empty(wl.B, dtype=torch.int32).pin_memory()
+        h2d = sum(s1 - s0 for s0, s1 in self.segs.values())
+        d2h = out_host.numel() * 4 + len_host.numel() * 4
+        copy_stream = torch.cuda.Stream(device=self.dev)
+        seg_ready = {k: torch.cuda.Event() for k in self.segs}
+        arena = self.arena
+
+        def body():
+            main = torch.cuda.current_stream()
+            copy_stream.wait_stream(main)
+            with torch.cuda.stream(copy_stream):
+                for k, (s0, s1) in self.segs.items():
+                    arena[s0:s1].copy_(host_arena[s0:s1], non_blocking=True)
+                    seg_ready[k].record()
+            main.wait_event(seg_ready["tree"])
+            self.L.copy_(self.L0)
+            st.run(self.dl, self.roots, self.M_succ, self.M_cnt, self.L, self.Q, self.tl,
+                   inputs_ready=lambda k: main.wait_event(seg_ready[k]))
+            out_host.copy_(st.acc["out_tok"], non_blocking=True)
+            len_host.copy_(st.acc["acc_len"], non_blocking=True)
+
+        body()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            body()
+
+        def one():
+            g.replay()
+            torch.cuda.current_stream().synchronize()
+
+        for _ in range(3):
+            one()
+        t0 = time.perf_counter()
+        for _ in range(steps):
+            one()
+        t = time.perf_counter() - t0
+        del g, host_arena
+        return t, h2d, d2h
+
+    def acc_len(self):
+        return self.step.acc["acc_len"].cpu().tolist()
+
+    def status(self):
+        return int(self.step.status.item())
+
+    def release(self):
+        import torch
+        del self.graph, self.step, self.arena, self.dl, self.tl, self.Q, self.roots, self.L0, self.L
+        del self.M_succ, self.M_cnt
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def workload_report(wb, parts, clocks, sms, t_e2e, n_e2e, h2d, d2h, per_ms=None):
+    """The per-workload object: step times, the attention call's roofline, attention + compaction against
+    the HBM roofline, tree build and retrieval fill, and the end-to-end step."""
+    import torch
+    wl = wb.wl
+    L0 = wb.L0.cpu()
+    rep = {}
+    if per_ms:
+        q = statistics.quantiles(per_ms, n=10) if len(per_ms) >= 10 else [min(per_ms)] + [float("nan")] * 7 + [max(per_ms)]
+        med = statistics.median(per_ms)
+        rep.update({"steps_per_s": 1000.0 / med, "step_ms": {"median": med, "p10": q[0], "p90": q[8]},
+                    "timed_steps": len(per_ms)})
+    t_attn = parts["attention"]
+    roof = attention_roofline(wl, L0, t_attn, clocks, sms)
+    roof.update({"kernel": "graft_tree_attention (one layer call)", "call_us": t_attn * 1e6,
+                 "traffic": recorded_traffic(wl.name)})
+    rep["attention"] = roof
+    hbm, hbm_kind = measured_peaks()
+    b_attn = attention_bytes_per_call(wl, L0) * wl.n_layers
+    b_comp = compaction_bytes_per_step(wl, wb.acc_len())
+    t_ac = t_attn * wl.n_layers + parts["compaction"]
+    rep["attention_compaction"] = {"bound": "hbm", "bytes_per_step": b_attn + b_comp,
+                                   "compaction_bytes_per_step": b_comp, "seconds_per_step": t_ac,
+                                   "compaction_us": parts["compaction"] * 1e6,
+                                   "achieved": (b_attn + b_comp) / t_ac / 1e9, "peak": hbm, "unit": "GB/s",
+                                   "frac": (b_attn + b_comp) / t_ac / 1e9 / hbm, "peak_source": f"{hbm_kind} hbm_gbs"}
+    rep["build_tree_us"] = parts["tree"] * 1e6
+    rep["retrieval_fill_us"] = parts["retrieval"] * 1e6
+    if n_e2e > 0:
+        rep["e2e"] = {"value": n_e2e / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    rep["launches_per_step"] = wb.launches_per_step
+    rep["device_status"] = wb.status()
+    rep["config"] = workload_config(wl)
+    return rep
 
 
 def run_graft(args):
     import torch
     import torch.distributed as dist
     from tree_verification_gb300 import _build, synth
-    from tree_verification_gb300 import binding as gb
-    from tree_verification_gb300.step import VerifyStep
 
     world, rank, local = dist_env()
     if world > 1:
@@ -383,82 +752,14 @@ def run_graft(args):
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
     _build.build()
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
     wl = synth.WORKLOADS[args.workload]
-    cfg, Lcap, dl, roots, L0, M_succ, M_cnt, layers, tl = make_inputs(wl, dev, gb, synth)
-    # Every per-step input lives in one device arena, segment by segment in the order the step
-    # consumes them (drafter logits, roots and lengths; then each layer's Q and tree K/V; then the
-    # target logits), mirrored by one pinned host arena: the end-to-end step streams each segment
-    # in with one copy while earlier stages run.
-    seg_tensors = [("tree", [dl, roots, L0])] + [(l, [layers[l][0], layers[l][3], layers[l][4]])
-                                                  for l in range(wl.n_layers)] + [("accept", [tl])]
-    arena, segs, views = input_arena(seg_tensors, dev)
-    dl, roots, L0 = views["tree"]
-    tl = views["accept"][0]
-    layers = [(views[l][0], layers[l][1], layers[l][2], views[l][1], views[l][2]) for l in range(wl.n_layers)]
-    Q = [x[0] for x in layers]
-    step = VerifyStep(cfg, wl.B, wl.Hq, wl.Hkv, wl.n_layers, Lcap, dev, [x[1] for x in layers],
-                      [x[2] for x in layers], [x[3] for x in layers], [x[4] for x in layers])
-    L = L0.clone()
+    n_e2e = args.e2e_steps if args.e2e_steps > 0 else args.steps
 
-    def body():
-        L.copy_(L0)
-        step.run(dl, roots, M_succ, M_cnt, L, Q, tl)
-
-    side = torch.cuda.Stream(device=dev)
-    side.wait_stream(torch.cuda.current_stream())
-    with torch.cuda.stream(side):
-        body()
-    torch.cuda.current_stream().wait_stream(side)
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    n0 = gb.graft_launch_count()
-    with torch.cuda.graph(graph):
-        body()
-    launches_per_step = gb.graft_launch_count() - n0
-
-    # attention alone (every layer call of a step), for the roofline
-    attn_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(attn_graph):
-        for l in range(wl.n_layers):
-            gb.graft_tree_attention(Q[l], step.Kc[l], step.Vc[l], step.Kt[l], step.Vt[l], L0, step.tree["mask"],
-                                    step.scale, O=step.O, status=step.status, ws=step.ws_attn)
-    # retrieval fill alone and the whole tree build
-    n_rep = 100
-    ret_out = torch.empty(wl.B, max(1, cfg.n_tmpl), dtype=torch.int32, device=dev)
-    ret_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(ret_graph):
-        for _ in range(n_rep):
-            gb.graft_retrieve(cfg, roots, M_succ, ret_tok=ret_out)
-    tree_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(tree_graph):
-        for _ in range(n_rep):
-            gb.graft_build_tree(cfg, dl, roots, M_succ, L0, out=step.tree, ws=step.ws_tree)
-
-    def timed(g, reps):
-        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        s.record()
-        for _ in range(reps):
-            g.replay()
-        e.record()
-        e.synchronize()
-        return s.elapsed_time(e) / 1000.0
-
-    def timed_steps(g, reps):
-        """Total seconds of reps back-to-back replays, and each replay's milliseconds (an event
-        before every replay and one after the last)."""
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(reps + 1)]
-        torch.cuda.synchronize()
-        for i in range(reps):
-            ev[i].record()
-            g.replay()
-        ev[reps].record()
-        ev[reps].synchronize()
-        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(reps)]
-        return ev[0].elapsed_time(ev[reps]) / 1000.0, per
-
+    # ---------------------------------------------------------------- headline: K timed steps
+    wb = WorkloadBench(wl, dev)
     for _ in range(max(3, args.warmup)):
-        graph.replay()
+        wb.graph.replay()
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -470,210 +771,175 @@ def run_graft(args):
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    t_main, per_step_ms = timed_steps(graph, args.steps)
+    t_main, per_step_ms = _timed_steps(wb.graph, args.steps)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     clocks = sampler.stop()
     t_max = slowest_over_ranks(t_main, dev, world)
-    status = int(step.status.item())
-
-    # secondary timings (after the main timed region)
-    t_attn = t_ret = t_tree = float("nan")
-    if args.secondary_reps > 0:
-        reps_attn = max(args.secondary_reps, min(args.steps, 300))
-        t_attn = timed(attn_graph, reps_attn) / (reps_attn * wl.n_layers)
-        t_ret = timed(ret_graph, args.secondary_reps) / (args.secondary_reps * n_rep)
-        t_tree = timed(tree_graph, args.secondary_reps) / (args.secondary_reps * n_rep)
-
-    # End to end through the public step API: every step copies its inputs in from pinned host
-    # memory (one copy per segment, on a copy stream, each stage waiting only for its own segment)
-    # and reads its accepted tokens and lengths back; the whole thing is one captured graph.
-    host_arena = arena.cpu().pin_memory()
-    out_host = torch.empty(wl.B, wl.Kmax, dtype=torch.int32).pin_memory()
-    len_host = torch.empty(wl.B, dtype=torch.int32).pin_memory()
-    h2d = sum(s1 - s0 for s0, s1 in segs.values())
-    d2h = out_host.numel() * 4 + len_host.numel() * 4
-    copy_stream = torch.cuda.Stream(device=dev)
-    seg_ready = {k: torch.cuda.Event() for k in segs}
-
-    def e2e_body():
-        main = torch.cuda.current_stream()
-        copy_stream.wait_stream(main)
-        with torch.cuda.stream(copy_stream):
-            for k, (s0, s1) in segs.items():
-                arena[s0:s1].copy_(host_arena[s0:s1], non_blocking=True)
-                seg_ready[k].record()
-        main.wait_event(seg_ready["tree"])
-        L.copy_(L0)
-        step.run(dl, roots, M_succ, M_cnt, L, Q, tl, inputs_ready=lambda k: main.wait_event(seg_ready[k]))
-        out_host.copy_(step.acc["out_tok"], non_blocking=True)
-        len_host.copy_(step.acc["acc_len"], non_blocking=True)
-
-    e2e_body()
-    torch.cuda.synchronize()
-    e2e_graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(e2e_graph):
-        e2e_body()
-
-    def e2e_step():
-        e2e_graph.replay()
-        torch.cuda.current_stream().synchronize()
-
-    n_e2e = min(args.e2e_steps, args.steps)
-    t_e2e = float("nan")
-    if n_e2e > 0:
-        for _ in range(3):
-            e2e_step()
-        t0 = time.perf_counter()
-        for _ in range(n_e2e):
-            e2e_step()
-        t_e2e = time.perf_counter() - t0
+    status = wb.status()
+    reps = max(1, args.secondary_reps)
+    parts = wb.parts(reps)
+    t_e2e, h2d, d2h = wb.e2e(n_e2e) if n_e2e > 0 else (float("nan"), 0, 0)
     t_e2e = slowest_over_ranks(t_e2e, dev, world)
+    head = workload_report(wb, parts, clocks, sms, t_e2e, n_e2e, h2d, d2h, per_step_ms)
+    launches = wb.launches_per_step
+    cpu_inputs_needed = rank == 0 and world == 1 and not args.no_cpu_baseline
+    wb.release()
+    del wb
 
-    # the fused lm_head argmax (greedy tokens straight from final hidden states) on this workload's rows
-    lmh = sample_from_logits = None
-    if args.secondary_reps > 0:
-        H, W_lm = synth.lm_head_inputs(wl, dev)
-        g_out = torch.empty(H.shape[0], dtype=torch.int32, device=dev)
-        m_out = torch.empty(H.shape[0], dtype=torch.float32, device=dev)
-        lws = torch.empty(max(1, gb.graft_lm_head_argmax_workspace_size(H.shape[0])), dtype=torch.uint8, device=dev)
-        lmh_graph = torch.cuda.CUDAGraph()
-        gb.graft_lm_head_argmax(H, W_lm, g_out, m_out, step.status, lws)
+    # ---------------------------------------------------------------- the other workloads' whole steps
+    configs = {}
+    names = [] if args.configs.strip() in ("", "none") else [x.strip() for x in args.configs.split(",")]
+    for name in names:
+        if name == wl.name:
+            continue
+        owl = synth.WORKLOADS[name]
+        ob = WorkloadBench(owl, dev)
+        ob.graph.replay()
         torch.cuda.synchronize()
-        with torch.cuda.graph(lmh_graph):
-            gb.graft_lm_head_argmax(H, W_lm, g_out, m_out, step.status, lws)
-        for _ in range(3):
-            lmh_graph.replay()
-        t_lmh = timed(lmh_graph, args.secondary_reps) / args.secondary_reps
-        flops = 2.0 * H.shape[0] * wl.d_model * wl.V
-        nbytes = (H.numel() + W_lm.numel()) * 2 + H.shape[0] * 8
-        lmh = {"rows": H.shape[0], "d_model": wl.d_model, "vocab": wl.V, "us": t_lmh * 1e6,
-               "tflops": flops / t_lmh / 1e12, "gbs": nbytes / t_lmh / 1e9}
-        # sampling acceptance: the target's sample per node, fused into the lm_head and from given logits
-        pos = step.tree["pos"]
-        smp_graph = torch.cuda.CUDAGraph()
-        gb.graft_lm_head_sample(H, W_lm, pos, 1.0, 1234, sampled=g_out, status=step.status, ws=lws)
-        torch.cuda.synchronize()
-        with torch.cuda.graph(smp_graph):
-            gb.graft_lm_head_sample(H, W_lm, pos, 1.0, 1234, sampled=g_out, status=step.status, ws=lws)
-        for _ in range(3):
-            smp_graph.replay()
-        t_smp = timed(smp_graph, args.secondary_reps) / args.secondary_reps
-        lmh["sample_us"] = t_smp * 1e6
-        sws = torch.empty(max(1, gb.graft_sample_tokens_workspace_size(wl.B, wl.Kmax, wl.V)), dtype=torch.uint8,
-                          device=dev)
-        st_graph = torch.cuda.CUDAGraph()
-        gb.graft_sample_tokens(tl, pos, 1.0, 1234, sampled=step.acc["argmax"], ws=sws)
-        torch.cuda.synchronize()
-        with torch.cuda.graph(st_graph):
-            gb.graft_sample_tokens(tl, pos, 1.0, 1234, sampled=step.acc["argmax"], ws=sws)
-        for _ in range(3):
-            st_graph.replay()
-        t_st = timed(st_graph, args.secondary_reps) / args.secondary_reps
-        sample_from_logits = {"us": t_st * 1e6, "gbs": tl.numel() * 4 / t_st / 1e9}
-        del H, W_lm
+        t_one = _timed(ob.graph, 3) / 3
+        n = int(min(3000, max(args.steps, 0.5 / max(t_one, 1e-6))))
+        _, per = ob.time_steps(n, args.warmup)
+        oparts = ob.parts(reps)
+        ne = int(min(n, max(args.steps, 0.5 / max(t_one, 1e-6))))
+        te, oh, od = ob.e2e(ne)
+        configs[name] = workload_report(ob, oparts, clocks, sms, te, ne, oh, od, per)
+        ob.release()
+        del ob
 
-    # attention alone on the other workloads' shapes (the long-context and batched configurations
-    # carry the HBM target), four distinct layers per replay so every call streams from DRAM
-    attn_other = {}
-    if args.secondary_reps > 0 and world == 1:
-        from tree_verification_gb300 import attn_bench
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        for name in ("llama31_8b_long", "qwen3_8b_batch", "qwen3_235b"):
-            owl = synth.WORKLOADS[name]
-            us, nb, st = attn_bench.time_calls(owl, 4, 10, dev=dev)
-            r = attention_roofline(owl, synth.prefix_lengths(owl), us * 1e-6, clocks, sms)
-            attn_other[name] = {"call_us": us, "gbs": nb / us / 1e3, "bound": r["bound"], "frac": r["frac"],
-                                "fractions": r["fractions"], "status": st}
-        torch.cuda.empty_cache()
-
-    bytes_call = attention_bytes_per_call(wl, L0.cpu())
-    peak, peak_kind = measured_peaks()
-    achieved = bytes_call / t_attn / 1e9
-    traffic = recorded_traffic(args.workload)
-    roof = attention_roofline(wl, L0.cpu(), t_attn, clocks, torch.cuda.get_device_properties(dev).multi_processor_count)
-    roof.update({"traffic": traffic, "kernel": "graft_tree_attention (one layer call)", "call_us": t_attn * 1e6})
-    q = statistics.quantiles(per_step_ms, n=10) if len(per_step_ms) >= 10 else [float("nan")] * 9
+    # ---------------------------------------------------------------- the rest of the line
+    lmh = lm_head_timing(wl, dev, reps) if args.secondary_reps > 0 else None
+    roof = dict(head["attention"])
+    roof["kernel"] = "graft_tree_attention (one layer call of the headline step)"
     result = {
         "metric": METRIC, "value": world * args.steps / t_max, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1000.0 * t_max / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "batch": wl.B, "layers": wl.n_layers, "heads_q_kv": [wl.Hq, wl.Hkv],
-                   "head_dim": wl.head_dim, "prefix": list(wl.L), "Kmax": wl.Kmax, "draft_depth_topk": [wl.D, wl.k],
-                   "vocab": wl.V, "M_width": wl.W, "tau": wl.tau, "checkpoints": list(wl.checkpoints),
-                   "l2": f"inputs larger than L2: {bytes_call * wl.n_layers / 1e6:.0f} MB of attention operands "
-                         f"per step in distinct per-layer buffers",
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "accumulate": "fp32"},
+        "config": workload_config(wl, world),
         "roofline": roof,
-        "step_ms": {"median": statistics.median(per_step_ms), "p10": q[0], "p90": q[8]},
-        "e2e": {"value": world * n_e2e / t_e2e if n_e2e > 0 else None, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step * args.steps,
+        "step_ms": head.get("step_ms"),
+        "e2e": head.get("e2e"),
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
-        "secondary": {"tree_attention_gbs": achieved, "tree_attention_frac_of_peak": achieved / peak,
-                      "retrieval_fill_us": t_ret * 1e6, "build_tree_us": t_tree * 1e6,
-                      "launches_per_step": launches_per_step, "device_status": status,
-                      "lm_head_argmax": lmh, "sample_tokens_from_logits": sample_from_logits,
-                      "attention_other_workloads": attn_other},
+        "secondary": {"attention_compaction": head["attention_compaction"],
+                      "retrieval_fill_us": head["retrieval_fill_us"], "build_tree_us": head["build_tree_us"],
+                      "launches_per_step": launches, "device_status": status, "lm_head_argmax": lmh},
+        "configs": configs,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        inputs = (dl, tl, roots, L0, M_succ, M_cnt, layers[0])
-        v, desc = oracle_timing(wl, inputs, args.cpu_budget_s, n_steps=50)
-        result["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
-                                  "sample": desc}
+    if cpu_inputs_needed:
+        inp = oracle_inputs(wl, dev, [0])
+        torch.cuda.empty_cache()
+        n_req, _ = calibrated_requests(wl, inp, args.cpu_budget_s / 3)
+        ests = []
+        t0 = time.perf_counter()
+        while len(ests) < 3 and (not ests or time.perf_counter() - t0 < args.cpu_budget_s):
+            ests.append(oracle_step_sample(wl, inp, list(range(n_req)), 1)[0])
+        v = len(ests) / sum(ests)
+        result["cpu_baseline"] = {
+            "value": v, "unit": UNIT, "cores": blas_threads(), "kind": "oracle",
+            "sample": (f"oracle (NumPy, float64 attention): {len(ests)} samples, each the whole tree build, "
+                       f"acceptance and M update for all {wl.B} requests, the compaction of 1 of {wl.n_layers} "
+                       f"layers and one layer call's attention for {n_req} of {wl.B} requests; the value scales "
+                       f"attention by requests and layers and compaction by layers (extrapolated)")}
+        del inp
+        result["cpu_full_steps"] = cpu_full_steps(budget_s=120.0)
     if rank == 0:
         print(json.dumps(result), flush=True)
     if world > 1:
         dist.destroy_process_group()
 
 
-def run_reference(args):
+def lm_head_timing(wl, dev, reps):
+    """The fused lm_head argmax and sampling kernels at this workload's rows (B Kmax), its vocabulary and
+    a 4096-wide hidden state, plus sampling from given logits."""
+    import torch
+    from tree_verification_gb300 import binding as gb
+    from tree_verification_gb300 import synth
+    H, W_lm = synth.lm_head_inputs(wl, dev)
+    N = H.shape[0]
+    g_out = torch.empty(N, dtype=torch.int32, device=dev)
+    m_out = torch.empty(N, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    lws = torch.empty(max(1, gb.graft_lm_head_argmax_workspace_size(N)), dtype=torch.uint8, device=dev)
+    pos = torch.arange(N, dtype=torch.int32, device=dev).view(wl.B, wl.Kmax)
+    res = {"rows": N, "d_model": wl.d_model, "vocab": wl.V}
+    for name, fn in (("argmax", lambda: gb.graft_lm_head_argmax(H, W_lm, g_out, m_out, status, lws)),
+                     ("sample", lambda: gb.graft_lm_head_sample(H, W_lm, pos, 1.0, 1234, sampled=g_out,
+                                                                status=status, ws=lws))):
+        g = _capture(fn)
+        g.replay()
+        t = _timed(g, reps) / reps
+        res[f"{name}_us"] = t * 1e6
+        del g
+    flops = 2.0 * N * wl.d_model * wl.V
+    nbytes = (H.numel() + W_lm.numel()) * 2 + N * 8
+    res["tflops"] = flops / (res["argmax_us"] * 1e-6) / 1e12
+    res["gbs"] = nbytes / (res["argmax_us"] * 1e-6) / 1e9
+    del H, W_lm
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_attention(args):
+    """--mode attention: microseconds per graft_tree_attention call of a workload (distinct buffers per
+    layer so calls stream from DRAM; the layer calls captured in one CUDA graph); one JSON line."""
+    import numpy as np
     import torch
     from tree_verification_gb300 import _build, synth
     from tree_verification_gb300 import binding as gb
-
-    world, rank, local = dist_env()
-    if rank != 0:
-        return  # the reference arm runs once, on rank 0
+    _build.build()
+    dev = torch.device("cuda")
     wl = synth.WORKLOADS[args.workload]
-    # inputs are drawn exactly as the GPU arm draws them (on the GPU when one is present)
-    if torch.cuda.is_available():
-        dev = torch.device(f"cuda:{local}")
-        torch.cuda.set_device(dev)
-        _build.build()
-        cfg, Lcap, dl, roots, L0, M_succ, M_cnt, layers, tl = make_inputs(wl.scaled(n_layers=1), dev, gb, synth)
-        inputs = (dl, tl, roots, L0, M_succ, M_cnt, layers[0])
-    else:
-        dev = torch.device("cpu")
-        small = wl
-        Lcap = wl.lcap(1)
-        s, c = synth.empty_M(wl.V, wl.W) if wl.M_init != "zipf" else synth.zipf_M(wl.V, wl.W, wl.seed + 5)
-        inputs = (synth.draft_logits(small, dev), synth.target_logits(small, dev), synth.root_tokens(small),
-                  synth.prefix_lengths(small), torch.from_numpy(s), torch.from_numpy(c),
-                  synth.layer_tensors(small, 0, dev, Lcap=Lcap))
-    samp = OracleSample(wl, inputs)
-    for _ in range(max(0, min(args.warmup, 3))):
-        samp.step(1)
-    budget = 150.0
-    _, spent = samp.step(1)
-    n_run = max(1, min(args.steps, int(budget / max(spent, 1e-3))))
-    ests = [samp.step(1)[0] for _ in range(n_run)]
-    value = len(ests) / sum(ests)
-    desc = samp.describe(1, n_run) + f" (of {args.steps} requested steps, bounded to about {budget:.0f} s)"
-    out = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-           "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 / value, "higher_is_better": True,
-           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-           "config": {"workload": wl.name, "batch": wl.B, "layers": wl.n_layers, "prefix": list(wl.L),
-                      "Kmax": wl.Kmax, "vocab": wl.V},
-           "cpu_baseline": {"value": value, "unit": UNIT, "cores": blas_threads(), "kind": "oracle", "sample": desc},
-           "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(out), flush=True)
+    Lcap = max(args.lcap, wl.lcap()) if args.lcap else wl.lcap()
+    L = synth.prefix_lengths(wl).to(dev)
+    layers = [synth.layer_tensors(wl, l, dev, Lcap=Lcap) for l in range(args.layers)]
+    chain = np.array([[(1 << (i + 1)) - 1 for i in range(wl.Kmax)]] * wl.B, dtype=np.uint64)
+    mask = torch.from_numpy(chain.view(np.int64)).to(dev)
+    ws = torch.zeros(max(1, gb.graft_tree_attention_workspace_size(wl.B, wl.Hq, wl.Hkv, wl.Kmax, Lcap)),
+                     dtype=torch.uint8, device=dev)
+    O = torch.empty_like(layers[0][0])
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    scale = 1.0 / math.sqrt(gb.HEAD_DIM)
+
+    def run():
+        for (Q, Kc, Vc, Kt, Vt) in layers:
+            gb.graft_tree_attention(Q, Kc, Vc, Kt, Vt, L, mask, scale, O=O, ws=ws, status=status)
+
+    g = _capture(run)
+    for _ in range(3):
+        g.replay()
+    us = _timed(g, args.reps) * 1e6 / (args.reps * args.layers)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    r = attention_roofline(wl, L.cpu(), us * 1e-6, None, sms)
+    print(json.dumps({"mode": "attention", "workload": wl.name, "layers": args.layers, "lcap": Lcap, "call_us": us,
+                      "bytes_per_call": r["bytes_per_call"], "gbs": r["bytes_per_call"] / us / 1e3,
+                      "bound": r["bound"], "frac": r["frac"], "fractions": r["fractions"],
+                      "status": int(status.item())}), flush=True)
 
 
-def main():
-    args = parse_args()
-    if args.impl == "reference":
+def run_lm_head(args):
+    """--mode lm_head: the fused lm_head argmax / sampling kernels on H [rows][d_model] and W [vocab][d_model]
+    bf16 N(0,1); one JSON line."""
+    import torch
+    from tree_verification_gb300 import _build, synth
+    _build.build()
+    dev = torch.device("cuda")
+    kmax = 64 if args.rows % 64 == 0 else args.rows
+    wl = synth.WORKLOADS["llama3_8b"].scaled(B=args.rows // kmax, Kmax=kmax, V=args.vocab, d_model=args.d_model)
+    res = lm_head_timing(wl, dev, args.reps)
+    print(json.dumps(dict(mode="lm_head", **res)), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.mode == "cpu_step":
+        run_cpu_step(args)
+    elif args.mode == "attention":
+        run_attention(args)
+    elif args.mode == "lm_head":
+        run_lm_head(args)
+    elif args.impl == "reference":
         run_reference(args)
     else:
         run_graft(args)
