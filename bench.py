@@ -77,12 +77,13 @@ def parse_args(argv=None):
     p.add_argument("--workload", default=HEADLINE)
     p.add_argument("--configs", default=",".join(OTHER_CONFIGS),
                    help="comma-separated workloads timed beside the headline ('none' for none)")
-    p.add_argument("--e2e-steps", type=int, default=0, help="end-to-end steps (0: the same as --steps)")
+    p.add_argument("--e2e-steps", type=int, default=0,
+                   help="end-to-end steps (0: the same as --steps; negative: none)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-budget-s", type=float, default=20.0)
     p.add_argument("--reference-budget-s", type=float, default=150.0)
     p.add_argument("--secondary-reps", type=int, default=10,
-                   help="replays of the attention / compaction / tree-build graphs (0 skips them)")
+                   help="replays of the attention / compaction / tree-build graphs (0 skips them and the lm_head)")
     # --mode attention / lm_head
     p.add_argument("--layers", type=int, default=4)
     p.add_argument("--reps", type=int, default=20)
@@ -717,6 +718,11 @@ def workload_report(wb, parts, clocks, sms, t_e2e, n_e2e, h2d, d2h, per_ms=None)
         med = statistics.median(per_ms)
         rep.update({"steps_per_s": 1000.0 / med, "step_ms": {"median": med, "p10": q[0], "p90": q[8]},
                     "timed_steps": len(per_ms)})
+    if parts is None:  # the parts were not timed
+        rep["launches_per_step"] = wb.launches_per_step
+        rep["device_status"] = wb.status()
+        rep["config"] = workload_config(wl)
+        return rep
     t_attn = parts["attention"]
     roof = attention_roofline(wl, L0, t_attn, clocks, sms)
     roof.update({"kernel": "graft_tree_attention (one layer call)", "call_us": t_attn * 1e6,
@@ -733,7 +739,7 @@ def workload_report(wb, parts, clocks, sms, t_e2e, n_e2e, h2d, d2h, per_ms=None)
                                    "frac": (b_attn + b_comp) / t_ac / 1e9 / hbm, "peak_source": f"{hbm_kind} hbm_gbs"}
     rep["build_tree_us"] = parts["tree"] * 1e6
     rep["retrieval_fill_us"] = parts["retrieval"] * 1e6
-    if n_e2e > 0:
+    if n_e2e > 0 and t_e2e == t_e2e:
         rep["e2e"] = {"value": n_e2e / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     rep["launches_per_step"] = wb.launches_per_step
     rep["device_status"] = wb.status()
@@ -754,7 +760,7 @@ def run_graft(args):
     _build.build()
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     wl = synth.WORKLOADS[args.workload]
-    n_e2e = args.e2e_steps if args.e2e_steps > 0 else args.steps
+    n_e2e = args.e2e_steps if args.e2e_steps > 0 else (args.steps if args.e2e_steps == 0 else 0)
 
     # ---------------------------------------------------------------- headline: K timed steps
     wb = WorkloadBench(wl, dev)
@@ -778,8 +784,8 @@ def run_graft(args):
     clocks = sampler.stop()
     t_max = slowest_over_ranks(t_main, dev, world)
     status = wb.status()
-    reps = max(1, args.secondary_reps)
-    parts = wb.parts(reps)
+    reps = args.secondary_reps
+    parts = wb.parts(reps) if reps > 0 else None
     t_e2e, h2d, d2h = wb.e2e(n_e2e) if n_e2e > 0 else (float("nan"), 0, 0)
     t_e2e = slowest_over_ranks(t_e2e, dev, world)
     head = workload_report(wb, parts, clocks, sms, t_e2e, n_e2e, h2d, d2h, per_step_ms)
@@ -801,17 +807,18 @@ def run_graft(args):
         t_one = _timed(ob.graph, 3) / 3
         n = int(min(3000, max(args.steps, 0.5 / max(t_one, 1e-6))))
         _, per = ob.time_steps(n, args.warmup)
-        oparts = ob.parts(reps)
-        ne = int(min(n, max(args.steps, 0.5 / max(t_one, 1e-6))))
-        te, oh, od = ob.e2e(ne)
+        oparts = ob.parts(reps) if reps > 0 else None
+        ne = int(min(n, max(args.steps, 0.5 / max(t_one, 1e-6)))) if n_e2e > 0 else 0
+        te, oh, od = ob.e2e(ne) if ne > 0 else (float("nan"), 0, 0)
         configs[name] = workload_report(ob, oparts, clocks, sms, te, ne, oh, od, per)
         ob.release()
         del ob
 
     # ---------------------------------------------------------------- the rest of the line
     lmh = lm_head_timing(wl, dev, reps) if args.secondary_reps > 0 else None
-    roof = dict(head["attention"])
-    roof["kernel"] = "graft_tree_attention (one layer call of the headline step)"
+    roof = dict(head["attention"]) if "attention" in head else None
+    if roof is not None:
+        roof["kernel"] = "graft_tree_attention (one layer call of the headline step)"
     result = {
         "metric": METRIC, "value": world * args.steps / t_max, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": 1000.0 * t_max / args.steps, "higher_is_better": True,
@@ -822,8 +829,8 @@ def run_graft(args):
         "e2e": head.get("e2e"),
         "gpu_launches": launches * args.steps,
         "clocks": clocks,
-        "secondary": {"attention_compaction": head["attention_compaction"],
-                      "retrieval_fill_us": head["retrieval_fill_us"], "build_tree_us": head["build_tree_us"],
+        "secondary": {"attention_compaction": head.get("attention_compaction"),
+                      "retrieval_fill_us": head.get("retrieval_fill_us"), "build_tree_us": head.get("build_tree_us"),
                       "launches_per_step": launches, "device_status": status, "lm_head_argmax": lmh},
         "configs": configs,
     }

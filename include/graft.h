@@ -58,6 +58,7 @@ typedef struct CUstream_st* graft_stream_t;
 #define GRAFT_STATUS_LENGTH 4         /* L[b] < 0 or L[b] > Lcap; that request was skipped */
 #define GRAFT_STATUS_TREE 8           /* a kept draft node's parent was not kept (cannot happen for finite logits) */
 #define GRAFT_STATUS_TIMEOUT 16       /* a bounded wait inside a kernel expired; that CTA's output is incomplete */
+#define GRAFT_STATUS_WORKSPACE 32     /* graft_tree_attention found its workspace's arrival counters not zeroed */
 
 /* Limits. */
 #define GRAFT_MAX_KMAX 64        /* tree nodes per request (one uint64 ancestor mask) */
@@ -214,6 +215,16 @@ int graft_retrieve(const GraftConfig* cfg, int B, const int32_t* root_tok, const
  * Float32 scores and accumulation.  Requires head_dim == 128, Hq % Hkv == 0,
  * Kmax * Hq / Hkv <= 1024.  Workspace: graft_tree_attention_workspace_size
  * (depends on the current device's SM count).
+ *
+ * The workspace must be ZERO-FILLED before its first use (cudaMemset): when
+ * the items' key blocks are split evenly over persistent CTAs
+ * (GraftAttnTuning.split), an item cut between two CTAs is merged by
+ * whichever piece finishes last, and the arrival counters that decide it
+ * live at the start of the workspace.  Every call that completes leaves the
+ * counters at zero again, so one zero fill per buffer suffices; after a call
+ * that reported GRAFT_STATUS_TIMEOUT, zero the buffer again.  Counters found
+ * non-zero set GRAFT_STATUS_WORKSPACE (that call's output is unreliable).
+ * Calls sharing a workspace must not run at the same time.
  */
 int graft_tree_attention_workspace_size(int B, int Hq, int Hkv, int head_dim, int Kmax,
                                         int64_t Lcap, size_t* bytes);
@@ -238,8 +249,23 @@ int graft_tree_attention(int B, int Hq, int Hkv, int head_dim, int Kmax, const v
  *                 give one chunk per request
  *   persist_ctas  0 = default (the persistent two-tile kernel with one CTA
  *                 per SM when the two-tile grid exceeds one wave); -1 = never
- *                 persistent; n > 0 = persistent with min(n, work items) CTAs
- *                 whenever the two-tile kernel runs with an even tile count
+ *                 persistent; n > 0 = persistent with n CTAs whenever the
+ *                 two-tile kernel runs with an even tile count (at most one
+ *                 per work item when requests are split into key chunks)
+ *   split         0 = default: a persistent launch deals whole items to
+ *                 its CTAs in turn; 1 = with one key chunk per request and at
+ *                 most 256 requests, split the items' key blocks evenly over
+ *                 the CTAs instead (an item cut between CTAs is merged by
+ *                 its last piece through the workspace's arrival counters)
+ *   wait_ns       0 = default (0.5 s); n > 0 = bound, in nanoseconds, on
+ *                 every pipeline wait inside the tensor-core kernels.  A
+ *                 wait that runs out sets GRAFT_STATUS_TIMEOUT; the CTA then
+ *                 stops issuing work, waits (with fixed bounds) for the loads
+ *                 and products it issued, frees its tensor memory and exits,
+ *                 so the device stays usable.  A bound under 1000 ns
+ *                 means no waiting at all (a wait succeeds only if its phase
+ *                 has already completed), so the first waits run out: the
+ *                 failure path, for tests
  *   reserved      must be zero
  *
  * graft_tree_attention_workspace_size_ex / graft_tree_attention_ex take the
@@ -251,7 +277,9 @@ typedef struct GraftAttnTuning {
     int32_t tiles;
     int32_t min_chunk;
     int32_t persist_ctas;
-    int32_t reserved[5];
+    int32_t split;
+    int32_t wait_ns;
+    int32_t reserved[3];
 } GraftAttnTuning;
 
 int graft_tree_attention_workspace_size_ex(int B, int Hq, int Hkv, int head_dim, int Kmax,

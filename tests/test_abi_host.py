@@ -65,7 +65,7 @@ def test_tuning_fields_are_checked():
     lib = gb().lib()
     b = gb()
     sz = ctypes.c_size_t()
-    for bad in (dict(tiles=3), dict(min_chunk=-1), dict(persist_ctas=-2), dict(reserved=(ctypes.c_int32 * 5)(0, 1))):
+    for bad in (dict(tiles=3), dict(min_chunk=-1), dict(persist_ctas=-2), dict(reserved=(ctypes.c_int32 * 3)(0, 1)), dict(split=2), dict(split=-1), dict(wait_ns=-5)):
         t = b.GraftAttnTuning()
         for k, v in bad.items():
             setattr(t, k, v)

@@ -307,6 +307,45 @@ def test_attention_parity_persistent(ctas, min_chunk, B, Hq, Hkv, Kmax, Ls, Lcap
     assert_attention_close(to_np(O), ref)
 
 
+@pytest.mark.parametrize("ctas,split", [(40, 1), (1, 0), (3, 0), (152, 1)])
+@pytest.mark.parametrize("B,Hq,Hkv,Kmax,Ls,Lcap", [
+    (2, 32, 8, 64, [4096, 777], 4160),               # 16 items over up to 152 CTAs: pieces of 1 to 3 blocks
+    (5, 32, 8, 64, [4096, 0, 777, 1, 2300], 4160),   # empty and one-key prefixes (a tree-only item)
+    (3, 64, 4, 64, [2000, 63, 1500], 2048),          # group 16: four tile pairs per KV head
+])
+def test_attention_parity_stream_schedule(ctas, split, B, Hq, Hkv, Kmax, Ls, Lcap):
+    """The persistent stream kernel (split 1, one key chunk per request): key blocks split evenly over
+    the CTAs, so items are cut into pieces merged by the last one to finish, with more CTAs than items;
+    and the whole-item deal (split 0) on the same shapes."""
+    tuning = dict(tiles=2, persist_ctas=ctas, min_chunk=1000000, split=split)
+    Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed=13 * B + ctas)
+    ws = torch.zeros(gb().graft_tree_attention_workspace_size(B, Hq, Hkv, Kmax, Lcap, tuning), dtype=torch.uint8,
+                     device=DEV)
+    ref = oatt.tree_attention(to_np(Q), to_np(Kc), to_np(Vc), to_np(Kt), to_np(Vt), L.numpy(), masks,
+                              1 / math.sqrt(128))
+    for call in range(2):  # the second call reuses the workspace its first call left zeroed
+        status = _status()
+        O = gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), torch.from_numpy(masks.view(np.int64)).to(DEV),
+                                      1 / math.sqrt(128), status=status, tuning=tuning, ws=ws)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0, f"call {call}: status {int(status.item())}"
+        assert_attention_close(to_np(O), ref)
+
+
+def test_attention_stream_schedule_flags_an_unzeroed_workspace():
+    """Arrival counters that do not start at zero are reported (GRAFT_STATUS_WORKSPACE)."""
+    B, Hq, Hkv, Kmax, Ls, Lcap = 2, 32, 8, 64, [4096, 777], 4160
+    tuning = dict(tiles=2, persist_ctas=40, min_chunk=1000000, split=1)
+    Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed=5)
+    ws = torch.full((gb().graft_tree_attention_workspace_size(B, Hq, Hkv, Kmax, Lcap, tuning),), 0x7f,
+                    dtype=torch.uint8, device=DEV)
+    status = _status()
+    gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), torch.from_numpy(masks.view(np.int64)).to(DEV),
+                              1 / math.sqrt(128), status=status, tuning=tuning, ws=ws)
+    torch.cuda.synchronize()
+    assert int(status.item()) & gb().STATUS_WORKSPACE
+
+
 def test_attention_persistent_length_past_capacity_is_flagged():
     Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(2, 32, 8, 64, [700, 100], 640, seed=3)
     status = _status()
@@ -326,10 +365,11 @@ def test_attention_length_past_capacity_is_flagged():
 
 
 @pytest.mark.parametrize("name,layers,reqs", [("tiny", [0], None), ("llama3_8b", [0, 31], None),
-                                              ("qwen3_8b_batch", [0], [0, 17, 63]),
-                                              ("llama31_8b_long", [0], None), ("qwen3_235b", [0], [0, 15])])
+                                              ("qwen3_8b_batch", [0], "sample"),
+                                              ("llama31_8b_long", [0], None), ("qwen3_235b", [0], "sample")])
 def test_attention_full_size_sampled(name, layers, reqs):
-    """Full-size layer calls; the oracle recomputes sampled requests."""
+    """Full-size layer calls; the oracle recomputes sampled requests: the longest, the median and the three
+    shortest (the longest-first order runs those last, and the stream schedule's last CTAs hold them)."""
     wl = synth.WORKLOADS[name]
     Lcap = wl.lcap()
     L = synth.prefix_lengths(wl)
@@ -345,6 +385,9 @@ def test_attention_full_size_sampled(name, layers, reqs):
         Q, Kc, Vc, Kt, Vt = synth.layer_tensors(wl, layer, DEV, Lcap=Lcap)
         O = gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), mask_d, 1 / math.sqrt(128))
         torch.cuda.synchronize()
+        if reqs == "sample":
+            order = np.lexsort((np.arange(wl.B), -L.numpy()))
+            reqs = sorted({int(order[0]), int(order[wl.B // 2])} | {int(x) for x in order[-3:]})
         for b in (range(wl.B) if reqs is None else reqs):
             lb = int(L[b])
             ref = oatt.tree_attention_one(to_np(Q[b]), to_np(Kc[b, :lb]), to_np(Vc[b, :lb]), to_np(Kt[b]),

@@ -24,6 +24,7 @@ STATUS_CACHE_OVERFLOW = 2
 STATUS_LENGTH = 4
 STATUS_TREE = 8
 STATUS_TIMEOUT = 16
+STATUS_WORKSPACE = 32
 EMPTY_TOKEN = -1
 
 MAX_KMAX = 64
@@ -58,7 +59,7 @@ class GraftAttnTuning(ctypes.Structure):
     """Mirror of the C struct GraftAttnTuning (graft.h): explicit launch-plan overrides of the tree
     attention (0 in a field keeps the default plan)."""
     _fields_ = [("tiles", ctypes.c_int32), ("min_chunk", ctypes.c_int32), ("persist_ctas", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 5)]
+                ("split", ctypes.c_int32), ("wait_ns", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 class GraftError(RuntimeError):
@@ -157,11 +158,11 @@ def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape=None) -> None:
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
 
 
-def _ws(nbytes: int, device, ws: Optional[torch.Tensor]):
+def _ws(nbytes: int, device, ws: Optional[torch.Tensor], zero: bool = False):
     if nbytes == 0:
         return None, 0
     if ws is None:
-        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        ws = (torch.zeros if zero else torch.empty)(nbytes, dtype=torch.uint8, device=device)
     if ws.numel() < nbytes:
         raise ValueError("workspace too small")
     return ws, ws.numel()
@@ -274,7 +275,8 @@ def graft_tree_attention(Q, Kc, Vc, Kt, Vt, L, tree_mask, scale: float, O=None, 
         O = torch.empty_like(Q)
     _need(O, "O", torch.bfloat16, Q.shape)
     t = _tuning(tuning)
-    ws, nws = _ws(graft_tree_attention_workspace_size(B, Hq, Hkv, Kmax, Lcap, t), Q.device, ws)
+    # the attention workspace starts zero-filled (its arrival counters); calls leave it that way
+    ws, nws = _ws(graft_tree_attention_workspace_size(B, Hq, Hkv, Kmax, Lcap, t), Q.device, ws, zero=True)
     args = (B, Hq, Hkv, d, Kmax, _ptr(Q), _ptr(Kc), _ptr(Vc), Lcap, _ptr(Kt), _ptr(Vt), _ptr(L), _ptr(tree_mask),
             float(scale), _ptr(O), _ptr(status))
     if t is None:

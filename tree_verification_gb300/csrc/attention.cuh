@@ -17,6 +17,7 @@ struct AttnArgs {
     int nchunk;                   // chunk CTAs per (request, KV head, row tile)
     int Lcap;
     float scale;
+    uint64_t wait_ns;  // bound on every pipeline wait inside the kernels (0.5 s unless tuned)
     const void* Q;
     const void* Kc;
     const void* Vc;
@@ -28,6 +29,10 @@ struct AttnArgs {
     float* part_o;    // [B][Hkv][nRB][nchunk][128][128] normalised partial outputs
     float* part_lse;  // [B][Hkv][nRB][nchunk][128] log2-sum-exp of each partial
     int32_t* status;
+    // stream schedule (attention_tcs.cu): items cut at a CTA-group boundary
+    int32_t* cut_cnt;  // [items][2] arrival counters (zero between calls)
+    float* cut_o;      // [2 ctas][2][128][128] partial rows of the cut pieces (two slots per CTA)
+    float* cut_lse;    // [2 ctas][2][128] their log2-sum-exp
 };
 
 // Marks the log2-sum-exp slots of one 128-row tile's partial for chunk c:
@@ -61,6 +66,10 @@ int attn_tc1_launch(const AttnArgs& a, cudaStream_t st);
 // dealt to `ctas` CTAs that run theirs back to back; then the merge, as attn_tc_launch.
 int attn_tcp_items(const AttnArgs& a);
 int attn_tcp_launch(const AttnArgs& a, int ctas, cudaStream_t st);
+// Persistent two-tile kernel with the stream schedule (attention_tcs.cu): one key chunk per request,
+// B <= 256, `ctas` a multiple of nRB / 2; the key blocks split evenly over the CTAs, cut items merged
+// by their last piece through the arrival counters a.cut_cnt.
+int attn_tcs_launch(const AttnArgs& a, int ctas, cudaStream_t st);
 // Merges split-key partials (no-op when every request fits one chunk).
 int attn_combine_launch(const AttnArgs& a, cudaStream_t st);
 

@@ -13,6 +13,7 @@ namespace {
 struct AttnPlan {
     int G, R, nRB, C, nchunk, tiles;
     int persist;  // > 0: CTAs of the persistent two-tile kernel
+    bool stream;  // persistent kernel with the stream schedule
     bool tc;
 };
 
@@ -34,7 +35,10 @@ struct AttnPlan {
 // work items than SMs) and the row tiles pair up (an even tile count), one
 // CTA per SM runs the items back to back (attention_tcp.cu), which hides each
 // item's start and finish behind its neighbours and deals items of
-// decreasing length evenly.
+// decreasing length evenly.  On request (GraftAttnTuning.split = 1), with
+// one key chunk per request and at most 256 requests, the stream kernel
+// splits the items' key blocks evenly over the CTAs instead, cut items
+// merged by their last piece.
 //
 // The plan depends only on the call's shape, the device's SM count and the
 // optional GraftAttnTuning overrides, never on the process environment, so a
@@ -51,8 +55,9 @@ long long chunk_count(long long Lcap, long long units, int sms, long long min_ch
 int check_tuning(const GraftAttnTuning* t) {
     if (t == nullptr) return GRAFT_OK;
     if (t->tiles != 0 && t->tiles != 1 && t->tiles != 2) return GRAFT_ERR_INVALID_ARG;
-    if (t->min_chunk < 0 || t->persist_ctas < -1) return GRAFT_ERR_INVALID_ARG;
-    for (int i = 0; i < 5; ++i)
+    if (t->min_chunk < 0 || t->persist_ctas < -1 || t->split < 0 || t->split > 1 || t->wait_ns < 0)
+        return GRAFT_ERR_INVALID_ARG;
+    for (int i = 0; i < 3; ++i)
         if (t->reserved[i] != 0) return GRAFT_ERR_INVALID_ARG;
     return GRAFT_OK;
 }
@@ -89,17 +94,35 @@ AttnPlan plan_attention(int B, int Hq, int Hkv, int Kmax, int64_t Lcap, const Gr
         else if (force == 0 && items > sms)
             p.persist = sms;
     }
+    p.stream = p.persist > 0 && p.nchunk == 1 && B <= 256 && tune != nullptr && tune->split == 1 &&
+               (long long)B * Hkv * (Lcap / ATTN_TC_BLOCK_KEYS + 4) < (1LL << 30);  // cost units fit an int
+    if (p.stream) {
+        // CTAs come in groups of one per row-tile pair of a (request, KV head)
+        const int pairs = p.nRB / 2;
+        const int want = (tune != nullptr && tune->persist_ctas > 0) ? tune->persist_ctas : sms;
+        p.persist = (want / pairs > 0 ? want / pairs : 1) * pairs;
+    }
     return p;
 }
 
+// Workspace: the stream schedule's arrival counters come first (the part the caller zeroes once and
+// every call leaves at zero), then the partial rows.
 size_t attn_ws(const AttnPlan& p, int B, int Hkv, AttnArgs* a, void* ws) {
     WsCarver c(ws);
+    const size_t items = p.stream ? (size_t)B * Hkv * (p.nRB / 2) : 0;
+    int32_t* cnt = c.take<int32_t>(items * 2);
+    const size_t cut_rows = p.stream ? (size_t)2 * p.persist * 2 * 128 : 0;
+    float* co = c.take<float>(cut_rows * GRAFT_HEAD_DIM);
+    float* cl = c.take<float>(cut_rows);
     const size_t parts = p.nchunk > 1 ? (size_t)B * Hkv * p.nRB * p.nchunk * 128 : 0;
     float* po = c.take<float>(parts * GRAFT_HEAD_DIM);
     float* pl = c.take<float>(parts);
     if (a) {
         a->part_o = po;
         a->part_lse = pl;
+        a->cut_cnt = cnt;
+        a->cut_o = co;
+        a->cut_lse = cl;
     }
     return c.bytes();
 }
@@ -168,6 +191,7 @@ extern "C" int graft_tree_attention_ex(int B, int Hq, int Hkv, int head_dim, int
     a.nchunk = p.nchunk;
     a.Lcap = (int)Lcap;
     a.scale = scale;
+    a.wait_ns = (tuning != nullptr && tuning->wait_ns > 0) ? (uint64_t)tuning->wait_ns : 500000000ull;
     a.Q = Q;
     a.Kc = Kc;
     a.Vc = Vc;
@@ -179,9 +203,11 @@ extern "C" int graft_tree_attention_ex(int B, int Hq, int Hkv, int head_dim, int
     a.status = status;
     attn_ws(p, B, Hkv, &a, ws);
     if ((long long)p.nRB * Hkv > 65535LL || p.nchunk > 65535) return GRAFT_ERR_UNSUPPORTED_SHAPE;
-    // the persistent kernel stores output rows in 32-byte pieces
+    // the persistent kernels store output rows in 32-byte pieces
     if (p.persist > 0 && (reinterpret_cast<uintptr_t>(O) & 31) == 0)
-        return attn_tcp_launch(a, p.persist, (cudaStream_t)stream);
+        return p.stream ? attn_tcs_launch(a, p.persist, (cudaStream_t)stream)
+                        : attn_tcp_launch(a, p.persist, (cudaStream_t)stream);
+    // (an O only 16-byte aligned runs the two-tile kernel, which needs no workspace with one chunk)
     if (p.tc) return p.tiles == 2 ? attn_tc_launch(a, (cudaStream_t)stream) : attn_tc1_launch(a, (cudaStream_t)stream);
     return attn_mma_launch(a, (cudaStream_t)stream);
 }

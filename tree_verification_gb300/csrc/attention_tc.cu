@@ -98,7 +98,10 @@ static_assert(2 * 128 * 128 * 4 <= (SK + SV) * BLK_BYTES, "staging of both tiles
 constexpr uint32_t TM_S = 0;    // + tile * 128
 constexpr uint32_t TM_O = 256;  // + tile * 128
 constexpr float RESCALE_LOG2 = 8.f;
-constexpr uint64_t kWaitNs = 500000000ull;   // bound on any single wait (the kernel runs for microseconds)
+// Pipeline waits are bounded by kWaitNs (a.wait_ns in the failure-path tests); the waits of the
+// teardown keep fixed bounds, so every issued load and MMA completes before the CTA frees TMEM and exits.
+constexpr uint64_t kWaitNs = 500000000ull;      // bound on any pipeline wait (the kernel runs for microseconds)
+constexpr uint64_t kTeardownNs = 500000000ull;  // bound on the last MMA completion before TMEM is freed
 constexpr uint64_t kDrainNs = 100000000ull;  // bound on draining in-flight loads after an abort
 
 struct Maps {
@@ -118,8 +121,12 @@ __device__ __forceinline__ void raise_abort(volatile uint32_t* flag, int32_t* st
     flag_status(status, GRAFT_STATUS_TIMEOUT);
 }
 
+// kTestWaits: pipeline waits bounded by a.wait_ns (the failure-path tests); otherwise by kWaitNs, a
+// compile-time constant, so the production instantiation carries no run-time bound.
+template <bool kTestWaits>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
+    const uint64_t wait_ns = kTestWaits ? a.wait_ns : kWaitNs;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -245,7 +252,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             for (int i = 0; i < nb; ++i) {
                 // K(i + SK) reuses the stage S_1(i) released; V(i + SV) the one PV_1(i) released
                 if (i + SK < nb) {
-                    if (!mbar_wait(bar(BAR_KE + i % SK), (i / SK) & 1, kWaitNs)) {
+                    if (!mbar_wait(bar(BAR_KE + i % SK), (i / SK) & 1, wait_ns)) {
                         raise_abort(abort_flag, a.status);
                         break;
                     }
@@ -253,7 +260,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                     load_k(i + SK);
                 }
                 if (i + SV < nb) {
-                    if (!mbar_wait(bar(BAR_VE + i % SV), (i / SV) & 1, kWaitNs)) {
+                    if (!mbar_wait(bar(BAR_VE + i % SV), (i / SV) & 1, wait_ns)) {
                         raise_abort(abort_flag, a.status);
                         break;
                     }
@@ -267,7 +274,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         // ------------------------------------------------------------ MMA issuer (lane 0 issues)
         const uint32_t idS = idesc_bf16(128, BN, false, false);
         const uint32_t idO = idesc_bf16(128, HD, false, true);
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), 0, kWaitNs));
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), 0, wait_ns));
         // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
         // start-address field, which sits in the low bits and cannot carry out of them here
         // (every shared-memory address is below 256 KB).
@@ -277,7 +284,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         // S_t(j) = Q_t K(j)^T into S_t; the last tile's product releases K(j)
         auto issue_S = [&](int t, int j) -> bool {
             if (t == 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KF + j % SK), (j / SK) & 1, kWaitNs))) return false;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KF + j % SK), (j / SK) & 1, wait_ns))) return false;
                 tc_fence_after();
             }
             if (lane == 0) {
@@ -297,7 +304,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         if (ok) tc_fence_after();
         for (int t = 0; t < ntile && ok && nb > 0; ++t) ok = issue_S(t, 0);
         for (int j = 0; j < nb && ok; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + j % SV), (j / SV) & 1, kWaitNs));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + j % SV), (j / SV) & 1, wait_ns));
             if (!ok) break;
             if (j == ragged_block) {
                 // zero the V rows past the chunk end (both 64-dim boxes) before any PV reads them
@@ -312,7 +319,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             }
             for (int t = 0; t < ntile && ok; ++t) {
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(bar(BAR_P + t), j & 1, kWaitNs) && !aborted(abort_flag));
+                                mbar_wait(bar(BAR_P + t), j & 1, wait_ns) && !aborted(abort_flag));
                 if (!ok) break;
                 tc_fence_after();
                 if (lane == 0) {
@@ -346,7 +353,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         bool ok = true;
         const uint32_t sbuf = tmem + lane_base + TM_S + t * 128;
         for (int j = 0; j < nb && t < ntile; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + t), j & 1, kWaitNs) && !aborted(abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + t), j & 1, wait_ns) && !aborted(abort_flag));
             if (!ok) break;
             tc_fence_after();
             float s[BN];
@@ -403,7 +410,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             // the other tile's exponentials run, instead of both P arriving together.
             if (ntile == 2 && (t == 1 || j > 0)) {
                 const int ph = t == 1 ? (j & 1) : ((j - 1) & 1);
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_TURN + t), ph, kWaitNs) && !aborted(abort_flag));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_TURN + t), ph, wait_ns) && !aborted(abort_flag));
                 if (!ok) break;
             }
 #pragma unroll
@@ -442,7 +449,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         if (t < ntile) {
             if (ok && nb > 0) {
                 // every MMA, the last PV included, has completed (one-shot barrier: no phase ambiguity)
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_DONE), 0, kWaitNs));
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_DONE), 0, wait_ns));
                 if (!ok) raise_abort(abort_flag, a.status);
             }
             const bool direct = (nck == 1);
@@ -483,7 +490,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 }
             }
             mbar_arrive(bar(BAR_EPI + t));
-            const bool staged = __all_sync(0xffffffffu, mbar_wait(bar(BAR_EPI + t), 0, kWaitNs));
+            const bool staged = __all_sync(0xffffffffu, mbar_wait(bar(BAR_EPI + t), 0, wait_ns));
             if (!staged) {
                 raise_abort(abort_flag, a.status);
                 ok = false;
@@ -531,7 +538,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     }
     if (warp == 1 && lane == 0) {
         // every issued MMA has completed before TMEM is released
-        mbar_wait(bar(BAR_DONE), 0, kWaitNs);
+        mbar_wait(bar(BAR_DONE), 0, kTeardownNs);
     }
     tc_fence_before();
     __syncthreads();
@@ -596,15 +603,17 @@ int attn_tc_launch(const AttnArgs& a, cudaStream_t st) {
         if (!encode(&m.kt, a.Kt, 4, dims, strides, box)) return GRAFT_ERR_CUDA;
         if (!encode(&m.vt, a.Vt, 4, dims, strides, box)) return GRAFT_ERR_CUDA;
     }
-    static bool attr_set[64] = {false};
+    static bool attr_set[64][2] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (!cuda_ok(cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES)))
+    const bool test_waits = a.wait_ns != kWaitNs;
+    auto kernel = test_waits ? attn_tc_kernel<true> : attn_tc_kernel<false>;
+    if (dev >= 0 && dev < 64 && !attr_set[dev][test_waits]) {
+        if (!cuda_ok(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES)))
             return GRAFT_ERR_CUDA;
-        attr_set[dev] = true;
+        attr_set[dev][test_waits] = true;
     }
-    launch_pdl(attn_tc_kernel, dim3(((a.nRB + 1) / 2) * a.Hkv, a.nchunk, a.B), dim3(NTHREADS), SMEM_BYTES, st, m, a);
+    launch_pdl(kernel, dim3(((a.nRB + 1) / 2) * a.Hkv, a.nchunk, a.B), dim3(NTHREADS), SMEM_BYTES, st, m, a);
     count_launches(1);
     const int rc = launch_status();
     if (rc != GRAFT_OK) return rc;

@@ -99,7 +99,10 @@ static_assert(BN == 128, "one S/P buffer is 128 columns, P its first 64");
 constexpr uint32_t TM_S = 0;    // + buf * 128
 constexpr uint32_t TM_O = 256;
 constexpr float RESCALE_LOG2 = 8.f;
-constexpr uint64_t kWaitNs = 500000000ull;   // bound on any single wait (the kernel runs for microseconds)
+// Pipeline waits are bounded by kWaitNs (a.wait_ns in the failure-path tests); the waits of the
+// teardown keep fixed bounds, so every issued load and MMA completes before the CTA frees TMEM and exits.
+constexpr uint64_t kWaitNs = 500000000ull;      // bound on any pipeline wait (the kernel runs for microseconds)
+constexpr uint64_t kTeardownNs = 500000000ull;  // bound on the last MMA completion before TMEM is freed
 constexpr uint64_t kDrainNs = 100000000ull;  // bound on draining in-flight loads after an abort
 
 struct Maps {
@@ -119,8 +122,12 @@ __device__ __forceinline__ void raise_abort(volatile uint32_t* flag, int32_t* st
     flag_status(status, GRAFT_STATUS_TIMEOUT);
 }
 
+// kTestWaits: pipeline waits bounded by a.wait_ns (the failure-path tests); otherwise by kWaitNs, a
+// compile-time constant, so the production instantiation carries no run-time bound.
+template <bool kTestWaits>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
+    const uint64_t wait_ns = kTestWaits ? a.wait_ns : kWaitNs;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -221,7 +228,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 tma_load_3d(base + OFF_Q + h * (Q_TILE_BYTES / 2), &maps.q, bar(BAR_Q), h * 64, kvh * a.G, nz);
             for (int j = 0; j < nb; ++j) {
                 // a K stage frees as soon as its S product has run
-                if (j >= SK && !mbar_wait(bar(BAR_KE + j % SK), ((j / SK) - 1) & 1, kWaitNs)) {
+                if (j >= SK && !mbar_wait(bar(BAR_KE + j % SK), ((j / SK) - 1) & 1, wait_ns)) {
                     raise_abort(abort_flag, a.status);
                     break;
                 }
@@ -235,7 +242,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         if (lane == 0) {
             for (int j = 0; j < nb; ++j) {
                 // a V stage frees once its PV product has run
-                if (j >= SV && !mbar_wait(bar(BAR_VE + j % SV), ((j / SV) - 1) & 1, kWaitNs)) {
+                if (j >= SV && !mbar_wait(bar(BAR_VE + j % SV), ((j / SV) - 1) & 1, wait_ns)) {
                     raise_abort(abort_flag, a.status);
                     break;
                 }
@@ -248,7 +255,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         // ------------------------------------------------------------ MMA issuer (lane 0 issues)
         const uint32_t idS = idesc_bf16(128, BN, false, false);
         const uint32_t idO = idesc_bf16(128, HD, false, true);
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), 0, kWaitNs));
+        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), 0, wait_ns));
         // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
         // start-address field, which sits in the low bits and cannot carry out of them here
         // (every shared-memory address is below 256 KB).
@@ -257,7 +264,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         const uint64_t v_desc = sdesc_sw128(base + OFF_V, BOX_BYTES, 1024);
         // S(j) into S/P buffer j % 2, then release K(j)
         auto issue_S = [&](int j) -> bool {
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KF + j % SK), (j / SK) & 1, kWaitNs))) return false;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KF + j % SK), (j / SK) & 1, wait_ns))) return false;
             tc_fence_after();
             if (lane == 0) {
                 const uint64_t kd = k_desc + (((j % SK) * BLK_BYTES) >> 4);
@@ -276,7 +283,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         if (ok) tc_fence_after();
         for (int j = 0; j < 2 && j < nb && ok; ++j) ok = issue_S(j);
         for (int j = 0; j < nb && ok; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + j % SV), (j / SV) & 1, kWaitNs));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + j % SV), (j / SV) & 1, wait_ns));
             if (!ok) break;
             if (j == ragged_block) {
                 // zero the V rows past the chunk end (both 64-dim boxes) before any PV reads them
@@ -289,7 +296,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_P + (j & 1)), (j >> 1) & 1, kWaitNs) && !aborted(abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_P + (j & 1)), (j >> 1) & 1, wait_ns) && !aborted(abort_flag));
             if (!ok) break;
             tc_fence_after();
             if (lane == 0) {
@@ -319,7 +326,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         float m_used = -INFINITY, l_sum = 0.f;  // running max (log2 units) and row sum
         bool ok = true;
         for (int j = 0; j < nb && ok; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + (j & 1)), (j >> 1) & 1, kWaitNs) &&
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + (j & 1)), (j >> 1) & 1, wait_ns) &&
                                              !aborted(abort_flag));
             if (!ok) break;
             tc_fence_after();
@@ -353,7 +360,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 // PV(j - 1 + SV) cannot have completed before this softmax hands over block j: the
                 // parity names block j - 1 unambiguously.
                 ok = __all_sync(0xffffffffu,
-                                mbar_wait(bar(BAR_VE + (j - 1) % SV), ((j - 1) / SV) & 1, kWaitNs));
+                                mbar_wait(bar(BAR_VE + (j - 1) % SV), ((j - 1) / SV) & 1, wait_ns));
                 if (!ok) break;
                 tc_fence_after();
                 const float m_new = fmaxf(mx, m_used);
@@ -395,7 +402,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         // ------------------------------------------------------------ epilogue
         if (ok && nb > 0) {
             // every MMA, the last PV included, has completed (one-shot barrier: no phase ambiguity)
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_DONE), 0, kWaitNs));
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_DONE), 0, wait_ns));
             if (!ok) raise_abort(abort_flag, a.status);
         }
         const bool direct = nck == 1;
@@ -440,7 +447,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             }
         }
         mbar_arrive(bar(BAR_EPI));
-        const bool staged = __all_sync(0xffffffffu, mbar_wait(bar(BAR_EPI), 0, kWaitNs));
+        const bool staged = __all_sync(0xffffffffu, mbar_wait(bar(BAR_EPI), 0, wait_ns));
         if (!staged) {
             raise_abort(abort_flag, a.status);
             ok = false;
@@ -490,7 +497,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     }
     if (warp == 2 && lane == 0) {
         // every issued MMA has completed before TMEM is released
-        mbar_wait(bar(BAR_DONE), 0, kWaitNs);
+        mbar_wait(bar(BAR_DONE), 0, kTeardownNs);
     }
     tc_fence_before();
     __syncthreads();
@@ -553,16 +560,18 @@ int attn_tc1_launch(const AttnArgs& a, cudaStream_t st) {
         if (!encode(&m.kt, a.Kt, 4, dims, strides, box)) return GRAFT_ERR_CUDA;
         if (!encode(&m.vt, a.Vt, 4, dims, strides, box)) return GRAFT_ERR_CUDA;
     }
-    static bool attr_set[64] = {false};
+    static bool attr_set[64][2] = {};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-        if (!cuda_ok(cudaFuncSetAttribute(attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES)))
+    const bool test_waits = a.wait_ns != kWaitNs;
+    auto kernel = test_waits ? attn_tc_kernel<true> : attn_tc_kernel<false>;
+    if (dev >= 0 && dev < 64 && !attr_set[dev][test_waits]) {
+        if (!cuda_ok(cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES)))
             return GRAFT_ERR_CUDA;
-        attr_set[dev] = true;
+        attr_set[dev][test_waits] = true;
     }
     dim3 grid(a.nRB * a.Hkv, a.nchunk, a.B);
-    launch_pdl(attn_tc_kernel, grid, dim3(NTHREADS), SMEM_BYTES, st, m, a);
+    launch_pdl(kernel, grid, dim3(NTHREADS), SMEM_BYTES, st, m, a);
     count_launches(1);
     const int rc = launch_status();
     if (rc != GRAFT_OK) return rc;

@@ -45,9 +45,22 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// Non-blocking test of the phase with the given parity (test_wait never suspends the thread).
+__device__ __forceinline__ bool mbar_test_now(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase with the given parity to complete; gives up after
-// limit_ns of wall-clock time and returns false.
+// limit_ns of wall-clock time and returns false.  A bound under a
+// microsecond (below the resolution of the suspend in try_wait and of
+// %globaltimer) means no waiting at all: one non-blocking test.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+    if (limit_ns < 1000) return mbar_test_now(bar, parity);
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
