@@ -31,7 +31,8 @@ struct AttnArgs {
     int32_t* status;
     // stream schedule (attention_tcs.cu): items cut at a CTA-group boundary
     int32_t* cut_cnt;  // [items][2] arrival counters (zero between calls)
-    float* cut_o;      // [2 ctas][2][128][128] partial rows of the cut pieces (two slots per CTA)
+    float* cut_o;      // [2 ctas][2][32][128] float4: partial rows of the cut pieces, chunk-major
+                       // (float4 column chunk x of the 128 rows side by side; two slots per CTA)
     float* cut_lse;    // [2 ctas][2][128] their log2-sum-exp
 };
 

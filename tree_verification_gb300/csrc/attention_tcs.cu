@@ -122,6 +122,14 @@ __device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
                  : "memory");
 }
 
+// 16-byte store to p + OFF bytes (16-byte aligned), the offset folded into the instruction so that
+// strided stores share one address register
+template <int OFF>
+__device__ __forceinline__ void st_global_v4(void* p, float x, float y, float z, float w) {
+    asm volatile("st.global.v4.f32 [%0+%5], {%1, %2, %3, %4};" ::"l"(p), "f"(x), "f"(y), "f"(z), "f"(w), "n"(OFF)
+                 : "memory");
+}
+
 // One piece: blocks [jb, je) of the item of (request b, KV head kvh, row-tile pair rb), whose
 // blocks are the prefix's (nb_prefix of them, the last one ragged when ragged_valid != 0) and then the
 // tree block.
@@ -617,7 +625,8 @@ attn_tcs_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(a.O) +
                                   (((size_t)it.b * a.Kmax + node) * a.Hq + it.kvh * a.G + gr % a.G) * HD;
             const int slot = cut ? cut_slot(it.jb == 0, (int)blockIdx.x) : 0;
-            float* prow = a.cut_o + (((size_t)slot * 2 + t) * 128 + r) * HD;
+            // cut partials are stored chunk-major: float4 chunk x of rows 0..127 side by side, so every
+            // warp store here and every warp load of the merge covers 512 contiguous bytes
             for (int c0 = 0; c0 < HD; c0 += 32) {
                 float o[32];
                 tmem_ld32(tmem + lane_base + TM_O + t * 128 + c0, o);
@@ -640,28 +649,32 @@ attn_tcs_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                         st_global_v8(orow + c0 + x, wd);  // O rows start 32-byte aligned (the launch checks O)
                     }
                 } else {
-#pragma unroll
-                    for (int x = 0; x < 32; x += 8) {
-                        uint32_t wd[8];
-#pragma unroll
-                        for (int y = 0; y < 8; ++y) wd[y] = __float_as_uint(o[x + y] * inv);
-                        st_global_v8(prow + c0 + x, wd);
-                    }
+                    float4* pcol = reinterpret_cast<float4*>(a.cut_o) + ((size_t)(slot * 2 + t) * (HD / 4) + c0 / 4) * 128 + r;
+                    // eight chunks 128 float4 (2 KB) apart
+                    st_global_v4<0>(pcol, o[0] * inv, o[1] * inv, o[2] * inv, o[3] * inv);
+                    st_global_v4<2048>(pcol, o[4] * inv, o[5] * inv, o[6] * inv, o[7] * inv);
+                    st_global_v4<4096>(pcol, o[8] * inv, o[9] * inv, o[10] * inv, o[11] * inv);
+                    st_global_v4<6144>(pcol, o[12] * inv, o[13] * inv, o[14] * inv, o[15] * inv);
+                    st_global_v4<8192>(pcol, o[16] * inv, o[17] * inv, o[18] * inv, o[19] * inv);
+                    st_global_v4<10240>(pcol, o[20] * inv, o[21] * inv, o[22] * inv, o[23] * inv);
+                    st_global_v4<12288>(pcol, o[24] * inv, o[25] * inv, o[26] * inv, o[27] * inv);
+                    st_global_v4<14336>(pcol, o[28] * inv, o[29] * inv, o[30] * inv, o[31] * inv);
                 }
             }
             if (cut) {
                 // -------------------------------------------- a cut piece
                 if (row_ok) a.cut_lse[((size_t)slot * 2 + t) * 128 + r] = m_used + log2f(l_sum);
-                __threadfence();  // this row's partial is visible device-wide before the arrival
                 const int kb = (slot & 1) * 2 + t;  // one-shot barriers of this slot kind and tile
                 mbar_arrive(bar(BAR_CUT + kb));
                 int32_t* cnt = a.cut_cnt + (size_t)it.idx * 2 + t;
                 // the pieces run in groups q_first..q_last, in each on the CTA of this row-tile pair
                 const int q_first = it.g_start / s_S, q_last = (it.g_start + it.nb - 1) / s_S;
                 if (r == 0) {
-                    // every row of the tile is written: count this piece in
+                    // every row of the tile is written (the barrier orders them before this thread's fence,
+                    // which is cumulative): publish them device-wide, then count this piece in
                     int old = -1;
                     if (mbar_wait(bar(BAR_CUT + kb), 0, wait_ns)) {
+                        __threadfence();
                         old = atomicAdd(cnt, 1);
                         __threadfence();
                     }
@@ -677,39 +690,70 @@ attn_tcs_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 }
                 if (old > q_last - q_first) flag_status(a.status, GRAFT_STATUS_WORKSPACE);  // counter not zeroed
                 if (old == q_last - q_first) {
-                    // the last piece to arrive: every piece's partial is complete (each wrote, fenced and
-                    // then counted in); merge them into the bf16 output and leave the counter at zero
+                    // the last piece to arrive: every piece's partial is complete (each wrote, and its CTA
+                    // fenced before counting it in); merge them into the bf16 output and leave the
+                    // counter at zero.  Loads are issued in batches before they are used (one round trip
+                    // per batch): every piece's log2-sum-exp, then two pieces' 32 columns at a time.
                     if (r == 0) *cnt = 0;
                     if (row_ok) {
+                        const int np = q_last - q_first + 1;
+                        // slot-tile index of piece i (its log2-sum-exp row is (index) * 128 + r)
+                        auto row_of = [&](int i) -> size_t {
+                            const int qq = q_first + i;
+                            return (size_t)cut_slot(qq == q_first, qq * nrb2 + it.rb) * 2 + t;
+                        };
                         float mx = -INFINITY;
-                        for (int qq = q_first; qq <= q_last; ++qq)
-                            mx = fmaxf(mx, __ldcg(a.cut_lse + ((size_t)cut_slot(qq == q_first, qq * nrb2 + it.rb) * 2 + t) * 128 + r));
+                        for (int i0 = 0; i0 < np; i0 += 4) {
+                            float l4[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) l4[u] = i0 + u < np ? __ldcg(a.cut_lse + row_of(i0 + u) * 128 + r) : -INFINITY;
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) mx = fmaxf(mx, l4[u]);
+                        }
                         float wsum = 0.f;
-                        for (int qq = q_first; qq <= q_last; ++qq)
-                            wsum += ex2(__ldcg(a.cut_lse + ((size_t)cut_slot(qq == q_first, qq * nrb2 + it.rb) * 2 + t) * 128 + r) - mx);
+                        for (int i0 = 0; i0 < np; i0 += 4) {
+                            float l4[4];
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) l4[u] = i0 + u < np ? __ldcg(a.cut_lse + row_of(i0 + u) * 128 + r) : -INFINITY;
+#pragma unroll
+                            for (int u = 0; u < 4; ++u) wsum += i0 + u < np ? ex2(l4[u] - mx) : 0.f;
+                        }
                         const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
                         for (int c0 = 0; c0 < HD; c0 += 16) {
-                            float accv[16];
+                            float4 acc[4];
 #pragma unroll
-                            for (int x = 0; x < 16; ++x) accv[x] = 0.f;
-                            for (int qq = q_first; qq <= q_last; ++qq) {
-                                const size_t row = ((size_t)cut_slot(qq == q_first, qq * nrb2 + it.rb) * 2 + t) * 128 + r;
-                                const float wq = ex2(__ldcg(a.cut_lse + row) - mx);
-                                const float4* src = reinterpret_cast<const float4*>(a.cut_o + row * HD + c0);
+                            for (int x = 0; x < 4; ++x) acc[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+                            for (int i0 = 0; i0 < np; i0 += 2) {
+                                float4 v[2][4];
+                                float wq[2];
 #pragma unroll
-                                for (int x = 0; x < 4; ++x) {
-                                    const float4 v = __ldcg(src + x);
-                                    accv[4 * x] += wq * v.x;
-                                    accv[4 * x + 1] += wq * v.y;
-                                    accv[4 * x + 2] += wq * v.z;
-                                    accv[4 * x + 3] += wq * v.w;
+                                for (int u = 0; u < 2; ++u) {
+                                    const bool live = i0 + u < np;
+                                    const size_t st = live ? row_of(i0 + u) : 0;
+                                    wq[u] = live ? ex2(__ldcg(a.cut_lse + st * 128 + r) - mx) : 0.f;
+                                    const float4* src = reinterpret_cast<const float4*>(a.cut_o) +
+                                                        (st * (HD / 4) + c0 / 4) * 128 + r;
+#pragma unroll
+                                    for (int x = 0; x < 4; ++x)
+                                        v[u][x] = live ? __ldcg(src + x * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
                                 }
+#pragma unroll
+                                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                                    for (int x = 0; x < 4; ++x) {
+                                        acc[x].x += wq[u] * v[u][x].x;
+                                        acc[x].y += wq[u] * v[u][x].y;
+                                        acc[x].z += wq[u] * v[u][x].z;
+                                        acc[x].w += wq[u] * v[u][x].w;
+                                    }
                             }
                             uint32_t wd[8];
 #pragma unroll
-                            for (int y = 0; y < 8; ++y) {
-                                __nv_bfloat162 h2 = __floats2bfloat162_rn(accv[2 * y] * winv, accv[2 * y + 1] * winv);
-                                wd[y] = *reinterpret_cast<uint32_t*>(&h2);
+                            for (int y = 0; y < 4; ++y) {
+                                __nv_bfloat162 lo = __floats2bfloat162_rn(acc[y].x * winv, acc[y].y * winv);
+                                __nv_bfloat162 hi = __floats2bfloat162_rn(acc[y].z * winv, acc[y].w * winv);
+                                wd[2 * y] = *reinterpret_cast<uint32_t*>(&lo);
+                                wd[2 * y + 1] = *reinterpret_cast<uint32_t*>(&hi);
                             }
                             st_global_v8(orow + c0, wd);
                         }
