@@ -58,7 +58,7 @@ typedef struct CUstream_st* graft_stream_t;
 #define GRAFT_STATUS_LENGTH 4         /* L[b] < 0 or L[b] > Lcap; that request was skipped */
 #define GRAFT_STATUS_TREE 8           /* a kept draft node's parent was not kept (cannot happen for finite logits) */
 #define GRAFT_STATUS_TIMEOUT 16       /* a bounded wait inside a kernel expired; that CTA's output is incomplete */
-#define GRAFT_STATUS_WORKSPACE 32     /* graft_tree_attention found its workspace's arrival counters not zeroed */
+#define GRAFT_STATUS_WORKSPACE 32     /* a workspace's arrival counter was found not zeroed (graft_build_tree, graft_tree_attention) */
 
 /* Limits. */
 #define GRAFT_MAX_KMAX 64        /* tree nodes per request (one uint64 ancestor mask) */
@@ -154,7 +154,16 @@ int graft_config_no_retrieval(GraftConfig* cfg);
  * Tree order: root; kept draft nodes by (depth asc, score desc); empty
  * nodes if the pool ran short of K_draft (graft_config_no_retrieval); then
  * the stage's first K_ret envelope nodes (empty M slots give pad token 0).
- * Workspace: graft_build_tree_workspace_size.
+ * Workspace: graft_build_tree_workspace_size bytes, 256-byte aligned,
+ * ZERO-FILLED once before its first use: the call is one cooperative launch
+ * (all CTAs resident, so it fails with GRAFT_ERR_CUDA where the device cannot
+ * host a cooperative grid) whose phases meet at a grid barrier kept in the
+ * workspace; every completed call leaves that barrier's count at zero again.
+ * A barrier wait is bounded (half a second): one that runs out sets
+ * GRAFT_STATUS_TIMEOUT and the outputs are incomplete; zero the workspace
+ * again before the next call.  A barrier count found out of its range sets
+ * GRAFT_STATUS_WORKSPACE (that call's output is unreliable).  Workspaces
+ * must not be shared by calls that may run concurrently.
  */
 int graft_build_tree_workspace_size(const GraftConfig* cfg, int B, size_t* bytes);
 int graft_build_tree(const GraftConfig* cfg, int B, const float* draft_logits,

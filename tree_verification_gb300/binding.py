@@ -215,7 +215,7 @@ def graft_build_tree(cfg: GraftConfig, draft_logits, root_tok, M_succ, L, out: O
                    pos=torch.empty(B, K, dtype=torch.int32, device=dev),
                    mask=torch.empty(B, K, dtype=torch.int64, device=dev),
                    stage=torch.empty(B, dtype=torch.int32, device=dev))
-    ws, nws = _ws(graft_build_tree_workspace_size(cfg, B), dev, ws)
+    ws, nws = _ws(graft_build_tree_workspace_size(cfg, B), dev, ws, zero=True)
     fn = lib().graft_build_tree_block if block else lib().graft_build_tree
     _check(fn(ctypes.byref(cfg), B, _ptr(draft_logits), _ptr(root_tok), _ptr(M_succ), _ptr(L),
               _ptr(out["tok"]), _ptr(out["parent"]), _ptr(out["depth"]), _ptr(out["pos"]),

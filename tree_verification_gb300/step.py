@@ -50,8 +50,9 @@ class VerifyStep:
                         bonus=torch.empty(B, **i32))
         self.status = torch.zeros(1, **i32)
         u8 = dict(dtype=torch.uint8, device=dev)
-        self.ws_tree = torch.empty(max(1, gb.graft_build_tree_workspace_size(cfg, B)), **u8)
-        # zero-filled once: the attention workspace's arrival counters must start at zero
+        # zero-filled once: the tree build's grid barrier and the attention workspace's arrival
+        # counters must start at zero (every call leaves them at zero)
+        self.ws_tree = torch.zeros(max(1, gb.graft_build_tree_workspace_size(cfg, B)), **u8)
         self.ws_attn = torch.zeros(max(1, gb.graft_tree_attention_workspace_size(B, Hq, Hkv, K, Lcap)), **u8)
         self.ws_acc = torch.empty(max(1, gb.graft_accept_compact_workspace_size(B, K, cfg.V)), **u8)
         self.ws_upd = torch.empty(max(1, gb.graft_update_M_workspace_size(B * K)), **u8)
