@@ -193,6 +193,34 @@ def test_build_tree_single_node_and_empty_M():
     assert all(t.tok[t.n_draft:] == [0] * (wl2.Kmax - t.n_draft) for t in trees2)
 
 
+@pytest.mark.parametrize("k", [8, 16])
+def test_build_tree_tied_and_masked_rows(k):
+    """Drafter rows full of ties and of -inf: integer-valued logits (the top-k decided by token id among
+    equal logits), an all-equal row (with k = 16 more than 32 of a warp's entries tie with its threshold,
+    so the split takes the per-thread insertion path), and rows masked to a dozen finite logits (-inf
+    elsewhere; -inf entries are real entries that rank after every finite one, by id)."""
+    wl = synth.WORKLOADS["llama3_8b"].scaled(B=4, V=32768, k=k, seed=11)
+    cfg, cfg_o = lib_cfg(wl), oracle_cfg(wl)
+    g = torch.Generator(device="cpu").manual_seed(11)
+    dl = torch.empty(wl.B, wl.D, wl.k, wl.V)
+    dl[0] = torch.round(torch.randn(wl.D, wl.k, wl.V, generator=g) * 2.0)
+    dl[1] = 0.0
+    dl[2] = -math.inf
+    dl[3] = torch.round(torch.randn(wl.D, wl.k, wl.V, generator=g) * 4.0) * 0.25
+    for d in range(wl.D):
+        for f in range(wl.k):
+            ids = torch.randperm(wl.V, generator=g)[:12]
+            dl[2, d, f, ids] = torch.randn(12, generator=g)
+    dl = dl.to(DEV)
+    roots, L = synth.root_tokens(wl), synth.prefix_lengths(wl)
+    s_np, _ = synth.zipf_M(wl.V, wl.W, 11)
+    succ = torch.from_numpy(s_np).to(DEV)
+    gpu = _build(wl, cfg, dl, roots, succ, L)
+    trees, margins, fns = _oracle_tree(wl, cfg_o, dl, roots, s_np, L)
+    _check_trees(gpu, trees, margins, fns, roots, s_np, L, cfg_o)
+    assert int(to_np(gpu["stage"])[2]) > 0  # the masked rows are confident: drafting goes past call 0
+
+
 def test_build_tree_zero_batch():
     wl = synth.WORKLOADS["tiny"].scaled(B=0, V=1000)
     cfg = lib_cfg(wl)

@@ -24,8 +24,12 @@
 //     from registers (bf16 output rows, or fp32 partial rows and their
 //     log2-sum-exp for the merge kernel), so it overlaps the next item's
 //     first S product and softmax instead of staging through the rings.
-// Everything else (warp roles, TMEM layout, masking, lazy rescale,
-// turn-taking exponentials of the two tiles) is the two-tile kernel's.
+// Everything else (TMEM layout, masking, lazy rescale, turn-taking
+// exponentials of the two tiles) is the two-tile kernel's, except two warp
+// roles: the MMA issuer is a single thread with running ring counters (the
+// tensor pipe queues hardly any products ahead, so the issuer's own time
+// between products is pipe idle time), and tile 0's softmax warps zero a
+// ragged block's V rows past the chunk end before they signal P_0.
 //
 // Every mbarrier wait is bounded; on timeout the CTA raises
 // GRAFT_STATUS_TIMEOUT, stops issuing work, drains what it issued (again
@@ -319,23 +323,30 @@ attn_tcp_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer (lane 0 issues)
-        const uint32_t idS = idesc_bf16(128, BN, false, false);
-        const uint32_t idO = idesc_bf16(128, HD, false, true);
-        // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
-        // start-address field, which sits in the low bits and cannot carry out of them here
-        // (every shared-memory address is below 256 KB).
-        const uint64_t q_desc = sdesc_sw128(base + OFF_Q, 16, 1024);
-        const uint64_t k_desc = sdesc_sw128(base + OFF_K, 16, 1024);
-        const uint64_t v_desc = sdesc_sw128(base + OFF_V, BOX_BYTES, 1024);
-        // S_t(g) = Q_t K(g)^T into S_t; tile 1's product releases K(g)
-        auto issue_S = [&](int t, int g) -> bool {
-            if (t == 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KF + g % SK), (g / SK) & 1, wait_ns))) return false;
-                tc_fence_after();
-            }
-            if (lane == 0) {
-                const uint64_t kd = k_desc + (((g % SK) * BLK_BYTES) >> 4);
+        // ------------------------------------------------------------ MMA issuer (lane 0 alone)
+        // tcgen05.mma issue barely queues ahead of the tensor pipe, so every cycle this thread
+        // spends between two products is a cycle the pipe idles: one thread runs the loop, with
+        // the ring positions kept as running counters and no warp-wide votes.  (A second issuer
+        // for the other tile, interleaving its products with these, measured slower.)
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16(128, BN, false, false);
+            const uint32_t idO = idesc_bf16(128, HD, false, true);
+            // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
+            // start-address field, which sits in the low bits and cannot carry out of them here
+            // (every shared-memory address is below 256 KB).
+            const uint64_t q_desc = sdesc_sw128(base + OFF_Q, 16, 1024);
+            const uint64_t k_desc = sdesc_sw128(base + OFF_K, 16, 1024);
+            const uint64_t v_desc = sdesc_sw128(base + OFF_V, BOX_BYTES, 1024);
+            int kst = 0, kph = 0;  // K ring: stage and phase of the next block the S products read
+            int vst = 0, vph = 0;  // V ring: stage and phase of the next block the PV products read
+            uint32_t pph = 0;      // phase of the S and P barriers of the current block (g & 1)
+            // S_t = Q_t K^T of the next K block into S_t; tile 1's product releases that K stage
+            auto issue_S = [&](int t) -> bool {
+                if (t == 0) {
+                    if (!mbar_wait(bar(BAR_KF + kst), kph, wait_ns)) return false;
+                    tc_fence_after();
+                }
+                const uint64_t kd = k_desc + ((kst * BLK_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
@@ -343,66 +354,55 @@ attn_tcp_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                     mma_bf16_ss(tmem + TM_S + t * 128, q_desc + (qoff >> 4), kd + (off >> 4), idS, kk > 0);
                 }
                 mma_commit(bar(BAR_S + t));
-                if (t == 1) mma_commit(bar(BAR_KE + g % SK));
-            }
-            __syncwarp();
-            return true;
-        };
-        bool ok = true;
-        int q = 0, g0 = 0;  // live items issued, global index of the item's first block
-        for (int k = 0; ok; ++k) {
-            const int i = item_index(k, n_items);
-            if (i < 0) break;
-            const Item it = make_item(a, order, i, nrb2);
-            if (it.skip) continue;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), q & 1, wait_ns) && !aborted(abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            for (int t = 0; t < 2 && ok; ++t) ok = issue_S(t, g0);
-            for (int j = 0; j < it.nb && ok; ++j) {
-                const int g = g0 + j;
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + g % SV), (g / SV) & 1, wait_ns));
-                if (!ok) break;
-                if (j == it.ragged_block) {
-                    // zero the V rows past the chunk end (both 64-dim boxes) before any PV reads them
-                    uint8_t* v0 = gbase + OFF_V + (g % SV) * BLK_BYTES;
-                    for (int x = lane; x < (BN - it.ragged_valid) * 16; x += 32) {
-                        const int r = it.ragged_valid + x / 16, c16 = x % 16;
-                        *reinterpret_cast<uint4*>(v0 + (c16 >= 8 ? BOX_BYTES : 0) + r * 128 + (c16 & 7) * 16) =
-                            make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
+                if (t == 1) {
+                    mma_commit(bar(BAR_KE + kst));
+                    if (++kst == SK) { kst = 0; kph ^= 1; }
                 }
-                for (int t = 0; t < 2 && ok; ++t) {
-                    bool w = mbar_wait(bar(BAR_P + t), g & 1, wait_ns);
-                    // the item's first PV overwrites O_t: the previous item's epilogue must have read it
-                    if (w && j == 0 && q > 0) w = mbar_wait(bar(BAR_OFREE + t), (q - 1) & 1, wait_ns);
-                    ok = __all_sync(0xffffffffu, w && !aborted(abort_flag));
+                return true;
+            };
+            bool ok = true;
+            int q = 0;  // live items issued
+            for (int k = 0; ok; ++k) {
+                const int i = item_index(k, n_items);
+                if (i < 0) break;
+                const Item it = make_item(a, order, i, nrb2);
+                if (it.skip) continue;
+                ok = mbar_wait(bar(BAR_Q), q & 1, wait_ns) && !aborted(abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                ok = issue_S(0) && issue_S(1);
+                for (int j = 0; j < it.nb && ok; ++j) {
+                    // (tile 0's softmax warps zero a ragged block's V rows past the chunk end before
+                    // they signal P_0, so PV_0 and PV_1, issued after that signal, read zeros there)
+                    ok = mbar_wait(bar(BAR_VF + vst), vph, wait_ns);
                     if (!ok) break;
-                    tc_fence_after();
-                    if (lane == 0) {
+                    const uint64_t vd = v_desc + ((vst * BLK_BYTES) >> 4);
+                    for (int t = 0; t < 2 && ok; ++t) {
+                        ok = mbar_wait(bar(BAR_P + t), pph, wait_ns);
+                        // the item's first PV overwrites O_t: the previous item's epilogue must have read it
+                        if (ok && j == 0 && q > 0) ok = mbar_wait(bar(BAR_OFREE + t), (q - 1) & 1, wait_ns);
+                        if (!ok) break;
+                        tc_fence_after();
                         const uint32_t p = tmem + TM_S + t * 128;  // P_t as packed bf16 pairs
-                        const uint64_t vd = v_desc + (((g % SV) * BLK_BYTES) >> 4);
 #pragma unroll
                         for (int kk = 0; kk < BN / 16; ++kk)
                             mma_bf16_ts(tmem + TM_O + t * 128, p + kk * 8, vd + ((kk * 2048) >> 4), idO,
                                         j > 0 || kk > 0);
-                        if (t == 1) mma_commit(bar(BAR_VE + g % SV));
+                        if (t == 1) mma_commit(bar(BAR_VE + vst));
+                        // this tile's next S right behind its PV: the other tile's softmax overlaps both
+                        if (j + 1 < it.nb) ok = issue_S(t);
                     }
-                    __syncwarp();
-                    // this tile's next S right behind its PV: the other tile's softmax overlaps both
-                    if (j + 1 < it.nb) ok = issue_S(t, g + 1);
+                    if (++vst == SV) { vst = 0; vph ^= 1; }
+                    pph ^= 1u;
                 }
+                // the item's MMAs (and everything before them) complete: its epilogue may read O
+                mma_commit(bar(BAR_DONE));
+                ++ndone;
+                ++q;
             }
-            // the item's MMAs (and everything before them) complete: its epilogue may read O
-            if (lane == 0) mma_commit(bar(BAR_DONE));
-            __syncwarp();
-            ++ndone;
-            g0 += it.nb;
-            ++q;
+            if (!ok && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
         }
-        if (!ok && lane == 0 && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         const int t = (warp - 2) >> 2;
@@ -447,6 +447,19 @@ attn_tcp_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + t), g & 1, wait_ns) && !aborted(abort_flag));
                 if (!ok) break;
                 tc_fence_after();
+                if (t == 0 && j == ragged_block) {
+                    // zero the V rows past the chunk end (both 64-dim boxes) before PV reads them: the
+                    // block's keys there are masked, but the cache rows may hold non-finite garbage
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + g % SV), (g / SV) & 1, wait_ns));
+                    if (!ok) break;
+                    uint8_t* v0 = gbase + OFF_V + (g % SV) * BLK_BYTES;
+                    for (int x = r; x < (BN - ragged_valid) * 16; x += 128) {
+                        const int rr = ragged_valid + x / 16, c16 = x % 16;
+                        *reinterpret_cast<uint4*>(v0 + (c16 >= 8 ? BOX_BYTES : 0) + rr * 128 + (c16 & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
                 float s[BN];
 #pragma unroll
                 for (int x = 0; x < BN / 32; ++x) tmem_ld32(sbuf + x * 32, s + x * 32);
