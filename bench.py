@@ -35,6 +35,8 @@ Other modes:
         microseconds per graft_tree_attention call of a workload
     --mode lm_head [--rows N --d-model D --vocab V --reps R]
         the fused lm_head argmax and sampling kernels
+    --mode tree --workload W [--drafts flat|confident --reps R]
+        microseconds per graft_build_tree call of a workload
     --mode cpu_step --workload W
         one whole oracle step on the host (run by the default mode in a
         subprocess, to fix the BLAS thread count)
@@ -62,8 +64,8 @@ HEADLINE = "qwen3_235b"
 OTHER_CONFIGS = ["tiny", "llama3_8b", "qwen3_8b_batch", "llama31_8b_long"]
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-ATTN_SOURCES = ["attention_tc.cu", "attention_tcp.cu", "attention_tc1.cu", "attention_mma.cu", "attention.cuh",
-                "attention_api.cu", "tc_ptx.cuh", "common.cuh"]
+ATTN_SOURCES = ["attention_tc.cu", "attention_tcp.cu", "attention_tcs.cu", "attention_tc1.cu", "attention_mma.cu",
+                "attention.cuh", "attention_api.cu", "tc_ptx.cuh", "common.cuh"]
 BLAS_ENV = ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS")
 
 
@@ -73,7 +75,7 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["graft", "reference"], default="graft")
-    p.add_argument("--mode", choices=["step", "attention", "lm_head", "cpu_step"], default="step")
+    p.add_argument("--mode", choices=["step", "attention", "lm_head", "tree", "cpu_step"], default="step")
     p.add_argument("--workload", default=HEADLINE)
     p.add_argument("--configs", default=",".join(OTHER_CONFIGS),
                    help="comma-separated workloads timed beside the headline ('none' for none)")
@@ -84,7 +86,10 @@ def parse_args(argv=None):
     p.add_argument("--reference-budget-s", type=float, default=150.0)
     p.add_argument("--secondary-reps", type=int, default=10,
                    help="replays of the attention / compaction / tree-build graphs (0 skips them and the lm_head)")
-    # --mode attention / lm_head
+    # --mode attention / lm_head / tree
+    p.add_argument("--drafts", choices=["flat", "confident"], default="flat",
+                   help="--mode tree: the workload's drafter logits (flat: pruned at the first checkpoint) or "
+                        "confident rows that draft through every call")
     p.add_argument("--layers", type=int, default=4)
     p.add_argument("--reps", type=int, default=20)
     p.add_argument("--lcap", type=int, default=0)
@@ -938,6 +943,39 @@ def run_lm_head(args):
     print(json.dumps(dict(mode="lm_head", **res)), flush=True)
 
 
+def run_tree(args):
+    """--mode tree: microseconds per graft_build_tree call of a workload (the calls captured in one CUDA
+    graph, the workspace zero-filled once); one JSON line with the stages the calls reached."""
+    import torch
+    from tree_verification_gb300 import _build, synth
+    from tree_verification_gb300 import binding as gb
+    _build.build()
+    dev = torch.device("cuda")
+    wl = synth.WORKLOADS[args.workload]
+    cfg = gb.graft_config_init(wl.Kmax, wl.D, wl.k, wl.V, wl.W, list(wl.checkpoints), wl.tau)
+    dl = synth.draft_logits(wl, dev) if args.drafts == "flat" else synth.peaked_draft_logits(wl, dev, [12.0] * wl.B)
+    roots, L = synth.root_tokens(wl).to(dev), synth.prefix_lengths(wl).to(dev)
+    s_np, _ = synth.zipf_M(wl.V, wl.W, wl.seed + 5) if wl.M_init == "zipf" else synth.empty_M(wl.V, wl.W)
+    M_succ = torch.from_numpy(s_np).to(dev)
+    ws = torch.zeros(max(1, gb.graft_build_tree_workspace_size(cfg, wl.B)), dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = gb.graft_build_tree(cfg, dl, roots, M_succ, L, ws=ws, status=status)
+    n_rep = 20
+
+    def run():
+        for _ in range(n_rep):
+            gb.graft_build_tree(cfg, dl, roots, M_succ, L, out=out, ws=ws, status=status)
+
+    g = _capture(run)
+    for _ in range(3):
+        g.replay()
+    us = _timed(g, args.reps) * 1e6 / (args.reps * n_rep)
+    torch.cuda.synchronize()
+    print(json.dumps({"mode": "tree", "workload": wl.name, "drafts": args.drafts, "batch": wl.B, "vocab": wl.V,
+                      "call_us": us, "stages": sorted(set(out["stage"].cpu().tolist())),
+                      "status": int(status.item())}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.mode == "cpu_step":
@@ -946,6 +984,8 @@ def main(argv=None):
         run_attention(args)
     elif args.mode == "lm_head":
         run_lm_head(args)
+    elif args.mode == "tree":
+        run_tree(args)
     elif args.impl == "reference":
         run_reference(args)
     else:
