@@ -17,12 +17,17 @@
 //               once both tiles' S products have run, a V stage once both
 //               tiles' PV products have run
 //   warp 1      owns the TMEM allocation (512 columns); MMA issuer (one
-//               lane): S_t = Q_t K^T, O_t += P_t V.  The two tiles
+//               thread): S_t = Q_t K^T, O_t += P_t V.  The two tiles
 //               ping-pong: as soon as tile t's P arrives its PV and its next
 //               S are issued, so the tensor pipe works on one tile while the
-//               other tile's softmax runs
+//               other tile's softmax runs.  tcgen05.mma issue hardly queues
+//               ahead of the pipe, so the issuer keeps its own time between
+//               products short: the barrier the next group of products needs
+//               is tested (non-blocking) just before the last two products
+//               of the current group
 //   warps 2-5   softmax + epilogue of tile 0 (one row per thread; warp w
-//               reaches TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31)
+//               reaches TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31); they also
+//               zero a ragged block's V rows before they signal P_0
 //   warps 6-9   softmax + epilogue of tile 1
 // TMEM columns: S_0 [0,128), S_1 [128,256), O_0 [256,384), O_1 [384,512).
 // Softmax overwrites the first 64 columns of S_t with P_t as packed bf16
@@ -88,8 +93,7 @@ constexpr int BAR_S = BAR_VE + SV;    // [tile] S_t ready in TMEM
 constexpr int BAR_P = BAR_S + 2;      // [tile] P_t written to TMEM (128 arrivals)
 constexpr int BAR_DONE = BAR_P + 2;   // every MMA completed (one-shot)
 constexpr int BAR_EPI = BAR_DONE + 1; // [tile] staging written (128 arrivals, one-shot)
-constexpr int BAR_TURN = BAR_EPI + 2; // [tile] the other tile's exponentials of a block are done (128)
-constexpr int N_BARS = BAR_TURN + 2;
+constexpr int N_BARS = BAR_EPI + 2;
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;  // tmem slot, abort flag
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -147,8 +151,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     if (tid == 0) {
         for (int i = 0; i < N_BARS; ++i) {
             uint32_t cnt = 1;
-            if (i == BAR_P || i == BAR_P + 1 || i == BAR_EPI || i == BAR_EPI + 1 || i == BAR_TURN ||
-                i == BAR_TURN + 1)
+            if (i == BAR_P || i == BAR_P + 1 || i == BAR_EPI || i == BAR_EPI + 1)
                 cnt = 128;
             mbar_init(bar(i), cnt);
         }
@@ -271,72 +274,108 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer (lane 0 issues)
-        const uint32_t idS = idesc_bf16(128, BN, false, false);
-        const uint32_t idO = idesc_bf16(128, HD, false, true);
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), 0, wait_ns));
-        // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
-        // start-address field, which sits in the low bits and cannot carry out of them here
-        // (every shared-memory address is below 256 KB).
-        const uint64_t q_desc = sdesc_sw128(base + OFF_Q, 16, 1024);
-        const uint64_t k_desc = sdesc_sw128(base + OFF_K, 16, 1024);
-        const uint64_t v_desc = sdesc_sw128(base + OFF_V, BOX_BYTES, 1024);
-        // S_t(j) = Q_t K(j)^T into S_t; the last tile's product releases K(j)
-        auto issue_S = [&](int t, int j) -> bool {
-            if (t == 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KF + j % SK), (j / SK) & 1, wait_ns))) return false;
-                tc_fence_after();
-            }
-            if (lane == 0) {
-                const uint64_t kd = k_desc + (((j % SK) * BLK_BYTES) >> 4);
+        // ------------------------------------------------------------ MMA issuer (lane 0 alone)
+        // tcgen05.mma issue hardly queues ahead of the tensor pipe, so every cycle this thread
+        // spends between two products, waits included, is a cycle the pipe idles: one thread runs
+        // the loop, and the barrier the next group of products needs is tested (non-blocking)
+        // just before the last two products of the current group, so the blocking wait runs only
+        // when that test came back false.
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16(128, BN, false, false);
+            const uint32_t idO = idesc_bf16(128, HD, false, true);
+            // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
+            // start-address field, which sits in the low bits and cannot carry out of them here
+            // (every shared-memory address is below 256 KB).
+            const uint64_t q_desc = sdesc_sw128(base + OFF_Q, 16, 1024);
+            const uint64_t k_desc = sdesc_sw128(base + OFF_K, 16, 1024);
+            const uint64_t v_desc = sdesc_sw128(base + OFF_V, BOX_BYTES, 1024);
+            // (plain values, no references: address-taken locals would live in local memory)
+            struct Pre {
+                int bar;  // barrier index, -1: none
+                uint32_t ph;
+            };
+            const Pre none{-1, 0u};
+            auto test_pre = [&](Pre pre) -> bool { return pre.bar < 0 || mbar_test_now(bar(pre.bar), pre.ph); };
+            auto wait_pre = [&](Pre pre, bool ready) -> bool {
+                return ready || mbar_wait(bar(pre.bar), pre.ph, wait_ns);
+            };
+            // S_t(jj) = Q_t K(jj)^T into S_t; the last tile's product releases K(jj)
+            auto group_S = [&](int t, int jj, Pre nxt) -> bool {
+                bool ready = false;
+                const uint64_t kd = k_desc + (((jj % SK) * BLK_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
+                    if (kk == HD / 16 - 2) ready = test_pre(nxt);
                     const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
                     const uint32_t qoff = t * Q_TILE_BYTES + (kk >> 2) * (Q_TILE_BYTES / 2) + (kk & 3) * 32;
                     mma_bf16_ss(tmem + TM_S + t * 128, q_desc + (qoff >> 4), kd + (off >> 4), idS, kk > 0);
                 }
                 mma_commit(bar(BAR_S + t));
-                if (t == ntile - 1) mma_commit(bar(BAR_KE + j % SK));
-            }
-            __syncwarp();
-            return true;
-        };
-        if (ok) tc_fence_after();
-        for (int t = 0; t < ntile && ok && nb > 0; ++t) ok = issue_S(t, 0);
-        for (int j = 0; j < nb && ok; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + j % SV), (j / SV) & 1, wait_ns));
-            if (!ok) break;
-            if (j == ragged_block) {
-                // zero the V rows past the chunk end (both 64-dim boxes) before any PV reads them
-                uint8_t* v0 = gbase + OFF_V + (j % SV) * BLK_BYTES;
-                for (int i = lane; i < (BN - ragged_valid) * 16; i += 32) {
-                    const int r = ragged_valid + i / 16, q = i % 16;
-                    *reinterpret_cast<uint4*>(v0 + (q >= 8 ? BOX_BYTES : 0) + r * 128 + (q & 7) * 16) =
-                        make_uint4(0, 0, 0, 0);
+                if (t == ntile - 1) mma_commit(bar(BAR_KE + jj % SK));
+                return ready;
+            };
+            // O_t += P_t V(j); the last tile's product releases V(j)
+            auto group_PV = [&](int t, int j, Pre nxt) -> bool {
+                bool ready = false;
+                const uint32_t p = tmem + TM_S + t * 128;  // P_t as packed bf16 pairs
+                const uint64_t vd = v_desc + (((j % SV) * BLK_BYTES) >> 4);
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    if (kk == BN / 16 - 2) ready = test_pre(nxt);
+                    mma_bf16_ts(tmem + TM_O + t * 128, p + kk * 8, vd + ((kk * 2048) >> 4), idO, j > 0 || kk > 0);
                 }
-                fence_proxy_async_smem();
-                __syncwarp();
+                if (t == ntile - 1) mma_commit(bar(BAR_VE + j % SV));
+                return ready;
+            };
+            bool ok = mbar_wait(bar(BAR_Q), 0, wait_ns) && (nb == 0 || mbar_wait(bar(BAR_KF), 0, wait_ns));
+            Pre vf{BAR_VF, 0u};
+            bool vf_ready = false;
+            if (ok && nb > 0) {
+                tc_fence_after();
+                if (ntile == 2) group_S(0, 0, none);
+                vf_ready = group_S(ntile - 1, 0, vf);
             }
-            for (int t = 0; t < ntile && ok; ++t) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(bar(BAR_P + t), j & 1, wait_ns) && !aborted(abort_flag));
+            // (tile 0's softmax warps zero a ragged block's V rows past the chunk end before they
+            // signal P_0, so every PV of that block, issued after that signal, reads zeros there)
+            for (int j = 0; j < nb && ok; ++j) {
+                const bool more = j + 1 < nb;
+                ok = wait_pre(vf, vf_ready) && mbar_wait(bar(BAR_P), j & 1, wait_ns) && !aborted(abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                if (lane == 0) {
-                    const uint32_t p = tmem + TM_S + t * 128;  // P_t as packed bf16 pairs
-                    const uint64_t vd = v_desc + (((j % SV) * BLK_BYTES) >> 4);
-#pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
-                        mma_bf16_ts(tmem + TM_O + t * 128, p + kk * 8, vd + ((kk * 2048) >> 4), idO, j > 0 || kk > 0);
-                    if (t == ntile - 1) mma_commit(bar(BAR_VE + j % SV));
+                const Pre kf{BAR_KF + (j + 1) % SK, (uint32_t)(((j + 1) / SK) & 1)};
+                const Pre p1{BAR_P + 1, (uint32_t)(j & 1)};
+                const Pre vn{BAR_VF + (j + 1) % SV, (uint32_t)(((j + 1) / SV) & 1)};
+                if (ntile == 2) {
+                    bool p1_ready;
+                    if (more) {
+                        const bool kf_ready = group_PV(0, j, kf);
+                        // this tile's next S right behind its PV: the other tile's softmax overlaps both
+                        ok = wait_pre(kf, kf_ready);
+                        if (!ok) break;
+                        tc_fence_after();
+                        p1_ready = group_S(0, j + 1, p1);
+                    } else {
+                        p1_ready = group_PV(0, j, p1);
+                    }
+                    ok = wait_pre(p1, p1_ready);
+                    if (!ok) break;
+                    tc_fence_after();
+                    group_PV(1, j, none);
+                    vf_ready = more ? group_S(1, j + 1, vn) : false;
+                } else if (more) {
+                    const bool kf_ready = group_PV(0, j, kf);
+                    ok = wait_pre(kf, kf_ready);
+                    if (!ok) break;
+                    tc_fence_after();
+                    vf_ready = group_S(0, j + 1, vn);
+                } else {
+                    group_PV(0, j, none);
                 }
-                __syncwarp();
-                // this tile's next S right behind its PV: the other tile's softmax overlaps both
-                if (j + 1 < nb) ok = issue_S(t, j + 1);
+                vf = vn;
             }
+            if (!ok && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
+            mma_commit(bar(BAR_DONE));
         }
-        if (!ok && lane == 0 && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
-        if (lane == 0) mma_commit(bar(BAR_DONE));
         __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
@@ -356,6 +395,19 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + t), j & 1, wait_ns) && !aborted(abort_flag));
             if (!ok) break;
             tc_fence_after();
+            if (t == 0 && j == ragged_block) {
+                // zero the V rows past the chunk end (both 64-dim boxes) before PV reads them: the
+                // block's keys there are masked, but the cache rows may hold non-finite garbage
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + j % SV), (j / SV) & 1, wait_ns));
+                if (!ok) break;
+                uint8_t* v0 = gbase + OFF_V + (j % SV) * BLK_BYTES;
+                for (int x = r; x < (BN - ragged_valid) * 16; x += 128) {
+                    const int rr = ragged_valid + x / 16, c16 = x % 16;
+                    *reinterpret_cast<uint4*>(v0 + (c16 >= 8 ? BOX_BYTES : 0) + rr * 128 + (c16 & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
             float s[BN];
 #pragma unroll
             for (int q = 0; q < BN / 32; ++q) tmem_ld32(sbuf + q * 32, s + q * 32);
@@ -405,14 +457,6 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
             const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
             float2 acc = make_float2(0.f, 0.f);
-            // The two tiles take turns at the exponentials (tile 0 first in every block), so
-            // one tile's P is ready early and its PV and next S run on the tensor pipe while
-            // the other tile's exponentials run, instead of both P arriving together.
-            if (ntile == 2 && (t == 1 || j > 0)) {
-                const int ph = t == 1 ? (j & 1) : ((j - 1) & 1);
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_TURN + t), ph, wait_ns) && !aborted(abort_flag));
-                if (!ok) break;
-            }
 #pragma unroll
             for (int hh = 0; hh < 4; ++hh) {
                 float packed[16];
@@ -426,7 +470,6 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 }
                 tmem_st16(sbuf + hh * 16, packed);  // P over the first 64 columns of S_t
             }
-            if (ntile == 2) mbar_arrive(bar(BAR_TURN + (1 - t)));
             if (rescale) {
                 // S_t(j) was issued after PV_t(j - 1) on the in-order tensor pipe, so its
                 // completion means O_t already holds every earlier block; PV_t(j) waits for P_t(j)

@@ -24,12 +24,17 @@
 //     from registers (bf16 output rows, or fp32 partial rows and their
 //     log2-sum-exp for the merge kernel), so it overlaps the next item's
 //     first S product and softmax instead of staging through the rings.
-// Everything else (TMEM layout, masking, lazy rescale, turn-taking
-// exponentials of the two tiles) is the two-tile kernel's, except two warp
-// roles: the MMA issuer is a single thread with running ring counters (the
-// tensor pipe queues hardly any products ahead, so the issuer's own time
-// between products is pipe idle time), and tile 0's softmax warps zero a
-// ragged block's V rows past the chunk end before they signal P_0.
+// Everything else (TMEM layout, masking, lazy rescale) is the two-tile
+// kernel's, except:
+//   * the MMA issuer is a single thread with running ring counters, and it
+//     tests the barrier of the next group of products (non-blocking) just
+//     before the last two products of the current group: the tensor pipe
+//     queues hardly any products ahead, so the issuer's own time between
+//     products, waits included, is pipe idle time;
+//   * the two tiles' softmax warps run their exponentials freely (no
+//     turn-taking hand-off between the tiles);
+//   * tile 0's softmax warps zero a ragged block's V rows past the chunk end
+//     before they signal P_0.
 //
 // Every mbarrier wait is bounded; on timeout the CTA raises
 // GRAFT_STATUS_TIMEOUT, stops issuing work, drains what it issued (again
@@ -79,8 +84,7 @@ constexpr int BAR_S = BAR_VE + SV;    // [tile] S_t ready in TMEM
 constexpr int BAR_P = BAR_S + 2;      // [tile] P_t written to TMEM (128 arrivals)
 constexpr int BAR_DONE = BAR_P + 2;   // an item's MMAs completed (one phase per item)
 constexpr int BAR_OFREE = BAR_DONE + 1;  // [tile] an item's O_t read out of TMEM (128 arrivals)
-constexpr int BAR_TURN = BAR_OFREE + 2;  // [tile] the other tile's exponentials of a block are done (128)
-constexpr int N_BARS = BAR_TURN + 2;
+constexpr int N_BARS = BAR_OFREE + 2;
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;  // tmem slot, abort flag
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -211,9 +215,7 @@ attn_tcp_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     if (tid == 0) {
         for (int i = 0; i < N_BARS; ++i) {
             uint32_t cnt = 1;
-            if (i == BAR_P || i == BAR_P + 1 || i == BAR_OFREE || i == BAR_OFREE + 1 || i == BAR_TURN ||
-                i == BAR_TURN + 1)
-                cnt = 128;
+            if (i == BAR_P || i == BAR_P + 1 || i == BAR_OFREE || i == BAR_OFREE + 1) cnt = 128;
             mbar_init(bar(i), cnt);
         }
         *abort_flag = 0;
@@ -340,15 +342,25 @@ attn_tcp_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             int kst = 0, kph = 0;  // K ring: stage and phase of the next block the S products read
             int vst = 0, vph = 0;  // V ring: stage and phase of the next block the PV products read
             uint32_t pph = 0;      // phase of the S and P barriers of the current block (g & 1)
-            // S_t = Q_t K^T of the next K block into S_t; tile 1's product releases that K stage
-            auto issue_S = [&](int t) -> bool {
-                if (t == 0) {
-                    if (!mbar_wait(bar(BAR_KF + kst), kph, wait_ns)) return false;
-                    tc_fence_after();
-                }
+            // A group of eight products; just before its last two, a non-blocking test of the barrier
+            // the next group needs is issued, so its latency overlaps the blocked issue of these
+            // products; the blocking wait then runs only if the test came back false.  (Plain values,
+            // no references: address-taken locals would live in local memory.)
+            struct Pre {
+                int bar;  // barrier index, -1: none
+                uint32_t ph;
+            };
+            const Pre none{-1, 0u};
+            auto test_pre = [&](Pre pre) -> bool { return pre.bar < 0 || mbar_test_now(bar(pre.bar), pre.ph); };
+            auto wait_pre = [&](Pre pre, bool ready) -> bool {
+                return ready || mbar_wait(bar(pre.bar), pre.ph, wait_ns);
+            };
+            auto group_S = [&](int t, Pre nxt) -> bool {
+                bool ready = false;
                 const uint64_t kd = k_desc + ((kst * BLK_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
+                    if (kk == HD / 16 - 2) ready = test_pre(nxt);
                     const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
                     const uint32_t qoff = t * Q_TILE_BYTES + (kk >> 2) * (Q_TILE_BYTES / 2) + (kk & 3) * 32;
                     mma_bf16_ss(tmem + TM_S + t * 128, q_desc + (qoff >> 4), kd + (off >> 4), idS, kk > 0);
@@ -358,7 +370,19 @@ attn_tcp_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                     mma_commit(bar(BAR_KE + kst));
                     if (++kst == SK) { kst = 0; kph ^= 1; }
                 }
-                return true;
+                return ready;
+            };
+            auto group_PV = [&](int t, bool first, Pre nxt) -> bool {
+                bool ready = false;
+                const uint64_t vd = v_desc + ((vst * BLK_BYTES) >> 4);
+                const uint32_t p = tmem + TM_S + t * 128;  // P_t as packed bf16 pairs
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    if (kk == BN / 16 - 2) ready = test_pre(nxt);
+                    mma_bf16_ts(tmem + TM_O + t * 128, p + kk * 8, vd + ((kk * 2048) >> 4), idO, !first || kk > 0);
+                }
+                if (t == 1) mma_commit(bar(BAR_VE + vst));
+                return ready;
             };
             bool ok = true;
             int q = 0;  // live items issued
@@ -367,32 +391,46 @@ attn_tcp_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 if (i < 0) break;
                 const Item it = make_item(a, order, i, nrb2);
                 if (it.skip) continue;
-                ok = mbar_wait(bar(BAR_Q), q & 1, wait_ns) && !aborted(abort_flag);
+                ok = mbar_wait(bar(BAR_Q), q & 1, wait_ns) && !aborted(abort_flag) &&
+                     mbar_wait(bar(BAR_KF + kst), kph, wait_ns);
                 if (!ok) break;
                 tc_fence_after();
-                ok = issue_S(0) && issue_S(1);
+                group_S(0, none);
+                Pre vf{BAR_VF + vst, (uint32_t)vph};
+                bool vf_ready = group_S(1, vf);
                 for (int j = 0; j < it.nb && ok; ++j) {
                     // (tile 0's softmax warps zero a ragged block's V rows past the chunk end before
                     // they signal P_0, so PV_0 and PV_1, issued after that signal, read zeros there)
-                    ok = mbar_wait(bar(BAR_VF + vst), vph, wait_ns);
+                    const bool more = j + 1 < it.nb;
+                    ok = wait_pre(vf, vf_ready) && mbar_wait(bar(BAR_P), pph, wait_ns);
+                    // the item's first PV overwrites O_t: the previous item's epilogue must have read it
+                    if (ok && j == 0 && q > 0) ok = mbar_wait(bar(BAR_OFREE), (q - 1) & 1, wait_ns);
                     if (!ok) break;
-                    const uint64_t vd = v_desc + ((vst * BLK_BYTES) >> 4);
-                    for (int t = 0; t < 2 && ok; ++t) {
-                        ok = mbar_wait(bar(BAR_P + t), pph, wait_ns);
-                        // the item's first PV overwrites O_t: the previous item's epilogue must have read it
-                        if (ok && j == 0 && q > 0) ok = mbar_wait(bar(BAR_OFREE + t), (q - 1) & 1, wait_ns);
+                    tc_fence_after();
+                    const Pre kf{BAR_KF + kst, (uint32_t)kph};
+                    const Pre p1{BAR_P + 1, pph};
+                    bool p1_ready;
+                    if (more) {
+                        const bool kf_ready = group_PV(0, j == 0, kf);
+                        // this tile's next S right behind its PV: the other tile's softmax overlaps both
+                        ok = wait_pre(kf, kf_ready);
                         if (!ok) break;
                         tc_fence_after();
-                        const uint32_t p = tmem + TM_S + t * 128;  // P_t as packed bf16 pairs
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk)
-                            mma_bf16_ts(tmem + TM_O + t * 128, p + kk * 8, vd + ((kk * 2048) >> 4), idO,
-                                        j > 0 || kk > 0);
-                        if (t == 1) mma_commit(bar(BAR_VE + vst));
-                        // this tile's next S right behind its PV: the other tile's softmax overlaps both
-                        if (j + 1 < it.nb) ok = issue_S(t);
+                        p1_ready = group_S(0, p1);
+                    } else {
+                        p1_ready = group_PV(0, j == 0, p1);
                     }
-                    if (++vst == SV) { vst = 0; vph ^= 1; }
+                    ok = wait_pre(p1, p1_ready);
+                    if (ok && j == 0 && q > 0) ok = mbar_wait(bar(BAR_OFREE + 1), (q - 1) & 1, wait_ns);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const int vst_next = vst + 1 == SV ? 0 : vst + 1;
+                    const int vph_next = vst + 1 == SV ? vph ^ 1 : vph;
+                    vf = Pre{BAR_VF + vst_next, (uint32_t)vph_next};
+                    group_PV(1, j == 0, none);
+                    vf_ready = more ? group_S(1, vf) : false;
+                    vst = vst_next;
+                    vph = vph_next;
                     pph ^= 1u;
                 }
                 // the item's MMAs (and everything before them) complete: its epilogue may read O
@@ -507,12 +545,6 @@ attn_tcp_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
                 const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
                 float2 acc = make_float2(0.f, 0.f);
-                // the tiles take turns at the exponentials, tile 0 first in every block
-                if (t == 1 || g > 0) {
-                    const int ph = t == 1 ? (g & 1) : ((g - 1) & 1);
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_TURN + t), ph, wait_ns) && !aborted(abort_flag));
-                    if (!ok) break;
-                }
 #pragma unroll
                 for (int hh = 0; hh < 4; ++hh) {
                     float packed[16];
@@ -526,7 +558,6 @@ attn_tcp_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                     }
                     tmem_st16(sbuf + hh * 16, packed);  // P over the first 64 columns of S_t
                 }
-                mbar_arrive(bar(BAR_TURN + (1 - t)));
                 if (rescale) {
                     // S_t(g) was issued after PV_t(g - 1) on the in-order tensor pipe, so its
                     // completion means O_t already holds every earlier block of the item
