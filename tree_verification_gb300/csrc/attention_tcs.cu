@@ -32,9 +32,10 @@
 // running across pieces with running stage and phase counters, the next
 // piece's Q tiles loaded once the current piece's last S product has run,
 // the epilogue writing rows from registers after signalling that the next
-// piece's first PV may overwrite O in TMEM; warp roles, TMEM layout,
-// masking, lazy rescale and the two tiles' turn-taking at the exponentials
-// are the two-tile kernel's.
+// piece's first PV may overwrite O in TMEM, a single-thread MMA issuer that
+// tests the next group's barrier before the last two products of the
+// current group, and free-running exponentials of the two tiles; TMEM
+// layout, masking and lazy rescale are the two-tile kernel's.
 //
 // Every mbarrier wait is bounded; on timeout the CTA raises
 // GRAFT_STATUS_TIMEOUT, stops issuing work, drains what it issued (again
@@ -79,9 +80,8 @@ constexpr int BAR_S = BAR_VE + SV;    // [tile] S_t ready in TMEM
 constexpr int BAR_P = BAR_S + 2;      // [tile] P_t written to TMEM (128 arrivals)
 constexpr int BAR_DONE = BAR_P + 2;   // an item's MMAs completed (one phase per item)
 constexpr int BAR_OFREE = BAR_DONE + 1;  // [tile] an item's O_t read out of TMEM (128 arrivals)
-constexpr int BAR_TURN = BAR_OFREE + 2;  // [tile] the other tile's exponentials of a block are done (128)
 // a CTA runs at most two cut pieces, its first (slot kind 0) and its last (kind 1): one-shot barriers
-constexpr int BAR_CUT = BAR_TURN + 2;    // [kind][tile] a cut piece's partial rows written (128 arrivals)
+constexpr int BAR_CUT = BAR_OFREE + 2;    // [kind][tile] a cut piece's partial rows written (128 arrivals)
 constexpr int BAR_CUTL = BAR_CUT + 4;    // [kind][tile] its arrival counter read (one arrival)
 constexpr int N_BARS = BAR_CUTL + 4;
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;  // tmem slot, abort flag
@@ -256,8 +256,8 @@ attn_tcs_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     if (tid == 0) {
         for (int i = 0; i < N_BARS; ++i) {
             uint32_t cnt = 1;
-            if (i == BAR_P || i == BAR_P + 1 || i == BAR_OFREE || i == BAR_OFREE + 1 || i == BAR_TURN ||
-                i == BAR_TURN + 1 || (i >= BAR_CUT && i < BAR_CUT + 4))
+            if (i == BAR_P || i == BAR_P + 1 || i == BAR_OFREE || i == BAR_OFREE + 1 ||
+                (i >= BAR_CUT && i < BAR_CUT + 4))
                 cnt = 128;
             mbar_init(bar(i), cnt);
         }
@@ -408,88 +408,118 @@ attn_tcs_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer (lane 0 issues)
-        const uint32_t idS = idesc_bf16(128, BN, false, false);
-        const uint32_t idO = idesc_bf16(128, HD, false, true);
-        // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
-        // start-address field, which sits in the low bits and cannot carry out of them here
-        // (every shared-memory address is below 256 KB).
-        const uint64_t q_desc = sdesc_sw128(base + OFF_Q, 16, 1024);
-        const uint64_t k_desc = sdesc_sw128(base + OFF_K, 16, 1024);
-        const uint64_t v_desc = sdesc_sw128(base + OFF_V, BOX_BYTES, 1024);
-        // S_t(g) = Q_t K(g)^T into S_t; tile 1's product releases K(g)
-        auto issue_S = [&](int t, int g) -> bool {
-            if (t == 0) {
-                if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KF + g % SK), (g / SK) & 1, wait_ns))) return false;
-                tc_fence_after();
-            }
-            if (lane == 0) {
-                const uint64_t kd = k_desc + (((g % SK) * BLK_BYTES) >> 4);
+        // ------------------------------------------------------------ MMA issuer (lane 0 alone)
+        // tcgen05.mma issue hardly queues ahead of the tensor pipe, so every cycle this thread
+        // spends between two products, waits included, is a cycle the pipe idles: one thread runs
+        // the loop with running ring counters, and the barrier the next group of products needs is
+        // tested (non-blocking) just before the last two products of the current group.
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16(128, BN, false, false);
+            const uint32_t idO = idesc_bf16(128, HD, false, true);
+            // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
+            // start-address field, which sits in the low bits and cannot carry out of them here
+            // (every shared-memory address is below 256 KB).
+            const uint64_t q_desc = sdesc_sw128(base + OFF_Q, 16, 1024);
+            const uint64_t k_desc = sdesc_sw128(base + OFF_K, 16, 1024);
+            const uint64_t v_desc = sdesc_sw128(base + OFF_V, BOX_BYTES, 1024);
+            int kst = 0, kph = 0;  // K ring: stage and phase of the next block the S products read
+            int vst = 0, vph = 0;  // V ring: stage and phase of the next block the PV products read
+            uint32_t pph = 0;      // phase of the S and P barriers of the current block (g & 1)
+            // (plain values, no references: address-taken locals would live in local memory)
+            struct Pre {
+                int bar;  // barrier index, -1: none
+                uint32_t ph;
+            };
+            const Pre none{-1, 0u};
+            auto test_pre = [&](Pre pre) -> bool { return pre.bar < 0 || mbar_test_now(bar(pre.bar), pre.ph); };
+            auto wait_pre = [&](Pre pre, bool ready) -> bool {
+                return ready || mbar_wait(bar(pre.bar), pre.ph, wait_ns);
+            };
+            auto group_S = [&](int t, Pre nxt) -> bool {
+                bool ready = false;
+                const uint64_t kd = k_desc + ((kst * BLK_BYTES) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
+                    if (kk == HD / 16 - 2) ready = test_pre(nxt);
                     const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
                     const uint32_t qoff = t * Q_TILE_BYTES + (kk >> 2) * (Q_TILE_BYTES / 2) + (kk & 3) * 32;
                     mma_bf16_ss(tmem + TM_S + t * 128, q_desc + (qoff >> 4), kd + (off >> 4), idS, kk > 0);
                 }
                 mma_commit(bar(BAR_S + t));
-                if (t == 1) mma_commit(bar(BAR_KE + g % SK));
-            }
-            __syncwarp();
-            return true;
-        };
-        bool ok = true;
-        int q = 0, g0 = 0;  // pieces issued, global ring index of the piece's first block
-        int w = walk_start(a);
-        Item it;
-        while (ok && next_item(w, a, it)) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), q & 1, wait_ns) && !aborted(abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            for (int t = 0; t < 2 && ok; ++t) ok = issue_S(t, g0);
-            for (int j = it.jb; j < it.je && ok; ++j) {
-                const int g = g0 + (j - it.jb);
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + g % SV), (g / SV) & 1, wait_ns));
-                if (!ok) break;
-                if (j == it.ragged_block) {
-                    // zero the V rows past the chunk end (both 64-dim boxes) before any PV reads them
-                    uint8_t* v0 = gbase + OFF_V + (g % SV) * BLK_BYTES;
-                    for (int x = lane; x < (BN - it.ragged_valid) * 16; x += 32) {
-                        const int r = it.ragged_valid + x / 16, c16 = x % 16;
-                        *reinterpret_cast<uint4*>(v0 + (c16 >= 8 ? BOX_BYTES : 0) + r * 128 + (c16 & 7) * 16) =
-                            make_uint4(0, 0, 0, 0);
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
+                if (t == 1) {
+                    mma_commit(bar(BAR_KE + kst));
+                    if (++kst == SK) { kst = 0; kph ^= 1; }
                 }
-                for (int t = 0; t < 2 && ok; ++t) {
-                    bool wt = mbar_wait(bar(BAR_P + t), g & 1, wait_ns);
+                return ready;
+            };
+            auto group_PV = [&](int t, bool first, Pre nxt) -> bool {
+                bool ready = false;
+                const uint64_t vd = v_desc + ((vst * BLK_BYTES) >> 4);
+                const uint32_t p = tmem + TM_S + t * 128;  // P_t as packed bf16 pairs
+#pragma unroll
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    if (kk == BN / 16 - 2) ready = test_pre(nxt);
+                    mma_bf16_ts(tmem + TM_O + t * 128, p + kk * 8, vd + ((kk * 2048) >> 4), idO, !first || kk > 0);
+                }
+                if (t == 1) mma_commit(bar(BAR_VE + vst));
+                return ready;
+            };
+            bool ok = true;
+            int q = 0;  // pieces issued
+            int w = walk_start(a);
+            Item it;
+            while (ok && next_item(w, a, it)) {
+                ok = mbar_wait(bar(BAR_Q), q & 1, wait_ns) && !aborted(abort_flag) &&
+                     mbar_wait(bar(BAR_KF + kst), kph, wait_ns);
+                if (!ok) break;
+                tc_fence_after();
+                group_S(0, none);
+                Pre vf{BAR_VF + vst, (uint32_t)vph};
+                bool vf_ready = group_S(1, vf);
+                for (int j = it.jb; j < it.je && ok; ++j) {
+                    // (tile 0's softmax warps zero a ragged block's V rows past the chunk end before
+                    // they signal P_0, so PV_0 and PV_1, issued after that signal, read zeros there)
+                    const bool more = j + 1 < it.je;
+                    const bool first = j == it.jb;
+                    ok = wait_pre(vf, vf_ready) && mbar_wait(bar(BAR_P), pph, wait_ns);
                     // the piece's first PV overwrites O_t: the previous piece's epilogue must have read it
-                    if (wt && j == it.jb && q > 0) wt = mbar_wait(bar(BAR_OFREE + t), (q - 1) & 1, wait_ns);
-                    ok = __all_sync(0xffffffffu, wt && !aborted(abort_flag));
+                    if (ok && first && q > 0) ok = mbar_wait(bar(BAR_OFREE), (q - 1) & 1, wait_ns);
                     if (!ok) break;
                     tc_fence_after();
-                    if (lane == 0) {
-                        const uint32_t p = tmem + TM_S + t * 128;  // P_t as packed bf16 pairs
-                        const uint64_t vd = v_desc + (((g % SV) * BLK_BYTES) >> 4);
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk)
-                            mma_bf16_ts(tmem + TM_O + t * 128, p + kk * 8, vd + ((kk * 2048) >> 4), idO,
-                                        j > it.jb || kk > 0);
-                        if (t == 1) mma_commit(bar(BAR_VE + g % SV));
+                    const Pre kf{BAR_KF + kst, (uint32_t)kph};
+                    const Pre p1{BAR_P + 1, pph};
+                    bool p1_ready;
+                    if (more) {
+                        const bool kf_ready = group_PV(0, first, kf);
+                        // this tile's next S right behind its PV: the other tile's softmax overlaps both
+                        ok = wait_pre(kf, kf_ready);
+                        if (!ok) break;
+                        tc_fence_after();
+                        p1_ready = group_S(0, p1);
+                    } else {
+                        p1_ready = group_PV(0, first, p1);
                     }
-                    __syncwarp();
-                    // this tile's next S right behind its PV: the other tile's softmax overlaps both
-                    if (j + 1 < it.je) ok = issue_S(t, g + 1);
+                    ok = wait_pre(p1, p1_ready);
+                    if (ok && first && q > 0) ok = mbar_wait(bar(BAR_OFREE + 1), (q - 1) & 1, wait_ns);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const int vst_next = vst + 1 == SV ? 0 : vst + 1;
+                    const int vph_next = vst + 1 == SV ? vph ^ 1 : vph;
+                    vf = Pre{BAR_VF + vst_next, (uint32_t)vph_next};
+                    group_PV(1, first, none);
+                    vf_ready = more ? group_S(1, vf) : false;
+                    vst = vst_next;
+                    vph = vph_next;
+                    pph ^= 1u;
                 }
+                // the piece's MMAs (and everything before them) complete: its epilogue may read O
+                mma_commit(bar(BAR_DONE));
+                ++ndone;
+                ++q;
             }
-            // the piece's MMAs (and everything before them) complete: its epilogue may read O
-            if (lane == 0) mma_commit(bar(BAR_DONE));
-            __syncwarp();
-            ++ndone;
-            g0 += it.je - it.jb;
-            ++q;
+            if (!ok && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
         }
-        if (!ok && lane == 0 && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + epilogue
         const int t = (warp - 2) >> 2;
@@ -523,6 +553,19 @@ attn_tcs_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_S + t), g & 1, wait_ns) && !aborted(abort_flag));
                 if (!ok) break;
                 tc_fence_after();
+                if (t == 0 && j == ragged_block) {
+                    // zero the V rows past the chunk end (both 64-dim boxes) before PV reads them: the
+                    // block's keys there are masked, but the cache rows may hold non-finite garbage
+                    ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + g % SV), (g / SV) & 1, wait_ns));
+                    if (!ok) break;
+                    uint8_t* v0 = gbase + OFF_V + (g % SV) * BLK_BYTES;
+                    for (int x = r; x < (BN - ragged_valid) * 16; x += 128) {
+                        const int rr = ragged_valid + x / 16, c16 = x % 16;
+                        *reinterpret_cast<uint4*>(v0 + (c16 >= 8 ? BOX_BYTES : 0) + rr * 128 + (c16 & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
+                    }
+                    fence_proxy_async_smem();
+                }
                 float s[BN];
 #pragma unroll
                 for (int x = 0; x < BN / 32; ++x) tmem_ld32(sbuf + x * 32, s + x * 32);
@@ -570,12 +613,6 @@ attn_tcs_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                 const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
                 const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
                 float2 acc = make_float2(0.f, 0.f);
-                // the tiles take turns at the exponentials, tile 0 first in every block
-                if (t == 1 || g > 0) {
-                    const int ph = t == 1 ? (g & 1) : ((g - 1) & 1);
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_TURN + t), ph, wait_ns) && !aborted(abort_flag));
-                    if (!ok) break;
-                }
 #pragma unroll
                 for (int hh = 0; hh < 4; ++hh) {
                     float packed[16];
@@ -589,7 +626,6 @@ attn_tcs_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                     }
                     tmem_st16(sbuf + hh * 16, packed);  // P over the first 64 columns of S_t
                 }
-                mbar_arrive(bar(BAR_TURN + (1 - t)));
                 if (rescale) {
                     // S_t(g) was issued after PV_t(g - 1) on the in-order tensor pipe, so its
                     // completion means O_t already holds every earlier block of the piece
