@@ -19,12 +19,15 @@
 //               stage is released as soon as its S product has run
 //   warp 3      TMA producer: V blocks into their own 3-stage ring, a stage
 //               released once its PV product has run
-//   warp 1      MMA issuer (one lane): S = Q K^T with both operands in
+//   warp 1      MMA issuer (one thread): S = Q K^T with both operands in
 //               shared memory, then O += P V with P read from TMEM;
-//               shared-memory descriptors are built once and offset per MMA
+//               shared-memory descriptors are built once and offset per MMA;
+//               the barrier the next group of products needs is tested
+//               (non-blocking) before the last two products of the current
+//               group, since tcgen05.mma issue hardly queues ahead of the pipe
 //   warp 2      owns the TMEM allocation (512 columns)
 //   warps 4-7   softmax + epilogue (TMEM lanes 0-127, one query row per
-//               thread)
+//               thread); they zero a ragged block's V rows before its P
 // TMEM columns: S/P double buffer [0,128) and [128,256), O [256,384).  The
 // first S product issues as soon as the Q tile and the first K block have
 // landed: Q is read by the tensor core from shared memory, which measured
@@ -252,66 +255,95 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer (lane 0 issues)
-        const uint32_t idS = idesc_bf16(128, BN, false, false);
-        const uint32_t idO = idesc_bf16(128, HD, false, true);
-        bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_Q), 0, wait_ns));
-        // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
-        // start-address field, which sits in the low bits and cannot carry out of them here
-        // (every shared-memory address is below 256 KB).
-        const uint64_t q_desc = sdesc_sw128(base + OFF_Q, 16, 1024);
-        const uint64_t k_desc = sdesc_sw128(base + OFF_K, 16, 1024);
-        const uint64_t v_desc = sdesc_sw128(base + OFF_V, BOX_BYTES, 1024);
-        // S(j) into S/P buffer j % 2, then release K(j)
-        auto issue_S = [&](int j) -> bool {
-            if (!__all_sync(0xffffffffu, mbar_wait(bar(BAR_KF + j % SK), (j / SK) & 1, wait_ns))) return false;
-            tc_fence_after();
-            if (lane == 0) {
+        // ------------------------------------------------------------ MMA issuer (lane 0 alone)
+        // tcgen05.mma issue hardly queues ahead of the tensor pipe, so every cycle this thread
+        // spends between two products, waits included, is a cycle the pipe idles: one thread runs
+        // the loop, and the barrier the next group of products needs is tested (non-blocking) just
+        // before the last two products of the current group.
+        if (lane == 0) {
+            const uint32_t idS = idesc_bf16(128, BN, false, false);
+            const uint32_t idO = idesc_bf16(128, HD, false, true);
+            // Descriptors are built once; each MMA adds a byte offset (in 16-byte units) to the
+            // start-address field, which sits in the low bits and cannot carry out of them here
+            // (every shared-memory address is below 256 KB).
+            const uint64_t q_desc = sdesc_sw128(base + OFF_Q, 16, 1024);
+            const uint64_t k_desc = sdesc_sw128(base + OFF_K, 16, 1024);
+            const uint64_t v_desc = sdesc_sw128(base + OFF_V, BOX_BYTES, 1024);
+            // (plain values, no references: address-taken locals would live in local memory)
+            struct Pre {
+                int bar;  // barrier index, -1: none
+                uint32_t ph;
+            };
+            const Pre none{-1, 0u};
+            auto test_pre = [&](Pre pre) -> bool { return pre.bar < 0 || mbar_test_now(bar(pre.bar), pre.ph); };
+            auto wait_pre = [&](Pre pre, bool ready) -> bool {
+                return ready || mbar_wait(bar(pre.bar), pre.ph, wait_ns);
+            };
+            auto kf_of = [&](int j) { return j < nb ? Pre{BAR_KF + j % SK, (uint32_t)((j / SK) & 1)} : none; };
+            auto vf_of = [&](int j) { return j < nb ? Pre{BAR_VF + j % SV, (uint32_t)((j / SV) & 1)} : none; };
+            // S(j) into S/P buffer j % 2, then the release of K(j)
+            auto group_S = [&](int j, Pre nxt) -> bool {
+                bool ready = false;
                 const uint64_t kd = k_desc + (((j % SK) * BLK_BYTES) >> 4);
                 const uint32_t d = tmem + TM_S + (j & 1) * 128;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
+                    if (kk == HD / 16 - 2) ready = test_pre(nxt);
                     const uint32_t off = (kk >> 2) * BOX_BYTES + (kk & 3) * 32;
                     mma_bf16_ss(d, q_desc + (off >> 4), kd + (off >> 4), idS, kk > 0);
                 }
                 mma_commit(bar(BAR_S + (j & 1)));
                 mma_commit(bar(BAR_KE + j % SK));
-            }
-            __syncwarp();
-            return true;
-        };
-        if (ok) tc_fence_after();
-        for (int j = 0; j < 2 && j < nb && ok; ++j) ok = issue_S(j);
-        for (int j = 0; j < nb && ok; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + j % SV), (j / SV) & 1, wait_ns));
-            if (!ok) break;
-            if (j == ragged_block) {
-                // zero the V rows past the chunk end (both 64-dim boxes) before any PV reads them
-                uint8_t* v0 = gbase + OFF_V + (j % SV) * BLK_BYTES;
-                for (int i = lane; i < (BN - ragged_valid) * 16; i += 32) {
-                    const int r = ragged_valid + i / 16, q = i % 16;
-                    *reinterpret_cast<uint4*>(v0 + (q >= 8 ? BOX_BYTES : 0) + r * 128 + (q & 7) * 16) =
-                        make_uint4(0, 0, 0, 0);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_P + (j & 1)), (j >> 1) & 1, wait_ns) && !aborted(abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            if (lane == 0) {
+                return ready;
+            };
+            // O += P(j) V(j), then the release of V(j)
+            auto group_PV = [&](int j, Pre nxt) -> bool {
+                bool ready = false;
                 const uint32_t p = tmem + TM_S + (j & 1) * 128;  // P as packed bf16 pairs
                 const uint64_t vd = v_desc + (((j % SV) * BLK_BYTES) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
+                for (int kk = 0; kk < BN / 16; ++kk) {
+                    if (kk == BN / 16 - 2) ready = test_pre(nxt);
                     mma_bf16_ts(tmem + TM_O, p + kk * 8, vd + ((kk * 2048) >> 4), idO, j > 0 || kk > 0);
+                }
                 mma_commit(bar(BAR_VE + j % SV));
+                return ready;
+            };
+            bool ok = mbar_wait(bar(BAR_Q), 0, wait_ns) && (nb == 0 || mbar_wait(bar(BAR_KF), 0, wait_ns));
+            bool vf_ready = false;
+            if (ok && nb > 0) {
+                tc_fence_after();
+                if (nb > 1) {
+                    const bool k1_ready = group_S(0, kf_of(1));
+                    ok = wait_pre(kf_of(1), k1_ready);
+                    if (ok) {
+                        tc_fence_after();
+                        vf_ready = group_S(1, vf_of(0));
+                    }
+                } else {
+                    vf_ready = group_S(0, vf_of(0));
+                }
             }
-            __syncwarp();
-            if (j + 2 < nb) ok = issue_S(j + 2);
+            // (the softmax warps zero a ragged block's V rows past the chunk end before they signal
+            // P of that block, so its PV, issued after that signal, reads zeros there)
+            for (int j = 0; j < nb && ok; ++j) {
+                ok = wait_pre(vf_of(j), vf_ready) && mbar_wait(bar(BAR_P + (j & 1)), (j >> 1) & 1, wait_ns) &&
+                     !aborted(abort_flag);
+                if (!ok) break;
+                tc_fence_after();
+                if (j + 2 < nb) {
+                    const bool kf_ready = group_PV(j, kf_of(j + 2));
+                    ok = wait_pre(kf_of(j + 2), kf_ready);
+                    if (!ok) break;
+                    tc_fence_after();
+                    vf_ready = group_S(j + 2, vf_of(j + 1));
+                } else {
+                    vf_ready = group_PV(j, vf_of(j + 1));
+                }
+            }
+            if (!ok && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
+            mma_commit(bar(BAR_DONE));
         }
-        if (!ok && lane == 0 && !aborted(abort_flag)) raise_abort(abort_flag, a.status);
-        if (lane == 0) mma_commit(bar(BAR_DONE));
         __syncwarp();
     } else if (warp >= 4) {
         // ------------------------------------------------------------ softmax, epilogue
@@ -330,6 +362,19 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                                              !aborted(abort_flag));
             if (!ok) break;
             tc_fence_after();
+            if (j == ragged_block) {
+                // zero the V rows past the chunk end (both 64-dim boxes) before PV reads them: the
+                // block's keys there are masked, but the cache rows may hold non-finite garbage
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_VF + j % SV), (j / SV) & 1, wait_ns));
+                if (!ok) break;
+                uint8_t* v0 = gbase + OFF_V + (j % SV) * BLK_BYTES;
+                for (int x = r; x < (BN - ragged_valid) * 16; x += 128) {
+                    const int rr = ragged_valid + x / 16, c16 = x % 16;
+                    *reinterpret_cast<uint4*>(v0 + (c16 >= 8 ? BOX_BYTES : 0) + rr * 128 + (c16 & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+                fence_proxy_async_smem();
+            }
             const uint32_t sbuf = tmem + lane_base + TM_S + (j & 1) * 128;
             float s[BN];
 #pragma unroll
