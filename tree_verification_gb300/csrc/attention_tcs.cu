@@ -236,6 +236,74 @@ __device__ __forceinline__ int cut_slot(bool first_piece, int q) { return first_
 
 // kTestWaits: pipeline waits bounded by a.wait_ns (the failure-path tests); otherwise by kWaitNs, a
 // compile-time constant, so the production instantiation carries no run-time bound.
+// The last arriving piece of a cut item merges every piece's normalised fp32 partial into the bf16
+// output row of thread r (one row per thread, tile t): weights 2^(lse_i - max), loads issued in batches
+// before they are used (every piece's log2-sum-exp, then two pieces' 16 columns at a time).  Out of
+// line: it runs once per cut item, and keeping it out of the kernel body keeps the hot loops' code
+// compact (a larger kernel body measured slower per key block).
+__device__ __noinline__ void merge_cut_pieces(const float* __restrict__ cut_lse, const float* __restrict__ cut_o,
+                                              __nv_bfloat16* orow, int q_first, int np, int nrb2, int rb, int t,
+                                              int r) {
+    // slot-tile index of piece i (its log2-sum-exp row is (index) * 128 + r)
+    auto row_of = [&](int i) -> size_t {
+        const int qq = q_first + i;
+        return (size_t)cut_slot(qq == q_first, qq * nrb2 + rb) * 2 + t;
+    };
+    float mx = -INFINITY;
+    for (int i0 = 0; i0 < np; i0 += 4) {
+        float l4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) l4[u] = i0 + u < np ? __ldcg(cut_lse + row_of(i0 + u) * 128 + r) : -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) mx = fmaxf(mx, l4[u]);
+    }
+    float wsum = 0.f;
+    for (int i0 = 0; i0 < np; i0 += 4) {
+        float l4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) l4[u] = i0 + u < np ? __ldcg(cut_lse + row_of(i0 + u) * 128 + r) : -INFINITY;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) wsum += i0 + u < np ? ex2(l4[u] - mx) : 0.f;
+    }
+    const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
+    for (int c0 = 0; c0 < HD; c0 += 16) {
+        float4 acc[4];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) acc[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i0 = 0; i0 < np; i0 += 2) {
+            float4 v[2][4];
+            float wq[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const bool live = i0 + u < np;
+                const size_t st = live ? row_of(i0 + u) : 0;
+                wq[u] = live ? ex2(__ldcg(cut_lse + st * 128 + r) - mx) : 0.f;
+                const float4* src = reinterpret_cast<const float4*>(cut_o) + (st * (HD / 4) + c0 / 4) * 128 + r;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) v[u][x] = live ? __ldcg(src + x * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    acc[x].x += wq[u] * v[u][x].x;
+                    acc[x].y += wq[u] * v[u][x].y;
+                    acc[x].z += wq[u] * v[u][x].z;
+                    acc[x].w += wq[u] * v[u][x].w;
+                }
+        }
+        uint32_t wd[8];
+#pragma unroll
+        for (int y = 0; y < 4; ++y) {
+            __nv_bfloat162 lo = __floats2bfloat162_rn(acc[y].x * winv, acc[y].y * winv);
+            __nv_bfloat162 hi = __floats2bfloat162_rn(acc[y].z * winv, acc[y].w * winv);
+            wd[2 * y] = *reinterpret_cast<uint32_t*>(&lo);
+            wd[2 * y + 1] = *reinterpret_cast<uint32_t*>(&hi);
+        }
+        st_global_v8(orow + c0, wd);
+    }
+}
+
 template <bool kTestWaits>
 __global__ void __launch_bounds__(NTHREADS, 1)
 attn_tcs_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
@@ -731,69 +799,7 @@ attn_tcs_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                     // counter at zero.  Loads are issued in batches before they are used (one round trip
                     // per batch): every piece's log2-sum-exp, then two pieces' 32 columns at a time.
                     if (r == 0) *cnt = 0;
-                    if (row_ok) {
-                        const int np = q_last - q_first + 1;
-                        // slot-tile index of piece i (its log2-sum-exp row is (index) * 128 + r)
-                        auto row_of = [&](int i) -> size_t {
-                            const int qq = q_first + i;
-                            return (size_t)cut_slot(qq == q_first, qq * nrb2 + it.rb) * 2 + t;
-                        };
-                        float mx = -INFINITY;
-                        for (int i0 = 0; i0 < np; i0 += 4) {
-                            float l4[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) l4[u] = i0 + u < np ? __ldcg(a.cut_lse + row_of(i0 + u) * 128 + r) : -INFINITY;
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) mx = fmaxf(mx, l4[u]);
-                        }
-                        float wsum = 0.f;
-                        for (int i0 = 0; i0 < np; i0 += 4) {
-                            float l4[4];
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) l4[u] = i0 + u < np ? __ldcg(a.cut_lse + row_of(i0 + u) * 128 + r) : -INFINITY;
-#pragma unroll
-                            for (int u = 0; u < 4; ++u) wsum += i0 + u < np ? ex2(l4[u] - mx) : 0.f;
-                        }
-                        const float winv = wsum > 0.f ? 1.f / wsum : 0.f;
-                        for (int c0 = 0; c0 < HD; c0 += 16) {
-                            float4 acc[4];
-#pragma unroll
-                            for (int x = 0; x < 4; ++x) acc[x] = make_float4(0.f, 0.f, 0.f, 0.f);
-                            for (int i0 = 0; i0 < np; i0 += 2) {
-                                float4 v[2][4];
-                                float wq[2];
-#pragma unroll
-                                for (int u = 0; u < 2; ++u) {
-                                    const bool live = i0 + u < np;
-                                    const size_t st = live ? row_of(i0 + u) : 0;
-                                    wq[u] = live ? ex2(__ldcg(a.cut_lse + st * 128 + r) - mx) : 0.f;
-                                    const float4* src = reinterpret_cast<const float4*>(a.cut_o) +
-                                                        (st * (HD / 4) + c0 / 4) * 128 + r;
-#pragma unroll
-                                    for (int x = 0; x < 4; ++x)
-                                        v[u][x] = live ? __ldcg(src + x * 128) : make_float4(0.f, 0.f, 0.f, 0.f);
-                                }
-#pragma unroll
-                                for (int u = 0; u < 2; ++u)
-#pragma unroll
-                                    for (int x = 0; x < 4; ++x) {
-                                        acc[x].x += wq[u] * v[u][x].x;
-                                        acc[x].y += wq[u] * v[u][x].y;
-                                        acc[x].z += wq[u] * v[u][x].z;
-                                        acc[x].w += wq[u] * v[u][x].w;
-                                    }
-                            }
-                            uint32_t wd[8];
-#pragma unroll
-                            for (int y = 0; y < 4; ++y) {
-                                __nv_bfloat162 lo = __floats2bfloat162_rn(acc[y].x * winv, acc[y].y * winv);
-                                __nv_bfloat162 hi = __floats2bfloat162_rn(acc[y].z * winv, acc[y].w * winv);
-                                wd[2 * y] = *reinterpret_cast<uint32_t*>(&lo);
-                                wd[2 * y + 1] = *reinterpret_cast<uint32_t*>(&hi);
-                            }
-                            st_global_v8(orow + c0, wd);
-                        }
-                    }
+                    if (row_ok) merge_cut_pieces(a.cut_lse, a.cut_o, orow, q_first, q_last - q_first + 1, nrb2, it.rb, t, r);
                 }
             }
             g0 += it.je - it.jb;
