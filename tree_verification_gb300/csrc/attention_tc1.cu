@@ -433,7 +433,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                     const float2 x = __ffma2_rn(make_float2(s[hh * 64 + i], s[hh * 64 + i + 1]), sc2, nm2);
                     __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2(x.x), ex2(x.y));
                     // the row sum adds the same rounded weights the PV product uses
-                    acc = __fadd2_rn(acc, make_float2(__low2float(h2), __high2float(h2)));
+                    acc = add_bf16x2_f32(acc, *reinterpret_cast<uint32_t*>(&h2));
                     packed[i / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&h2));
                 }
                 tmem_st32(sbuf + hh * 32, packed);  // P over the first 64 columns of its S buffer

@@ -689,7 +689,7 @@ attn_tcs_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                         const float2 v = __ffma2_rn(make_float2(s[hh * 32 + x], s[hh * 32 + x + 1]), sc2, nm2);
                         __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2(v.x), ex2(v.y));
                         // the row sum adds the same rounded weights the PV product uses
-                        acc = __fadd2_rn(acc, make_float2(__low2float(h2), __high2float(h2)));
+                        acc = add_bf16x2_f32(acc, *reinterpret_cast<uint32_t*>(&h2));
                         packed[x / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&h2));
                     }
                     tmem_st16(sbuf + hh * 16, packed);  // P over the first 64 columns of S_t

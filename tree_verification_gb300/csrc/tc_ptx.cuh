@@ -107,6 +107,18 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, uint
         : "memory");
 }
 
+// ---------------------------------------------------------------- softmax arithmetic
+// acc.x + the low bf16 of a packed pair, acc.y + the high one: each half widened to fp32
+// exactly and added with one round-to-nearest, as unpacking the halves and adding them would,
+// but in one mixed-precision add per half (sm_100 family).
+__device__ __forceinline__ float2 add_bf16x2_f32(float2 acc, uint32_t pair) {
+    float x = acc.x, y = acc.y;
+    const unsigned short lo = (unsigned short)(pair & 0xffffu), hi = (unsigned short)(pair >> 16);
+    asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(x) : "h"(lo));
+    asm("add.rn.f32.bf16 %0, %1, %0;" : "+f"(y) : "h"(hi));
+    return make_float2(x, y);
+}
+
 // ---------------------------------------------------------------- TMEM
 // Allocation and release are warp-wide (.sync.aligned): call from a whole warp.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
