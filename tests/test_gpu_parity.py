@@ -360,6 +360,47 @@ def test_attention_parity_stream_schedule(ctas, split, B, Hq, Hkv, Kmax, Ls, Lca
         assert_attention_close(to_np(O), ref)
 
 
+@pytest.mark.parametrize("pattern", ["ramp", "jump", "fall"])
+@pytest.mark.parametrize("Hq,Hkv,tuning", [
+    (32, 8, dict(tiles=1, persist_ctas=-1, min_chunk=1000000)),     # one-tile kernel, one chunk per request
+    (32, 8, dict(tiles=2, persist_ctas=-1, min_chunk=1000000)),     # two-tile kernel
+    (32, 8, dict(tiles=2, persist_ctas=3, min_chunk=1000000)),      # persistent kernel, items back to back
+    (32, 8, dict(tiles=2, persist_ctas=40, min_chunk=1000000, split=1)),  # stream schedule, cut items
+    (32, 8, None),                                                  # the default plan (split-key chunks)
+    (12, 4, None),                                                  # group 3: the mma.sync path
+])
+def test_attention_parity_shifting_scores(pattern, Hq, Hkv, tuning):
+    """Scores that shift block to block by far more than a random cache gives: every query has 8 in
+    dimension 0 and a cached key at position p of a request of L keys has 16 p / L there (ramp), 0 then
+    16 from L / 2 on (jump), or 16 then 0 (fall), moving a block's scores by up to 16 log2 units.  The
+    running maximum is raised mid-chunk and O rescaled (ramp, jump), or later blocks weigh next to
+    nothing (fall); the rows' softmax within a block stays spread."""
+    B, Kmax, Ls, Lcap = 2, 64, [3000, 1100], 3072
+    Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed=17 + Hq + len(pattern))
+    Q[..., 0] = 8.0
+    for b, Lb in enumerate(Ls):
+        pos = torch.arange(Lb, dtype=torch.float32, device=DEV)
+        if pattern == "ramp":
+            k0 = 16.0 * pos / Lb
+        elif pattern == "jump":
+            k0 = torch.where(pos >= Lb // 2, 16.0, 0.0)
+        else:
+            k0 = torch.where(pos < Lb // 2, 16.0, 0.0)
+        Kc[b, :Lb, :, 0] = k0[:, None].to(torch.bfloat16)
+    status = _status()
+    kw = {} if tuning is None else dict(tuning=tuning)
+    if tuning is not None and tuning.get("split") == 1:
+        kw["ws"] = torch.zeros(gb().graft_tree_attention_workspace_size(B, Hq, Hkv, Kmax, Lcap, tuning),
+                               dtype=torch.uint8, device=DEV)
+    O = gb().graft_tree_attention(Q, Kc, Vc, Kt, Vt, L.to(DEV), torch.from_numpy(masks.view(np.int64)).to(DEV),
+                                  1 / math.sqrt(128), status=status, **kw)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    ref = oatt.tree_attention(to_np(Q), to_np(Kc), to_np(Vc), to_np(Kt), to_np(Vt), L.numpy(), masks,
+                              1 / math.sqrt(128))
+    assert_attention_close(to_np(O), ref)
+
+
 def test_attention_stream_schedule_flags_an_unzeroed_workspace():
     """Arrival counters that do not start at zero are reported (GRAFT_STATUS_WORKSPACE)."""
     B, Hq, Hkv, Kmax, Ls, Lcap = 2, 32, 8, 64, [4096, 777], 4160
