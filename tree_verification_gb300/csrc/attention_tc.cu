@@ -147,7 +147,8 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
     int b = blockIdx.z;  // remapped below to the request this CTA serves
     const int ntile = (2 * rb + 1 < a.nRB) ? 2 : 1;  // the last pair of an odd tile count has one
 
-    // Prologue that touches no global memory: it overlaps the previous kernel's tail.
+    // Prologue: it overlaps the previous kernel's tail, so it reads nothing it relies on from global
+    // memory (the L2 warm-up below only takes a hint from it).
     if (tid == 0) {
         for (int i = 0; i < N_BARS; ++i) {
             uint32_t cnt = 1;
@@ -164,6 +165,25 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         tma_prefetch_desc(&maps.q);
         tma_prefetch_desc(&maps.kc);
         tma_prefetch_desc(&maps.kt);
+        if (a.B == 1) {
+            // L2 warm-up while the previous kernel finishes: this CTA's Q tiles and first K and V
+            // block, placed by the request's length as it reads now.  A prefetch hands no data to the
+            // CTA, and L2 is where every write lands, so a length or cache the previous kernel is still
+            // writing costs at most a wasted prefetch; the loads proper follow the wait.  (Warming
+            // three blocks per CTA measured slower: more DRAM traffic than the previous kernel's tail
+            // hides.)
+            const int Lh = a.L[0];
+            const int k0 = c * chunk_len(a, Lh > 0 && Lh <= a.Lcap ? Lh : 0);
+            if (Lh > 0 && Lh <= a.Lcap && k0 < Lh) {
+                for (int t = 0; t < ntile; ++t)
+                    for (int h = 0; h < 2; ++h)
+                        tma_prefetch_l2_3d(&maps.q, h * 64, kvh * a.G, (rb * 256 + t * 128) / a.G);
+                for (int h = 0; h < 2; ++h) {
+                    tma_prefetch_l2_4d(&maps.kc, h * 64, kvh, k0, 0);
+                    tma_prefetch_l2_4d(&maps.vc, h * 64, kvh, k0, 0);
+                }
+            }
+        }
     }
     if (warp == 1) {
         __syncwarp();
