@@ -312,11 +312,13 @@ attn_partial_kernel(AttnArgs a) {
 // kept as a running maximum.  The attention kernels mark chunks past a
 // request's keys with lse = -inf and rows already written directly with
 // lse_0 = +inf, so the merge needs no request length.  One warp per output
-// row, four dims per lane; the loads of up to 16 chunks are issued together,
-// so a row costs one memory round trip per 16 chunks.
-constexpr int kMergeBatch = 16;
-
-__global__ void __launch_bounds__(256)
+// row, four dims per lane; the loads of up to kMergeBatch chunks are issued
+// together, so a row costs one memory round trip per kMergeBatch chunks: 16,
+// or 20 when a call has more chunks (the 19 of a 65536-token prefix over 152
+// SMs then take one round trip, where the unused slots of a wider batch would
+// cost the calls with few chunks more than they save).
+template <int kMergeBatch>
+__global__ void __launch_bounds__(256, 2)
 attn_combine_kernel(AttnArgs a) {
     griddep_enter();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -384,7 +386,11 @@ attn_combine_kernel(AttnArgs a) {
 int attn_combine_launch(const AttnArgs& a, cudaStream_t st) {
     if (a.nchunk <= 1) return GRAFT_OK;
     const long long rows = (long long)a.B * a.Hkv * a.nRB * 128;
-    launch_pdl(attn_combine_kernel, dim3((unsigned)((rows + 7) / 8)), dim3(256), 0, st, a);
+    const dim3 grid((unsigned)((rows + 7) / 8));
+    if (a.nchunk > 16)
+        launch_pdl(attn_combine_kernel<20>, grid, dim3(256), 0, st, a);
+    else
+        launch_pdl(attn_combine_kernel<16>, grid, dim3(256), 0, st, a);
     count_launches(1);
     return launch_status();
 }

@@ -93,7 +93,8 @@ constexpr int BAR_S = BAR_VE + SV;    // [tile] S_t ready in TMEM
 constexpr int BAR_P = BAR_S + 2;      // [tile] P_t written to TMEM (128 arrivals)
 constexpr int BAR_DONE = BAR_P + 2;   // every MMA completed (one-shot)
 constexpr int BAR_EPI = BAR_DONE + 1; // [tile] staging written (128 arrivals, one-shot)
-constexpr int N_BARS = BAR_EPI + 2;
+constexpr int BAR_ODONE = BAR_EPI + 2; // O_0 complete: tile 0's last PV ran (one-shot)
+constexpr int N_BARS = BAR_ODONE + 1;
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;  // tmem slot, abort flag
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -376,6 +377,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                         p1_ready = group_S(0, j + 1, p1);
                     } else {
                         p1_ready = group_PV(0, j, p1);
+                        mma_commit(bar(BAR_ODONE));  // tile 0's epilogue may start
                     }
                     ok = wait_pre(p1, p1_ready);
                     if (!ok) break;
@@ -390,6 +392,7 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                     vf_ready = group_S(0, j + 1, vn);
                 } else {
                     group_PV(0, j, none);
+                    mma_commit(bar(BAR_ODONE));
                 }
                 vf = vn;
             }
@@ -511,8 +514,10 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
         // ------------------------------------------------------------ epilogue
         if (t < ntile) {
             if (ok && nb > 0) {
-                // every MMA, the last PV included, has completed (one-shot barrier: no phase ambiguity)
-                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_DONE), 0, wait_ns));
+                // the tile's last PV has completed (one-shot barriers: no phase ambiguity); tile 0 needs
+                // only its own (every S product, the K ring's last reader, ran before it), tile 1 every
+                // product (its rows are staged over the V ring)
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(t == 0 ? BAR_ODONE : BAR_DONE), 0, wait_ns));
                 if (!ok) raise_abort(abort_flag, a.status);
             }
             const bool direct = (nck == 1);
