@@ -694,6 +694,17 @@ class WorkloadBench:
         for _ in range(steps):
             one()
         t = time.perf_counter() - t0
+        # the same host-to-device copies alone, back to back on the copy stream: the host link's rate on
+        # this machine, which bounds how much of them the step can hide
+        torch.cuda.synchronize()
+        n_copy = 3
+        c0 = time.perf_counter()
+        for _ in range(n_copy):
+            with torch.cuda.stream(copy_stream):
+                for k, (s0, s1) in self.segs.items():
+                    arena[s0:s1].copy_(host_arena[s0:s1], non_blocking=True)
+            copy_stream.synchronize()
+        self.h2d_copy_s = (time.perf_counter() - c0) / n_copy
         del g, host_arena
         return t, h2d, d2h
 
@@ -746,6 +757,10 @@ def workload_report(wb, parts, clocks, sms, t_e2e, n_e2e, h2d, d2h, per_ms=None)
     rep["retrieval_fill_us"] = parts["retrieval"] * 1e6
     if n_e2e > 0 and t_e2e == t_e2e:
         rep["e2e"] = {"value": n_e2e / t_e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        copy_s = getattr(wb, "h2d_copy_s", None)
+        if copy_s:
+            rep["e2e"]["h2d_copies_alone_ms"] = copy_s * 1e3
+            rep["e2e"]["h2d_gbs"] = h2d / copy_s / 1e9
     rep["launches_per_step"] = wb.launches_per_step
     rep["device_status"] = wb.status()
     rep["config"] = workload_config(wl)
