@@ -573,6 +573,29 @@ def test_update_M_parity(V, W, n, fill, seed):
         assert np.array_equal(to_np(s_d), want_s) and np.array_equal(to_np(c_d), want_c)
 
 
+@pytest.mark.parametrize("W,hot_pairs,hot_span", [(16, 6000, 2000), (32, 3000, 40000), (1, 2500, 300)])
+def test_update_M_hot_row_parity(W, hot_pairs, hot_span):
+    """One source token in thousands of pairs (as a token repeated over most of a batch's tree nodes): its
+    row has far more new successors than a list walk should take one by one, with repeated successors
+    (multiplicities, ties on count), on top of scattered background pairs."""
+    V, n_bg = 151936, 2000
+    rng = np.random.default_rng(W + hot_pairs)
+    succ, cnt, _, _ = _update_case(V, W, 0, W, fill=min(W, 4))
+    hot = 4242
+    src = np.concatenate([np.full(hot_pairs, hot, np.int32), rng.integers(0, V, n_bg).astype(np.int32)])
+    dst = np.concatenate([rng.integers(0, hot_span, hot_pairs), rng.integers(0, V, n_bg)]).astype(np.int32)
+    want_s, want_c = oupd.update_M(succ, cnt, src, dst)
+    for perm_seed in (None, 11):
+        s_d, c_d = torch.from_numpy(succ).to(DEV), torch.from_numpy(cnt).to(DEV)
+        order = np.arange(len(src)) if perm_seed is None else np.random.default_rng(perm_seed).permutation(len(src))
+        status = _status()
+        gb().graft_update_M(s_d, c_d, torch.from_numpy(src[order]).to(DEV), torch.from_numpy(dst[order]).to(DEV),
+                            status=status)
+        torch.cuda.synchronize()
+        assert int(status.item()) == 0
+        assert np.array_equal(to_np(s_d), want_s) and np.array_equal(to_np(c_d), want_c)
+
+
 def test_update_M_out_of_range_pairs_are_skipped():
     succ, cnt, src, dst = _update_case(40, 4, 100, 5, 2)
     src[3] = 40

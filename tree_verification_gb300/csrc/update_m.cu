@@ -14,8 +14,14 @@
 //                  present successor, or counts the new (src, dst) key and
 //                  links it into its row's list
 //   rerank_kernel  one warp per touched row: bitonic-sorts the W slots by
-//                  the packed key, then inserts every new successor with a
-//                  warp ballot; the result depends only on the multiset
+//                  the packed key, then inserts the new successors with a
+//                  warp ballot, walking the row's list of them when it is
+//                  short, else scanning the pair table 256 slots at a time
+//                  (independent loads) and inserting only the candidates
+//                  that beat the row's current last entry, so a token
+//                  repeated across thousands of tree nodes does not turn
+//                  into thousands of dependent loads; the result depends
+//                  only on the multiset
 #include <mutex>
 
 #include "common.cuh"
@@ -24,6 +30,7 @@ namespace graft {
 namespace {
 
 constexpr unsigned long long kEmptyPair = ~0ull;
+constexpr int kListWalk = 8;  // rows with more new successors scan the pair table instead of their list
 
 struct UpdWs {
     unsigned long long* pair_key;  // [cap] (src << 32) | dst, kEmptyPair = free
@@ -31,6 +38,7 @@ struct UpdWs {
     int32_t* pair_next;            // [cap] next new pair of the same row, -1 = end
     int32_t* row_key;              // [cap] src token, -1 = free
     int32_t* row_head;             // [cap] first new pair of the row, -1 = none
+    int32_t* row_ncand;            // [cap] new successors of the row
     int32_t* touched;              // [n] row-table slots in arrival order
     int32_t* n_touched;            // [1]
     int cap;                       // power of two >= 2n
@@ -61,6 +69,7 @@ __global__ void clear_kernel(UpdWs w) {
         w.pair_next[i] = -1;
         w.row_key[i] = -1;
         w.row_head[i] = -1;
+        w.row_ncand[i] = 0;
     }
     if (blockIdx.x == 0 && threadIdx.x == 0) *w.n_touched = 0;
 }
@@ -105,6 +114,7 @@ __global__ void pairs_kernel(int32_t* __restrict__ succ, int32_t* __restrict__ c
         const unsigned long long old = atomicCAS(&w.pair_key[q], kEmptyPair, key);
         if (old == kEmptyPair) {
             w.pair_next[q] = atomicExch(&w.row_head[row_slot], (int)q);
+            atomicAdd(&w.row_ncand[row_slot], 1);
             atomicAdd(&w.pair_mult[q], 1);
             return;
         }
@@ -147,16 +157,45 @@ __global__ void rerank_kernel(int32_t* __restrict__ succ, int32_t* __restrict__ 
             key = (lower == up) ? lo : hi;
         }
     }
-    // insert each new successor of the row; order of insertion does not matter
-    for (int p = w.row_head[slot]; p >= 0; p = w.pair_next[p]) {
-        const int t = (int)(uint32_t)(w.pair_key[p] & 0xffffffffull);
-        const unsigned long long ck = pack_slot(w.pair_mult[p], t);
+    // insert the row's new successors (order of insertion does not matter): a candidate enters at the
+    // number of entries ranked ahead of it, if that is below W, shifting the rest down one
+    auto insert = [&](unsigned long long ck) {
         const unsigned ahead = __ballot_sync(0xffffffffu, key < ck);
         const int pos = __popc(ahead);  // entries that stay in front (a prefix, the list is sorted)
         if (pos < W) {
             const unsigned long long prev = __shfl_up_sync(0xffffffffu, key, 1);
             if (lane > pos) key = prev;
             else if (lane == pos) key = ck;
+        }
+    };
+    if (w.row_ncand[slot] <= kListWalk) {
+        for (int p = w.row_head[slot]; p >= 0; p = w.pair_next[p])
+            insert(pack_slot(w.pair_mult[p], (int)(uint32_t)(w.pair_key[p] & 0xffffffffull)));
+    } else {
+        // many new successors: every pair-table slot is read once, eight independent loads per lane per
+        // pass, and a candidate is inserted only if it ranks ahead of the row's current W-th entry
+        const unsigned long long row_src = (unsigned long long)(uint32_t)s;
+        for (int base = 0; base < w.cap; base += 8 * 32) {
+            unsigned long long kk[8];
+            int mm[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int q = base + u * 32 + lane;
+                kk[u] = q < w.cap ? w.pair_key[q] : kEmptyPair;
+                mm[u] = q < w.cap ? w.pair_mult[q] : 0;
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const bool mine = kk[u] != kEmptyPair && (kk[u] >> 32) == row_src;
+                const unsigned long long ck = mine ? pack_slot(mm[u], (int)(uint32_t)(kk[u] & 0xffffffffull)) : ~0ull;
+                const unsigned long long last = __shfl_sync(0xffffffffu, key, W - 1);
+                unsigned want = __ballot_sync(0xffffffffu, ck < last);
+                while (want) {
+                    const int from = __ffs(want) - 1;
+                    want &= want - 1;
+                    insert(__shfl_sync(0xffffffffu, ck, from));
+                }
+            }
         }
     }
     if (lane < W) {
@@ -202,6 +241,7 @@ UpdWs carve_update(WsCarver& c, int64_t n) {
     w.pair_next = c.take<int32_t>(w.cap);
     w.row_key = c.take<int32_t>(w.cap);
     w.row_head = c.take<int32_t>(w.cap);
+    w.row_ncand = c.take<int32_t>(w.cap);
     w.touched = c.take<int32_t>(n > 0 ? n : 1);
     w.n_touched = c.take<int32_t>(1);
     return w;
