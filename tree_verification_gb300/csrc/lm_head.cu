@@ -7,17 +7,20 @@
 // each tree node.  g[n] = argmax_v sum_k H[n][k] W[v][k], ties to the lower
 // token id.
 //
-// One CTA computes a 128-row x 256-token tile of logits over the whole
-// hidden dimension: TMA brings 64-wide k slices of H and W (128-byte
-// swizzled boxes) into a 4-stage ring, one lane issues tcgen05.mma (M=128,
-// N=256, K=16, bf16 in, fp32 accumulator in TMEM), and four epilogue warps
-// read the accumulator back one row per thread, keep the row's first maximum
-// over the tile's tokens and fold it into a per-row 64-bit key with
-// atomicMax.  The key orders by the logit's value first (its float bits
-// mapped to a monotone unsigned order) and then by the complemented token
-// id, so the combination is independent of the order tiles finish in and
-// ties go to the lower id.  Consecutive CTAs take the row tiles of one
-// token tile, so each W tile is read from HBM once while H stays in L2.
+// A persistent CTA per SM computes 128-row x 256-token tiles of logits, each
+// over the whole hidden dimension: TMA brings 64-wide k slices of H and W
+// (128-byte swizzled boxes) into a 4-stage ring that runs across tiles, one
+// lane issues tcgen05.mma (M=128, N=256, K=16, bf16 in, fp32 accumulator in
+// TMEM), and four epilogue warps read an accumulator back one row per thread,
+// keep the row's first maximum over the tile's tokens and fold it into a
+// per-row 64-bit key with atomicMax.  Two accumulators (2 x 256 TMEM
+// columns) alternate between tiles, so a tile's epilogue runs while the next
+// tile's products do.  The key orders by the logit's value first (its float
+// bits mapped to a monotone unsigned order) and then by the complemented
+// token id, so the combination is independent of the order tiles finish in
+// and ties go to the lower id.  Tiles are numbered row tile fastest and dealt
+// round-robin, so the CTAs working at one time cover whole token tiles: each
+// W tile is read from HBM once while H stays in L2.
 //
 // The sampling variant (graft_lm_head_sample) adds Gumbel noise keyed by
 // (request, position, token) to every logit / T before the maximum
@@ -47,10 +50,12 @@ constexpr uint32_t A_BYTES = BM * BK * 2;
 constexpr uint32_t B_BYTES = BN * BK * 2;
 constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t OFF_BAR = ST * STAGE_BYTES;
-constexpr int BAR_FULL = 0;          // [ST] stage landed
-constexpr int BAR_EMPTY = ST;        // [ST] stage consumed by its MMAs
-constexpr int BAR_DONE = 2 * ST;     // accumulator complete (one-shot)
-constexpr int N_BARS = 2 * ST + 1;
+constexpr int BAR_FULL = 0;              // [ST] stage landed
+constexpr int BAR_EMPTY = ST;            // [ST] stage consumed by its MMAs
+constexpr int BAR_ACC_FULL = 2 * ST;     // [2] an accumulator's tile complete (one phase per use)
+constexpr int BAR_ACC_EMPTY = 2 * ST + 2;  // [2] an accumulator read out (128 arrivals per use)
+constexpr int BAR_DONE = 2 * ST + 4;     // every MMA completed (one-shot, before TMEM is freed)
+constexpr int N_BARS = 2 * ST + 5;
 constexpr uint32_t OFF_MISC = OFF_BAR + N_BARS * 8;  // tmem slot, abort flag
 constexpr uint32_t SMEM_BYTES = OFF_MISC + 64 + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
@@ -110,12 +115,14 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
     volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(gbase + OFF_MISC + 4);
     auto bar = [&](int i) { return base + OFF_BAR + 8u * (uint32_t)i; };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int row0 = blockIdx.x * BM;
-    const int v0 = blockIdx.y * BN;
     const int nk = (d + BK - 1) / BK;
+    const int nrt = (N + BM - 1) / BM;                        // row tiles
+    const long long ntiles = (long long)nrt * ((V + BN - 1) / BN);
+    // tile t: row tile t % nrt, token tile t / nrt; this CTA takes t = blockIdx.x + i gridDim.x
 
     if (tid == 0) {
-        for (int i = 0; i < N_BARS; ++i) mbar_init(bar(i), 1);
+        for (int i = 0; i < N_BARS; ++i)
+            mbar_init(bar(i), (i == BAR_ACC_EMPTY || i == BAR_ACC_EMPTY + 1) ? 128 : 1);
         *abort_flag = 0;
         fence_mbar_init();
     } else if (tid == 32) {
@@ -124,7 +131,7 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
     }
     if (warp == 1) {
         __syncwarp();
-        tmem_alloc(base + OFF_MISC, 256);
+        tmem_alloc(base + OFF_MISC, 512);
         tmem_relinquish();
         tc_fence_before();
     }
@@ -138,18 +145,27 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
     if (warp == 0) {
         // ------------------------------------------------------------ TMA producer (lane 0)
         if (lane == 0) {
-            for (int kt = 0; kt < nk; ++kt) {
-                const int s = kt % ST;
-                if (kt >= ST && !mbar_wait(bar(BAR_EMPTY + s), ((kt / ST) - 1) & 1, kWaitNs)) {
-                    raise_abort(abort_flag, status);
-                    break;
+            int it = 0;  // k slices loaded so far, over every tile of this CTA
+            bool ok = true;
+            for (long long t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const int row0 = (int)(t % nrt) * BM, v0 = (int)(t / nrt) * BN;
+                for (int kt = 0; kt < nk; ++kt, ++it) {
+                    const int s = it % ST;
+                    if (it >= ST && !mbar_wait(bar(BAR_EMPTY + s), ((it / ST) - 1) & 1, kWaitNs)) {
+                        raise_abort(abort_flag, status);
+                        ok = false;
+                        break;
+                    }
+                    if (aborted(abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t a = base + s * STAGE_BYTES;
+                    mbar_expect_tx(bar(BAR_FULL + s), STAGE_BYTES);
+                    tma_load_2d(a, &maps.h, bar(BAR_FULL + s), kt * BK, row0);
+                    tma_load_2d(a + A_BYTES, &maps.w, bar(BAR_FULL + s), kt * BK, v0);
+                    ++issued;
                 }
-                if (aborted(abort_flag)) break;
-                const uint32_t a = base + s * STAGE_BYTES;
-                mbar_expect_tx(bar(BAR_FULL + s), STAGE_BYTES);
-                tma_load_2d(a, &maps.h, bar(BAR_FULL + s), kt * BK, row0);
-                tma_load_2d(a + A_BYTES, &maps.w, bar(BAR_FULL + s), kt * BK, v0);
-                ++issued;
             }
         }
         __syncwarp();
@@ -159,19 +175,36 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
         const uint64_t a_desc = sdesc_sw128(base, 16, 1024);
         const uint64_t b_desc = sdesc_sw128(base + A_BYTES, 16, 1024);
         bool ok = true;
-        for (int kt = 0; kt < nk && ok; ++kt) {
-            const int s = kt % ST;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_FULL + s), (kt / ST) & 1, kWaitNs) && !aborted(abort_flag));
-            if (!ok) break;
-            tc_fence_after();
-            if (lane == 0) {
-                const uint64_t so = (s * STAGE_BYTES) >> 4;
-#pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_bf16_ss(tmem, a_desc + so + ((kk * 32) >> 4), b_desc + so + ((kk * 32) >> 4), id,
-                                kt > 0 || kk > 0);
-                mma_commit(bar(BAR_EMPTY + s));
+        int it = 0;
+        int ti = 0;  // this CTA's tiles so far; tile ti accumulates into buffer ti & 1
+        for (long long t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++ti) {
+            const int acc = ti & 1;
+            if (ti >= 2) {
+                // the epilogue has read this buffer's previous tile out
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_ACC_EMPTY + acc), ((ti >> 1) - 1) & 1, kWaitNs) &&
+                                                 !aborted(abort_flag));
+                if (!ok) break;
+                tc_fence_after();
             }
+            const uint32_t d_acc = tmem + (uint32_t)acc * BN;
+            for (int kt = 0; kt < nk && ok; ++kt, ++it) {
+                const int s = it % ST;
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(bar(BAR_FULL + s), (it / ST) & 1, kWaitNs) && !aborted(abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+                if (lane == 0) {
+                    const uint64_t so = (s * STAGE_BYTES) >> 4;
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        mma_bf16_ss(d_acc, a_desc + so + ((kk * 32) >> 4), b_desc + so + ((kk * 32) >> 4), id,
+                                    kt > 0 || kk > 0);
+                    mma_commit(bar(BAR_EMPTY + s));
+                }
+                __syncwarp();
+            }
+            if (!ok) break;
+            if (lane == 0) mma_commit(bar(BAR_ACC_FULL + acc));  // the tile's products complete
             __syncwarp();
         }
         if (!ok && lane == 0 && !aborted(abort_flag)) raise_abort(abort_flag, status);
@@ -181,9 +214,17 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
         // ------------------------------------------------------------ epilogue: row argmax (warps 2-5)
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
-        const int n = row0 + r;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_DONE), 0, kWaitNs)) && !aborted(abort_flag);
-        if (ok) {
+        int ti = 0;
+        for (long long t = blockIdx.x; t < ntiles; t += gridDim.x, ++ti) {
+            const int acc = ti & 1;
+            const int row0 = (int)(t % nrt) * BM, v0 = (int)(t / nrt) * BN;
+            const int n = row0 + r;
+            const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_ACC_FULL + acc), (ti >> 1) & 1, kWaitNs)) &&
+                            !aborted(abort_flag);
+            if (!ok) {
+                if (!aborted(abort_flag)) raise_abort(abort_flag, status);
+                break;
+            }
             tc_fence_after();
             float best = -INFINITY;
             int bi = -1;
@@ -194,8 +235,13 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
             }
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 float x[32];
-                tmem_ld32(tmem + ((uint32_t)(quad * 32) << 16) + c0, x);
+                tmem_ld32(tmem + (uint32_t)acc * BN + ((uint32_t)(quad * 32) << 16) + c0, x);
                 tmem_wait_ld();
+                if (c0 == BN - 32) {
+                    // the accumulator is in registers: the tile after next may overwrite it
+                    tc_fence_before();
+                    mbar_arrive(bar(BAR_ACC_EMPTY + acc));
+                }
                 if (SAMPLE) {
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
@@ -220,8 +266,6 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
                                                (unsigned long long)(0xffffffffu - (uint32_t)bi);
                 atomicMax(keys + n, key);
             }
-        } else if (!aborted(abort_flag)) {
-            raise_abort(abort_flag, status);
         }
     }
     // ---------------------------------------------------------------- teardown
@@ -235,7 +279,7 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem, 256);
+    if (warp == 1) tmem_dealloc(tmem, 512);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
@@ -310,7 +354,11 @@ int lm_head_impl(int N, int d_model, int V, const void* H, const void* W_lm, int
     }
     cudaStream_t st = (cudaStream_t)stream;
     const unsigned small = (unsigned)((N + 255) / 256 < 1024 ? (N + 255) / 256 : 1024);
-    const dim3 grid((unsigned)row_tiles, (unsigned)tok_tiles);
+    // persistent: one CTA per SM (shared memory allows no more), at most one per tile
+    const long long tiles = row_tiles * tok_tiles;
+    int sms = device_sm_count();
+    if (sms <= 0) sms = 148;
+    const dim3 grid((unsigned)(tiles < sms ? tiles : sms));
     launch_pdl(key_init_kernel, dim3(small), dim3(256), 0, st, keys, N);
     if (smp)
         launch_pdl(lm_head_argmax_kernel<true>, grid, dim3(NTHREADS), SMEM_BYTES, st, m, N, d_model, V, keys, status,
