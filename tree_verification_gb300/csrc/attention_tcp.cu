@@ -498,66 +498,77 @@ attn_tcp_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
                     }
                     fence_proxy_async_smem();
                 }
-                float s[BN];
-#pragma unroll
-                for (int x = 0; x < BN / 32; ++x) tmem_ld32(sbuf + x * 32, s + x * 32);
-                tmem_wait_ld();
                 const bool tree_blk = j >= nb_prefix;
-                if (tree_blk || j == ragged_block) {
-                    // only the ragged tail and the tree block need masking: keep-bits for the
-                    // block's keys as four 32-bit words (tree keys are < 64, in the ancestor mask)
-                    const int valid = tree_blk ? a.Kmax : ragged_valid;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const int n = valid - 32 * x;
-                        w[x] = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
-                    }
-                    if (tree_blk) {
-                        w[0] &= (uint32_t)anc;
-                        w[1] &= (uint32_t)(anc >> 32);
-                        w[2] = w[3] = 0u;
-                    }
-#pragma unroll
-                    for (int x = 0; x < BN; ++x) s[x] = ((w[x >> 5] >> (x & 31)) & 1u) ? s[x] : -INFINITY;
-                }
-                // block maximum by a tree of pairwise maxima (short dependency chains)
-                float m8[8];
-#pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                    float m = fmaxf(s[x], s[x + 8]);
-#pragma unroll
-                    for (int y = 16; y < BN; y += 16) m = fmaxf(m, fmaxf(s[x + y], s[x + y + 8]));
-                    m8[x] = m;
-                }
-                const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
-                                       fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;  // sl2 > 0
                 float alpha = 1.f;
                 bool rescale = false;
-                if (j == 0) {
-                    m_used = mx;
-                } else if (__any_sync(0xffffffffu, mx > m_used + RESCALE_LOG2)) {
-                    const float m_new = fmaxf(mx, m_used);
-                    alpha = (m_used == -INFINITY) ? 1.f : ex2(m_used - m_new);
-                    m_used = m_new;
-                    rescale = true;
-                }
-                const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
-                const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
-                float2 acc = make_float2(0.f, 0.f);
+                float2 acc;
+                float packed[BN / 2];
+                // An item's first block takes its maximum; a later block is first weighed against the
+                // running maximum alone and stands if its row sum stays within 2^16 (so no weight
+                // passed 2^16: none overflowed, and bf16 P, the fp32 sums and O carry them).  Otherwise
+                // it is weighed again with its own maximum; S_t is still intact in TMEM, since P is
+                // stored over it only once the block stands.
+                for (int pass = 0; pass < 2; ++pass) {
+                    float s[BN];
 #pragma unroll
-                for (int hh = 0; hh < 4; ++hh) {
-                    float packed[16];
+                    for (int x = 0; x < BN / 32; ++x) tmem_ld32(sbuf + x * 32, s + x * 32);
+                    tmem_wait_ld();
+                    if (tree_blk || j == ragged_block) {
+                        // only the ragged tail and the tree block need masking: keep-bits for the
+                        // block's keys as four 32-bit words (tree keys are < 64, in the ancestor mask)
+                        const int valid = tree_blk ? a.Kmax : ragged_valid;
+                        uint32_t w[4];
 #pragma unroll
-                    for (int x = 0; x < 32; x += 2) {
-                        const float2 v = __ffma2_rn(make_float2(s[hh * 32 + x], s[hh * 32 + x + 1]), sc2, nm2);
+                        for (int x = 0; x < 4; ++x) {
+                            const int n = valid - 32 * x;
+                            w[x] = n >= 32 ? 0xffffffffu : (n <= 0 ? 0u : ((1u << n) - 1u));
+                        }
+                        if (tree_blk) {
+                            w[0] &= (uint32_t)anc;
+                            w[1] &= (uint32_t)(anc >> 32);
+                            w[2] = w[3] = 0u;
+                        }
+#pragma unroll
+                        for (int x = 0; x < BN; ++x) s[x] = ((w[x >> 5] >> (x & 31)) & 1u) ? s[x] : -INFINITY;
+                    }
+                    const bool full = j == 0 || pass == 1;
+                    if (full) {
+                        // block maximum by a tree of pairwise maxima (short dependency chains)
+                        float m8[8];
+#pragma unroll
+                        for (int x = 0; x < 8; ++x) {
+                            float m = fmaxf(s[x], s[x + 8]);
+#pragma unroll
+                            for (int y = 16; y < BN; y += 16) m = fmaxf(m, fmaxf(s[x + y], s[x + y + 8]));
+                            m8[x] = m;
+                        }
+                        const float mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                               fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7]))) * sl2;  // sl2 > 0
+                        if (j == 0) {
+                            m_used = mx;
+                        } else if (__any_sync(0xffffffffu, mx > m_used + RESCALE_LOG2)) {
+                            const float m_new = fmaxf(mx, m_used);
+                            alpha = (m_used == -INFINITY) ? 1.f : ex2(m_used - m_new);
+                            m_used = m_new;
+                            rescale = true;
+                        }
+                    }
+                    const float neg_m = (m_used == -INFINITY) ? 0.f : -m_used;
+                    const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
+                    acc = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int x = 0; x < BN; x += 2) {
+                        const float2 v = __ffma2_rn(make_float2(s[x], s[x + 1]), sc2, nm2);
                         __nv_bfloat162 h2 = __floats2bfloat162_rn(ex2(v.x), ex2(v.y));
                         // the row sum adds the same rounded weights the PV product uses
                         acc = add_bf16x2_f32(acc, *reinterpret_cast<uint32_t*>(&h2));
                         packed[x / 2] = __uint_as_float(*reinterpret_cast<uint32_t*>(&h2));
                     }
-                    tmem_st16(sbuf + hh * 16, packed);  // P over the first 64 columns of S_t
+                    // (!(x <= bound) also sends a NaN sum to the second pass)
+                    if (full || !__any_sync(0xffffffffu, !(acc.x + acc.y <= 65536.f))) break;
                 }
+#pragma unroll
+                for (int hh = 0; hh < 4; ++hh) tmem_st16(sbuf + hh * 16, packed + hh * 16);  // P over S_t[0, 64)
                 if (rescale) {
                     // S_t(g) was issued after PV_t(g - 1) on the in-order tensor pipe, so its
                     // completion means O_t already holds every earlier block of the item
