@@ -155,8 +155,14 @@ __device__ __forceinline__ int ranked_request(const AttnArgs& a, int z) { return
 // A position in this CTA's walk: the next cost unit of the sequence.
 __device__ __forceinline__ int walk_start(const AttnArgs& a) { return min((int)blockIdx.x / (a.nRB / 2) * s_S, s_T); }
 
+// The arguments the walk reads, passed by value to its out-of-line search.
+struct WalkArgs {
+    int B, Hkv, nRB;
+    const int32_t* L;
+};
+
 // The next piece of this CTA's walk; false past the end of its group's range.
-__device__ __forceinline__ bool next_item(int& w, const AttnArgs& a, Item& it) {
+__device__ __forceinline__ bool next_item_search(int& w, const WalkArgs& a, Item& it) {
     const int nrb2 = a.nRB / 2;
     const int S = s_S;
     const int g_end = min(((int)blockIdx.x / nrb2 + 1) * S, s_T);
@@ -179,7 +185,7 @@ __device__ __forceinline__ bool next_item(int& w, const AttnArgs& a, Item& it) {
         w = g_end;
         return false;
     }
-    const int b = ranked_request(a, z);
+    const int b = a.B > 1 ? s_order[z] : z;  // requests ranked by length (the launch keeps B <= MAX_ORDER)
     const int Lb = a.L[b];  // in [0, Lcap]: requests outside it hold no blocks
     it.b = b;
     it.kvh = kvh;
@@ -194,6 +200,28 @@ __device__ __forceinline__ bool next_item(int& w, const AttnArgs& a, Item& it) {
     it.je = min(cz - ITEM_COST, g_end - b0);
     w = b0 + it.je;  // the item's end (its last cost unit + 1) when its last block is in the range
     return true;
+}
+
+struct NextItem {
+    Item it;
+    int w;
+    bool live;
+};
+
+// The search runs once per piece; kept out of line (and out of the block loops that call it), it
+// leaves those loops small in the instruction cache.
+__device__ __noinline__ NextItem next_item_ool(int w, WalkArgs wa) {
+    NextItem r;
+    r.w = w;
+    r.live = next_item_search(r.w, wa, r.it);
+    return r;
+}
+
+__device__ __forceinline__ bool next_item(int& w, const AttnArgs& a, Item& it) {
+    const NextItem r = next_item_ool(w, WalkArgs{a.B, a.Hkv, a.nRB, a.L});
+    w = r.w;
+    it = r.it;
+    return r.live;
 }
 
 // A position (item, block) in this CTA's stream of blocks, with the few item fields the TMA
