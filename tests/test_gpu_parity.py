@@ -360,7 +360,7 @@ def test_attention_parity_stream_schedule(ctas, split, B, Hq, Hkv, Kmax, Ls, Lca
         assert_attention_close(to_np(O), ref)
 
 
-@pytest.mark.parametrize("pattern", ["ramp", "jump", "fall"])
+@pytest.mark.parametrize("pattern", ["ramp", "jump", "fall", "cliff"])
 @pytest.mark.parametrize("Hq,Hkv,tuning", [
     (32, 8, dict(tiles=1, persist_ctas=-1, min_chunk=1000000)),     # one-tile kernel, one chunk per request
     (32, 8, dict(tiles=2, persist_ctas=-1, min_chunk=1000000)),     # two-tile kernel
@@ -372,9 +372,12 @@ def test_attention_parity_stream_schedule(ctas, split, B, Hq, Hkv, Kmax, Ls, Lca
 def test_attention_parity_shifting_scores(pattern, Hq, Hkv, tuning):
     """Scores that shift block to block by far more than a random cache gives: every query has 8 in
     dimension 0 and a cached key at position p of a request of L keys has 16 p / L there (ramp), 0 then
-    16 from L / 2 on (jump), or 16 then 0 (fall), moving a block's scores by up to 16 log2 units.  The
-    running maximum is raised mid-chunk and O rescaled (ramp, jump), or later blocks weigh next to
-    nothing (fall); the rows' softmax within a block stays spread."""
+    16 from L / 2 on (jump), or 16 then 0 (fall), moving a block's scores by up to 16 log2 units, or 0
+    then 128 (cliff: about 130 log2 units, past the float32 range of 2^x).  The running maximum is
+    raised mid-chunk and O rescaled (ramp, jump, cliff), or later blocks weigh next to nothing (fall);
+    the rows' softmax within a block stays spread.  A kernel that weighs a block against the running
+    maximum alone must weigh the jump and cliff blocks again with their own maximum (their weights
+    pass 2^16, at the cliff overflowing to infinity)."""
     B, Kmax, Ls, Lcap = 2, 64, [3000, 1100], 3072
     Q, Kc, Vc, Kt, Vt, L, masks = _attention_case(B, Hq, Hkv, Kmax, Ls, Lcap, seed=17 + Hq + len(pattern))
     Q[..., 0] = 8.0
@@ -384,6 +387,8 @@ def test_attention_parity_shifting_scores(pattern, Hq, Hkv, tuning):
             k0 = 16.0 * pos / Lb
         elif pattern == "jump":
             k0 = torch.where(pos >= Lb // 2, 16.0, 0.0)
+        elif pattern == "cliff":
+            k0 = torch.where(pos >= Lb // 2, 128.0, 0.0)
         else:
             k0 = torch.where(pos < Lb // 2, 16.0, 0.0)
         Kc[b, :Lb, :, 0] = k0[:, None].to(torch.bfloat16)
