@@ -214,11 +214,23 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
         // ------------------------------------------------------------ epilogue: row argmax (warps 2-5)
         const int quad = warp & 3;
         const int r = quad * 32 + lane;
+        // the largest Gumbel draw any 32-bit word gives (the draw grows with the word), with a margin
+        // for the rounding of its logarithms
+        const float g_top = SAMPLE ? gumbel_of(0xffffffffu) + 1e-3f : 0.f;
         int ti = 0;
         for (long long t = blockIdx.x; t < ntiles; t += gridDim.x, ++ti) {
             const int acc = ti & 1;
             const int row0 = (int)(t % nrt) * BM, v0 = (int)(t / nrt) * BN;
             const int n = row0 + r;
+            // (the sampler's row loads are issued before the wait for the accumulator, which hides them)
+            uint32_t nb = 0, npos = 0;
+            unsigned long long key_seen = 0ull;
+            if (SAMPLE && n < N) {
+                nb = (uint32_t)(n / sa.Kmax);
+                npos = (uint32_t)(sa.tree_pos[n] + 1);
+                // the row's key as other tiles have raised it so far (any value read is a real score)
+                key_seen = __ldcg(keys + n);
+            }
             const bool ok = __all_sync(0xffffffffu, mbar_wait(bar(BAR_ACC_FULL + acc), (ti >> 1) & 1, kWaitNs)) &&
                             !aborted(abort_flag);
             if (!ok) {
@@ -228,11 +240,11 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
             tc_fence_after();
             float best = -INFINITY;
             int bi = -1;
-            uint32_t nb = 0, npos = 0;
-            if (SAMPLE && n < N) {
-                nb = (uint32_t)(n / sa.Kmax);
-                npos = (uint32_t)(sa.tree_pos[n] + 1);
-            }
+            // a score another tile reached in this row, if any (sampling); until a row of the warp has
+            // one, the warp draws every token's noise without the tests below
+            const float reached = key_seen != 0ull ? unordered_bits((uint32_t)(key_seen >> 32)) : -INFINITY;
+            const bool prune = SAMPLE && __any_sync(0xffffffffu, key_seen != 0ull);
+
             for (int c0 = 0; c0 < BN; c0 += 32) {
                 float x[32];
                 tmem_ld32(tmem + (uint32_t)acc * BN + ((uint32_t)(quad * 32) << 16) + c0, x);
@@ -242,7 +254,7 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
                     tc_fence_before();
                     mbar_arrive(bar(BAR_ACC_EMPTY + acc));
                 }
-                if (SAMPLE) {
+                if (SAMPLE && !prune) {
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
                         const uint4 r4 = noise_draws(sa.seed, nb, npos, (uint32_t)((v0 + c0 + i) >> 2));
@@ -250,6 +262,27 @@ lm_head_argmax_kernel(const __grid_constant__ Maps maps, int N, int d, int V, un
                         x[i + 1] = x[i + 1] * sa.inv_T + gumbel_of(r4.y);
                         x[i + 2] = x[i + 2] * sa.inv_T + gumbel_of(r4.z);
                         x[i + 3] = x[i + 3] * sa.inv_T + gumbel_of(r4.w);
+                    }
+                } else if (SAMPLE) {
+                    // A token whose scaled logit plus the largest draw (g_top) stays below a score
+                    // already reached in its row cannot be the row's pick: four such tokens draw no
+                    // noise and score -inf.  The bound allows for the rounding of the sums (a relative
+                    // 2^-20).
+                    const float top = fmaxf(reached, best);
+                    const float lim = top - g_top - fabsf(top) * 9.5367431640625e-7f;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float s0 = x[i] * sa.inv_T, s1 = x[i + 1] * sa.inv_T;
+                        const float s2 = x[i + 2] * sa.inv_T, s3 = x[i + 3] * sa.inv_T;
+                        if (fmaxf(fmaxf(s0, s1), fmaxf(s2, s3)) >= lim) {
+                            const uint4 r4 = noise_draws(sa.seed, nb, npos, (uint32_t)((v0 + c0 + i) >> 2));
+                            x[i] = s0 + gumbel_of(r4.x);
+                            x[i + 1] = s1 + gumbel_of(r4.y);
+                            x[i + 2] = s2 + gumbel_of(r4.z);
+                            x[i + 3] = s3 + gumbel_of(r4.w);
+                        } else {
+                            x[i] = x[i + 1] = x[i + 2] = x[i + 3] = -INFINITY;
+                        }
                     }
                 }
 #pragma unroll
