@@ -903,6 +903,17 @@ def lm_head_timing(wl, dev, reps):
     nbytes = (H.numel() + W_lm.numel()) * 2 + N * 8
     res["tflops"] = flops / (res["argmax_us"] * 1e-6) / 1e12
     res["gbs"] = nbytes / (res["argmax_us"] * 1e-6) / 1e9
+    # sampling from given fp32 logits (the same products, materialised once by torch for the input)
+    logits = (H.float() @ W_lm.float().t()).view(wl.B, wl.Kmax, wl.V)
+    sampled = torch.empty(wl.B, wl.Kmax, dtype=torch.int32, device=dev)
+    sws = torch.empty(max(1, gb.graft_sample_tokens_workspace_size(wl.B, wl.Kmax, wl.V)), dtype=torch.uint8,
+                      device=dev)
+    g = _capture(lambda: gb.graft_sample_tokens(logits, pos, 1.0, 1234, sampled=sampled, ws=sws))
+    g.replay()
+    t = _timed(g, reps) / reps
+    res["sample_tokens_us"] = t * 1e6
+    res["sample_tokens_gbs"] = logits.numel() * 4 / t / 1e9  # the logits, read once
+    del g, logits
     del H, W_lm
     torch.cuda.empty_cache()
     return res

@@ -27,7 +27,8 @@ def _check(logits, pos, T, seed, got):
     return int(cert.sum())
 
 
-@pytest.mark.parametrize("V,T,seed", [(5000, 1.0, 7), (5000, 0.5, (1 << 40) + 3), (128256, 2.0, 11), (3, 1.0, 5)])
+@pytest.mark.parametrize("V,T,seed", [(5000, 1.0, 7), (5000, 0.5, (1 << 40) + 3), (128256, 2.0, 11), (3, 1.0, 5),
+                                        (4097, 0.05, 13), (128256, 0.1, 17)])  # (low T: most noise skipped)
 def test_sample_tokens_parity(V, T, seed):
     B, K = 3, 16
     rng = np.random.default_rng(seed & 0xFFFF)

@@ -10,8 +10,9 @@
 // G keyed by position (philox.cuh); graft_accept_compact with these samples
 // as its argmax input then applies the acceptance.
 //
-// Kernels: sample_part_kernel splits each row over CTAs (one Philox call per
-// four tokens, HBM bound on the logits) and keeps the best perturbed score
+// Kernels: sample_part_kernel splits each row over CTAs, reads its split's
+// logits once, draws noise (one Philox call per four tokens) only for groups
+// that can still hold the split's pick, and keeps the best perturbed score
 // with the lower id on ties; sample_reduce_kernel merges a row's splits (one
 // warp per row).
 #include <climits>
@@ -23,7 +24,7 @@ namespace graft {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kChunk = 16384;  // tokens per split (a multiple of 4)
+constexpr int kChunk = 8192;  // tokens per split (a multiple of 4 kThreads)
 
 struct SamplePart {
     float z;
@@ -33,6 +34,9 @@ struct SamplePart {
 __device__ __forceinline__ bool better(float a, int ia, float b, int ib) {
     return a > b || (a == b && ia < ib);
 }
+
+constexpr int kGroups = kChunk / (4 * kThreads);  // four-token groups per thread and split
+static_assert(kChunk % (4 * kThreads) == 0, "a split is whole four-token groups of every thread");
 
 __global__ void __launch_bounds__(kThreads)
 sample_part_kernel(const float* __restrict__ logits, int Kmax, int V, int S, float inv_T, unsigned long long seed,
@@ -44,17 +48,64 @@ sample_part_kernel(const float* __restrict__ logits, int Kmax, int V, int S, flo
     const uint32_t pos = (uint32_t)(tree_pos[row] + 1);  // the position of the token this node samples
     const float* r = logits + row * (size_t)V;
     const int lo = s * kChunk, hi = min(V, lo + kChunk);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // The split's scaled logits, read once (group g of this thread: tokens 4 q .. 4 q + 3 with
+    // q = lo / 4 + threadIdx.x + g kThreads; -inf past the row), and their maximum.
+    const bool vec = ((V & 3) == 0) && ((reinterpret_cast<uintptr_t>(logits) & 15) == 0);
+    float4 xs[kGroups];
+    if (vec && hi - lo == kChunk) {
+        // a whole aligned split: every load issued before any is used
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g)
+            xs[g] = __ldcs(reinterpret_cast<const float4*>(r + 4 * (lo / 4 + (int)threadIdx.x + g * kThreads)));
+    } else {
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) {
+            const int v = 4 * (lo / 4 + (int)threadIdx.x + g * kThreads);
+            xs[g].x = v < hi ? __ldcs(r + v) : -INFINITY;
+            xs[g].y = v + 1 < hi ? __ldcs(r + v + 1) : -INFINITY;
+            xs[g].z = v + 2 < hi ? __ldcs(r + v + 2) : -INFINITY;
+            xs[g].w = v + 3 < hi ? __ldcs(r + v + 3) : -INFINITY;
+        }
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < kGroups; ++g) {
+        const float4 x = make_float4(xs[g].x * inv_T, xs[g].y * inv_T, xs[g].z * inv_T, xs[g].w * inv_T);
+        xs[g] = x;
+        m = fmaxf(m, fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)));
+    }
+    __shared__ float sm[kThreads / 32];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == 0) sm[warp] = m;
+    __syncthreads();
+    m = sm[0];
+#pragma unroll
+    for (int w = 1; w < kThreads / 32; ++w) m = fmaxf(m, sm[w]);
+    // Every token's score is its scaled logit plus a draw of at least g_bot, so the split's best score
+    // is at least m + g_bot; a group whose scaled logits plus the largest draw (g_top) stay below that
+    // cannot hold the split's pick and draws no noise.  The margins allow for the rounding of the
+    // logarithms and of the sums; without a finite bound nothing is skipped.
+    const float g_top = gumbel_of(0xffffffffu) + 1e-3f, g_bot = gumbel_of(0u) - 1e-3f;
+    const float floor_score = m + g_bot;
+    const float lim = fabsf(floor_score) < INFINITY
+                          ? floor_score - g_top - fabsf(floor_score) * 9.5367431640625e-7f
+                          : -INFINITY;
     float bz = -INFINITY;
     int bi = INT_MAX;
-    for (int q = lo / 4 + threadIdx.x; 4 * q < hi; q += kThreads) {
-        const uint4 x = noise_draws(seed, b, pos, (uint32_t)q);
-        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int v = 4 * q + j;
-            if (v < hi) {
-                const float z = __ldcs(r + v) * inv_T + gumbel_of(xs[j]);
-                if (better(z, v, bz, bi)) { bz = z; bi = v; }
+    for (int g = 0; g < kGroups; ++g) {
+        const int q = lo / 4 + threadIdx.x + g * kThreads;
+        const float4 x = xs[g];
+        if (4 * q < hi && fmaxf(fmaxf(x.x, x.y), fmaxf(x.z, x.w)) >= lim) {
+            const uint4 d = noise_draws(seed, b, pos, (uint32_t)q);
+            const float z[4] = {x.x + gumbel_of(d.x), x.y + gumbel_of(d.y), x.z + gumbel_of(d.z),
+                                x.w + gumbel_of(d.w)};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int v = 4 * q + j;
+                if (v < hi && better(z[j], v, bz, bi)) { bz = z[j]; bi = v; }
             }
         }
     }
@@ -66,7 +117,6 @@ sample_part_kernel(const float* __restrict__ logits, int Kmax, int V, int S, flo
     }
     __shared__ float sz[kThreads / 32];
     __shared__ int si[kThreads / 32];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     if (lane == 0) { sz[warp] = bz; si[warp] = bi; }
     __syncthreads();
     if (warp == 0) {
