@@ -475,15 +475,19 @@ attn_tc_kernel(const __grid_constant__ Maps maps, AttnArgs a) {
             // stage this thread's row, 16-byte chunks permuted by the row index so a warp's
             // 32 rows spread over all banks
             uint8_t* srow = gbase + OFF_STAGE + r * (direct ? 256 : 512);
-            for (int c0 = 0; c0 < HD; c0 += 32) {
-                float o[32];
-                if (nb > 0) {
-                    tmem_ld32(tmem + lane_base + TM_O + c0, o);
-                    tmem_wait_ld();
-                } else {
+            // the row's 128 columns in one round of TMEM loads (the scores' registers are free now)
+            float ob[HD];
+            if (nb > 0) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = 0.f;  // no block ran: O was never written
-                }
+                for (int c0 = 0; c0 < HD; c0 += 32) tmem_ld32(tmem + lane_base + TM_O + c0, ob + c0);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int i = 0; i < HD; ++i) ob[i] = 0.f;  // no block ran: O was never written
+            }
+#pragma unroll
+            for (int c0 = 0; c0 < HD; c0 += 32) {
+                const float* o = ob + c0;
                 if (direct) {
 #pragma unroll
                     for (int i = 0; i < 32; i += 8) {
